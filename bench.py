@@ -1,0 +1,557 @@
+#!/usr/bin/env python3
+"""Benchmark of the int4 group-quantized decode matvec path on GB300.
+
+One step = one decode step of a 7B-shaped stack of 32 layers at M lanes
+(default M = 1), each layer four calls through the C ABI:
+
+    quad   : QKV 4096 -> 4096 + 1024 + 1024 (routed to q, k, v)
+    matvec : O 4096 -> 4096 on q (a stand-in for the attention output)
+    gated  : gate/up 4096 -> 2 x 11008 with the residual + RMSNorm prologue
+             x = h + o, a = RMSNorm(x) * W_norm (writes residual_out = x)
+    matvec : down 11008 -> 4096; its output is the next layer's h
+
+with int4 weights at group size 128 (3.19 GB of packed weights, scales and
+zeros per step, every step streams them from HBM: the working set is far
+larger than the 129 MB L2).  Weights and inputs are seeded synthetic data.
+
+Output: one JSON line (metric, value in GB/s of algorithmic bytes, roofline
+of the dominant kernel, CPU oracle baseline, end-to-end through the API).
+``--impl reference`` times the plain C oracle on the host instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "int4 matvec HBM GB/s and % of GB300 peak; 7B-stack decode µs/step at M=1"
+HIDDEN, FFN, GS = 4096, 11008, 128
+QKV = (4096, 1024, 1024)
+EPS = 1e-6
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes: K*N/2 + 8*N*K/gs per matrix + activations + outputs (f32)
+# ---------------------------------------------------------------------------
+
+def matrix_bytes(K, N, gs=GS):
+    return K * N // 2 + 8 * N * (K // gs)
+
+
+def layer_call_bytes(M):
+    """Algorithmic bytes of the four calls of one layer at M lanes."""
+    nq = sum(QKV)
+    f = 4 * M  # bytes per f32 element per lane
+    return {
+        "quad": matrix_bytes(HIDDEN, nq) + f * HIDDEN + f * nq,
+        "o": matrix_bytes(HIDDEN, HIDDEN) + f * HIDDEN + f * HIDDEN,
+        # A, A_b, W_norm, residual_out, out
+        "gated": 2 * matrix_bytes(HIDDEN, FFN) + 3 * f * HIDDEN + 4 * HIDDEN + f * FFN,
+        "down": matrix_bytes(FFN, HIDDEN) + f * FFN + f * HIDDEN,
+    }
+
+
+def step_bytes(M, layers):
+    return layers * sum(layer_call_bytes(M).values())
+
+
+# ---------------------------------------------------------------------------
+# Distributed helpers (replicas: each rank runs its own stack)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="gq4_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        busy = [s for s in sm if smax and s >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Peaks and profile-derived traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_group_quantized_quant_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernels are unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not m_bytes or not m_hash or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+# ---------------------------------------------------------------------------
+# The device-resident stack
+# ---------------------------------------------------------------------------
+
+class Stack:
+    def __init__(self, gq4, layers: int, M: int, seed: int = 4):
+        import torch
+        from int4_group_quantized_quant_gb300 import inputs as I
+        self.gq4 = gq4
+        self.M = M
+        self.layers = []
+        dev = torch.device("cuda")
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).to(dev)
+
+        for li in range(layers):
+            L = I.stack_layer(li, seed)
+            self.layers.append({k: (up(v.Bq), up(v.scales), up(v.zeros)) if k != "W_norm" else up(v)
+                                for k, v in L.items()})
+        f32 = dict(dtype=torch.float32, device=dev)
+        nq = sum(QKV)
+        self.h0 = up(I.stack_input(M, seed))
+        self.q = torch.empty((M, QKV[0]), **f32)
+        self.k = torch.empty((M, QKV[1]), **f32)
+        self.v = torch.empty((M, QKV[2]), **f32)
+        self.o = torch.empty((M, HIDDEN), **f32)
+        self.res = torch.empty((M, HIDDEN), **f32)
+        self.f = torch.empty((M, FFN), **f32)
+        # ping-pong residual-stream buffers: down output of layer l is h of layer l+1
+        self.hbuf = [torch.empty((M, HIDDEN), **f32) for _ in range(2)]
+        self.n0, self.n1, self.n2 = QKV[0], QKV[0] + QKV[1], nq
+
+    def launches_per_step(self):
+        return 4 * len(self.layers)
+
+    def layer(self, li, h, h_next, stream):
+        gq4, L = self.gq4, self.layers[li]
+        gq4.quad_matvec(h, *L["qkv"], GS, self.n0, self.n1, self.n2,
+                        outs=[self.q, self.k, self.v, None], stream=stream)
+        gq4.matvec(self.q, *L["o"], GS, C=self.o, stream=stream)
+        gq4.gated_matvec(h, *L["gate"], *L["up"], GS, W_norm=L["W_norm"], eps=EPS, A_b=self.o,
+                         residual_out=self.res, out=self.f, stream=stream)
+        gq4.matvec(self.f, *L["down"], GS, C=h_next, stream=stream)
+
+    def step(self, stream):
+        h = self.h0
+        for li in range(len(self.layers)):
+            h_next = self.hbuf[li % 2]
+            self.layer(li, h, h_next, stream)
+            h = h_next
+        return h
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist_init(world, "nccl")
+    from int4_group_quantized_quant_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    barrier(world)
+    from int4_group_quantized_quant_gb300 import gq4
+
+    M, layers = args.lanes, args.layers
+    stack = Stack(gq4, layers, M)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # warm-up (eager), then capture one step into a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            out = stack.step(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        out = stack.step(torch.cuda.current_stream())
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, events on the replay stream ----
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, device="cuda")
+    ms_step = ms_max / args.steps
+
+    # ---- roofline: average launch duration of the dominant kernel ----
+    # the gated gate/up call with its norm prologue (about half the step's bytes),
+    # launched alone over the layers' distinct weights, events on its stream
+    durs = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.roofline_rounds):
+            for li in range(layers):
+                L = stack.layers[li]
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                gq4.gated_matvec(stack.h0, *L["gate"], *L["up"], GS, W_norm=L["W_norm"], eps=EPS,
+                                 A_b=stack.o, residual_out=stack.res, out=stack.f, stream=stream)
+                e1.record(stream)
+                durs.append((e0, e1))
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    gated_ms = [a.elapsed_time(b_) for a, b_ in durs]
+    gated_avg_s = statistics.mean(gated_ms) / 1e3
+    gated_bytes = layer_call_bytes(M)["gated"]
+
+    # ---- end to end through the API: pinned H2D of h, replay, D2H of the output ----
+    h_host = torch.empty_like(stack.h0, device="cpu").pin_memory()
+    h_host.copy_(stack.h0.cpu())
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    e2e_steps = args.steps
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            stack.h0.copy_(h_host, non_blocking=True)
+            graph.replay()
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+    t1 = time.perf_counter()
+    e2e_s = max_over_ranks((t1 - t0) / e2e_steps, world, device="cuda")
+
+    sbytes = step_bytes(M, layers)
+    value = world * sbytes / (ms_step / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+    achieved = gated_bytes / gated_avg_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; int4 codes uniform 0..15, scales U[0.005,0.02], zeros U[6,9], "
+                "activations N(0,1), norm gain U[0.5,1.5])",
+        "config": {
+            "workload": f"7B-shaped decode layer stack, {layers} layers, int4 group 128, M={M}",
+            "lanes": M, "layers": layers, "hidden": HIDDEN, "ffn": FFN, "qkv": list(QKV),
+            "group_size": GS, "bytes_per_step": sbytes,
+            "l2": "inputs larger than L2: each step streams 3.2 GB of weights (L2 129 MB)",
+            "timing": "CUDA graph of one step, replayed; CUDA events on the replay stream",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "kernel": "gq4 gated gate/up + RMSNorm prologue, 4096 -> 2 x 11008 (fp32 CUDA-core)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic("gated_norm_4096x2x11008_M1"),
+            "bytes_per_launch": gated_bytes,
+            "avg_launch_us": round(gated_avg_s * 1e6, 3),
+            "launches_timed": len(gated_ms),
+        },
+        "e2e": {
+            "value": round(world * sbytes / e2e_s / 1e9, 2),
+            "unit": "GB/s",
+            "us_per_step": round(e2e_s * 1e6, 2),
+            "h2d_bytes_per_step": int(stack.h0.numel() * 4),
+            "d2h_bytes_per_step": int(out.numel() * 4),
+            "how": "pinned host h -> device, graph replay of the step's C-ABI calls, "
+                   "output -> pinned host, stream sync; host wall clock",
+        },
+        "gpu_launches": args.steps * stack.launches_per_step(),
+        "clocks": clock_info,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(M, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_layer(orc, L, h, M):
+    """One layer through the C oracle (same data flow as the GPU step)."""
+    n0, n1, n2 = QKV[0], QKV[0] + QKV[1], sum(QKV)
+    outs, _ = orc.quad_matvec(h, L["qkv"].Bq, L["qkv"].scales, L["qkv"].zeros, HIDDEN, n2, GS,
+                              n0, n1, n2)
+    q = outs[0].astype(np.float32)
+    o, _ = orc.matvec(q, L["o"].Bq, L["o"].scales, L["o"].zeros, HIDDEN, HIDDEN, GS)
+    g = orc.gated_matvec(h, L["gate"].Bq, L["gate"].scales, L["gate"].zeros, L["up"].Bq,
+                         L["up"].scales, L["up"].zeros, HIDDEN, FFN, GS,
+                         A_b=o.astype(np.float32), W_norm=L["W_norm"], eps=EPS)
+    d, _ = orc.matvec(g["out"].astype(np.float32), L["down"].Bq, L["down"].scales,
+                      L["down"].zeros, FFN, HIDDEN, GS)
+    return d.astype(np.float32)
+
+
+def cpu_baseline(M, seconds):
+    """The oracle as it stands on the host, over whole layers until ~seconds of CPU work."""
+    import oracle
+    from int4_group_quantized_quant_gb300 import inputs as I
+    orc = oracle.load()
+    h = I.stack_input(M)
+    done, t_total, li = 0, 0.0, 0
+    while True:
+        L = I.stack_layer(li)
+        t0 = time.perf_counter()
+        h = oracle_layer(orc, L, h, M)
+        t_total += time.perf_counter() - t0
+        done += 1
+        li += 1
+        if t_total >= seconds or li >= 32:
+            break
+    sbytes = done * sum(layer_call_bytes(M).values())
+    return {"value": round(sbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{done} of 32 layers of the same stack at M={M} (4 calls each), "
+                      f"single-threaded C fp64 oracle, {t_total:.1f} s",
+            "us_per_layer": round(t_total / done * 1e6, 1)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from int4_group_quantized_quant_gb300 import inputs as I
+    orc = oracle.load()
+    M = args.lanes
+    h = I.stack_input(M)
+    li = 0
+    # warm-up layers (untimed), then K timed steps of one layer each (a bounded sample)
+    for _ in range(args.warmup):
+        h = oracle_layer(orc, I.stack_layer(li % args.layers), h, M)
+        li += 1
+    t_total = 0.0
+    for _ in range(args.steps):
+        L = I.stack_layer(li % args.layers)
+        t0 = time.perf_counter()
+        h = oracle_layer(orc, L, h, M)
+        t_total += time.perf_counter() - t0
+        li += 1
+    lbytes = sum(layer_call_bytes(M).values())
+    value = args.steps * lbytes / t_total / 1e9
+    sample = (f"{args.steps} timed layers (of the {args.layers}-layer stack) at M={M}, 4 calls "
+              f"each, single-threaded C fp64 oracle")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded, same generator and distributions as the GPU arm)",
+        "config": {"workload": f"7B-shaped decode layer stack, {args.layers} layers, int4 group "
+                               f"128, M={M}", "lanes": M, "layers": args.layers,
+                   "step": "one layer (bounded sample)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Profile cases (small, for ncu): a few launches of one kernel
+# ---------------------------------------------------------------------------
+
+def run_profile_case(args):
+    import torch
+    from int4_group_quantized_quant_gb300 import build as b
+    b.build()
+    from int4_group_quantized_quant_gb300 import gq4
+    torch.cuda.set_device(0)
+    stack = Stack(gq4, args.layers, args.lanes)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.steps):
+        for li in range(args.layers):
+            if args.profile == "step":
+                stack.layer(li, stack.h0, stack.hbuf[0], stream)
+            elif args.profile == "gated":
+                L = stack.layers[li]
+                gq4.gated_matvec(stack.h0, *L["gate"], *L["up"], GS, W_norm=L["W_norm"], eps=EPS,
+                                 A_b=stack.o, residual_out=stack.res, out=stack.f, stream=stream)
+            elif args.profile == "down":
+                L = stack.layers[li]
+                gq4.matvec(stack.f, *L["down"], GS, C=stack.hbuf[0], stream=stream)
+            elif args.profile == "quad":
+                L = stack.layers[li]
+                gq4.quad_matvec(stack.h0, *L["qkv"], GS, stack.n0, stack.n1, stack.n2,
+                                outs=[stack.q, stack.k, stack.v, None], stream=stream)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile, "layers": args.layers, "lanes": args.lanes,
+                      "launch_rounds": args.steps}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--lanes", type=int, default=1, help="decode lanes M (1..32)")
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--roofline-rounds", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["gated", "down", "quad", "step"], default=None,
+                    help="run a small launch sequence of one kernel for ncu (no timing)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and args.profile is None:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    rank, world, local_rank = dist_env()
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

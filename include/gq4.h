@@ -1,0 +1,161 @@
+/*
+ * gq4.h -- C ABI of libgq4: the int4 weight-only group-quantized
+ * matrix-vector product used in LLM token decode, with its fused variants,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Source of the operations (gerbil 1.12.0 -> 1.13.0 bundle diffs):
+ *   - format and dequant rule: moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4
+ *     main loop; gpu bundle, Gepard graph builder `addLinearOp` (tensors
+ *     `.q` u32, `.scales` / `.zeros` f32); executor declarations,
+ *     `fuseMambaFrontDecodeEntries` doc (weights column-major, one column
+ *     contiguous);
+ *   - quad routing: WGSL_QUAD_MATVEC_INT4 epilogue and QUAD_MATVEC_INT4_SPEC
+ *     (bindings A, B_q, scales, zeros, out0..out3, params {K, N, group_size,
+ *     n0, n1, n2});
+ *   - RMSNorm prologue: WGSL_NORM_MATVEC_INT4 and NORM_MATVEC_INT4_SPEC
+ *     (bindings A_a, A_b, W_norm, B_q, scales, zeros, C, residual_out,
+ *     norm_out, params {K, N, group_size, eps});
+ *   - SiLU-gated gate/up: executor declarations, fuseSwiGLUDecodeEntries and
+ *     fuseNormSwiGLUDecodeEntries docs (silu(gate) * up, optional residual +
+ *     RMSNorm prologue);
+ *   - batched lanes: executor declarations, buildBatchEntries doc (lanes run
+ *     the same weights and never interact).
+ *
+ * ---------------------------------------------------------------------------
+ * Weight format (one int4 matrix of K inputs and N output columns, group size
+ * gs, G = K / gs groups per column):
+ *   Bq      u32 [N][K/8]   column n owns words n*K/8 .. n*K/8 + K/8 - 1;
+ *                          element k of column n is bits 4*(k%8) .. 4*(k%8)+3
+ *                          of word k/8 (low nibble first), a code q in 0..15.
+ *   scales  f32 [N][G]     one per (column, group of gs consecutive k).
+ *   zeros   f32 [N][G]     one per (column, group); need not be an integer.
+ *   w(n,k) = (q(n,k) - zeros[n][k/gs]) * scales[n][k/gs].
+ * Activations A are f32 [M][K] (lane-major), outputs f32 [M][len].
+ * C[m][n] = sum_k A[m][k] * w(n,k).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller; the caller keeps
+ *     the buffers alive until the stream has passed the call.  The library
+ *     allocates no memory, keeps no global state and never synchronizes.
+ *   - All checks run on the host before anything is enqueued.  A status other
+ *     than GQ4_OK means nothing was enqueued on the stream.  GQ4_ERR_CUDA
+ *     means a launch was rejected by the CUDA runtime (cudaGetLastError);
+ *     errors raised later by the kernel surface on the stream as usual.
+ *   - Shape rules: 1 <= M <= GQ4_MAX_LANES, K > 0, N > 0,
+ *     group_size % 32 == 0, K % group_size == 0.  (Every element group then
+ *     holds whole 32-code / 16-byte chunks, the unit of the 128-bit loads.)
+ *   - Alignment: Bq, A and every [M][K] vector 16-byte aligned; scales, zeros
+ *     and outputs 4-byte aligned.  Otherwise GQ4_ERR_MISALIGNED.
+ *   - Outputs must not overlap each other or any input (GQ4_ERR_ALIAS).
+ *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
+ *   - Results are deterministic: the same inputs give the same bits.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef GQ4_H
+#define GQ4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQ4_MAX_LANES 32
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define GQ4_API __attribute__((visibility("default")))
+#else
+#define GQ4_API
+#endif
+
+typedef enum gq4_status {
+    GQ4_OK = 0,
+    GQ4_ERR_INVALID_ARG = 1, /* a shape rule or a required pointer is violated */
+    GQ4_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+    GQ4_ERR_ALIAS = 3,       /* an output overlaps another output or an input */
+    GQ4_ERR_CUDA = 4,        /* the CUDA runtime rejected a launch */
+    GQ4_ERR_MISALIGNED = 5   /* a pointer breaks its alignment rule */
+} gq4_status;
+
+/* Optional residual + RMSNorm prologue (WGSL_NORM_MATVEC_INT4 prologue):
+ *   x[m][k]   = A[m][k] + A_b[m][k]                (A_b == NULL: x = A)
+ *   inv_rms   = 1 / sqrt(sum_k x[m][k]^2 / K + eps)
+ *   a[m][k]   = x[m][k] * inv_rms * W_norm[k]      (the matvec activation)
+ * residual_out[m][k] = x (bit-exact f32 sum) and norm_out[m][k] = a are
+ * written for every lane when non-NULL. */
+typedef struct gq4_norm {
+    const float *A_b;     /* [M][K] second addend, or NULL */
+    const float *W_norm;  /* [K] gain, required */
+    float eps;            /* e.g. 1e-6f; must be >= 0 */
+    float *residual_out;  /* [M][K] or NULL */
+    float *norm_out;      /* [M][K] or NULL */
+} gq4_norm;
+
+/* Plain matvec (the base decode MatMulInt4): C [M][N]. */
+GQ4_API gq4_status gq4_matvec(int M, int K, int N, int group_size,
+                      const float *A, const uint32_t *Bq,
+                      const float *scales, const float *zeros,
+                      float *C, cudaStream_t stream);
+
+/* Quad-output matvec over a column-concatenated weight matrix (the byte
+ * append of up to four projections sharing A, K and group_size).  Column
+ * col goes to out0[m][col] (col < n0), out1[m][col-n0] (n0 <= col < n1),
+ * out2[m][col-n1] (n1 <= col < n2) or out3[m][col-n2] (col >= n2).
+ * Requires 0 <= n0 <= n1 <= n2 <= N; out_i is [M][len_i] with
+ * len = {n0, n1-n0, n2-n1, N-n2} and may be NULL exactly when len_i == 0.
+ * Each column's value is bit-identical to gq4_matvec on the same weights. */
+GQ4_API gq4_status gq4_quad_matvec(int M, int K, int N, int group_size,
+                           int n0, int n1, int n2,
+                           const float *A, const uint32_t *Bq,
+                           const float *scales, const float *zeros,
+                           float *out0, float *out1, float *out2, float *out3,
+                           cudaStream_t stream);
+
+/* Norm-prologue matvec: C [M][N] = matvec of the RMSNorm prologue of A
+ * (+ norm->A_b).  norm must be non-NULL with W_norm set. */
+GQ4_API gq4_status gq4_norm_matvec(int M, int K, int N, int group_size,
+                           const gq4_norm *norm,
+                           const float *A, const uint32_t *Bq,
+                           const float *scales, const float *zeros,
+                           float *C, cudaStream_t stream);
+
+/* SiLU-gated gate/up matvec: out[m][n] = silu(g) * u with
+ * g = a . w_gate(n, .), u = a . w_up(n, .), silu(t) = t / (1 + exp(-t)).
+ * Both matrices are K x N with the same group_size.  a = A, or the RMSNorm
+ * prologue of A when norm != NULL (applied once, shared by both). */
+GQ4_API gq4_status gq4_gated_matvec(int M, int K, int N, int group_size,
+                            const gq4_norm *norm, const float *A,
+                            const uint32_t *Bq_gate, const float *scales_gate,
+                            const float *zeros_gate,
+                            const uint32_t *Bq_up, const float *scales_up,
+                            const float *zeros_up,
+                            float *out, cudaStream_t stream);
+
+/* Integer unpack test kernel: q[n*K + k] = q(n,k) as u8 [N][K].
+ * Uses the same in-register extraction as the matvec kernels.
+ * Requires K % 32 == 0. */
+GQ4_API gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q,
+                      cudaStream_t stream);
+
+/* Dequant test kernel: W[n*K + k] = fl32(fl32(q - zero) * scale) as f32
+ * [N][K], one rounding per operation, through the same extraction as the
+ * matvec kernels. */
+GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
+                       const float *scales, const float *zeros, float *W,
+                       cudaStream_t stream);
+
+/* Static description of a status code. */
+GQ4_API const char *gq4_status_string(gq4_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+GQ4_API int gq4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ4_H */

@@ -1,0 +1,300 @@
+// gq4_api.cu -- the extern "C" entry points of libgq4 (declared in gq4.h).
+//
+// Every entry point validates its arguments on the host, synchronously,
+// before anything is enqueued; a non-OK status means the stream is untouched.
+// The checks mirror the pages' preconditions: the quad and norm fusion passes
+// of the gerbil executor refuse to fuse when an output buffer aliases an
+// input or another output (fuseMambaFrontDecodeEntries,
+// fuseNormMatVecDecodeEntries), and the WGSL kernels assume K and the group
+// size are whole multiples of the 32-code vec4u load.
+#include <cstdint>
+#include <cstring>
+
+#include "gq4.h"
+#include "gq4_internal.h"
+
+namespace {
+
+constexpr int kMaxK = 1 << 24;  // keeps 32-code chunk indices below 2^20
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void *p, size_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+
+bool overlap(Range a, Range b)
+{
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Collects the byte ranges of a call and checks them.
+struct RangeSet {
+    Range in[16];
+    int n_in = 0;
+    Range out[8];
+    int n_out = 0;
+    void input(const void *p, size_t bytes)
+    {
+        if (p && bytes) in[n_in++] = range_of(p, bytes);
+    }
+    void output(const void *p, size_t bytes)
+    {
+        if (p && bytes) out[n_out++] = range_of(p, bytes);
+    }
+    bool disjoint() const
+    {
+        for (int i = 0; i < n_out; ++i) {
+            for (int j = 0; j < n_in; ++j)
+                if (overlap(out[i], in[j])) return false;
+            for (int j = i + 1; j < n_out; ++j)
+                if (overlap(out[i], out[j])) return false;
+        }
+        return true;
+    }
+};
+
+gq4_status check_shape(int M, int K, int N, int gs)
+{
+    if (M < 1 || M > GQ4_MAX_LANES) return GQ4_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || gs <= 0) return GQ4_ERR_INVALID_ARG;
+    if (K > kMaxK) return GQ4_ERR_INVALID_ARG;
+    if (gs % 32 != 0 || K % gs != 0) return GQ4_ERR_INVALID_ARG;
+    return GQ4_OK;
+}
+
+// One int4 matrix: pointers present, Bq 16-byte aligned, scales/zeros 4-byte.
+gq4_status check_weights(const uint32_t *Bq, const float *s, const float *z, int K, int N, int gs,
+                         RangeSet &rs)
+{
+    if (!Bq || !s || !z) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(Bq, 16) || !aligned(s, 4) || !aligned(z, 4)) return GQ4_ERR_MISALIGNED;
+    const size_t n = (size_t)N;
+    rs.input(Bq, n * (size_t)K / 2);
+    rs.input(s, n * (size_t)(K / gs) * sizeof(float));
+    rs.input(z, n * (size_t)(K / gs) * sizeof(float));
+    return GQ4_OK;
+}
+
+gq4_status check_norm(const gq4_norm *norm, int M, int K, RangeSet &rs)
+{
+    if (!norm->W_norm) return GQ4_ERR_INVALID_ARG;
+    if (!(norm->eps >= 0.0f)) return GQ4_ERR_INVALID_ARG;  // also rejects NaN
+    const size_t mk = (size_t)M * (size_t)K * sizeof(float);
+    if (!aligned(norm->W_norm, 16) || (norm->A_b && !aligned(norm->A_b, 16)) ||
+        (norm->residual_out && !aligned(norm->residual_out, 16)) ||
+        (norm->norm_out && !aligned(norm->norm_out, 16)))
+        return GQ4_ERR_MISALIGNED;
+    rs.input(norm->A_b, mk);
+    rs.input(norm->W_norm, (size_t)K * sizeof(float));
+    rs.output(norm->residual_out, mk);
+    rs.output(norm->norm_out, mk);
+    return GQ4_OK;
+}
+
+gq4_status check_activation(const float *A, int M, int K, RangeSet &rs)
+{
+    if (!A) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(A, 16)) return GQ4_ERR_MISALIGNED;
+    rs.input(A, (size_t)M * (size_t)K * sizeof(float));
+    return GQ4_OK;
+}
+
+gq4_status check_output(const float *out, size_t elems, RangeSet &rs)
+{
+    if (elems == 0) return GQ4_OK;
+    if (!out) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return GQ4_ERR_MISALIGNED;
+    rs.output(out, elems * sizeof(float));
+    return GQ4_OK;
+}
+
+#define GQ4_TRY(expr)                       \
+    do {                                    \
+        const gq4_status st_ = (expr);      \
+        if (st_ != GQ4_OK) return st_;      \
+    } while (0)
+
+gq4_status run(const gq4::Call &call, cudaStream_t stream)
+{
+    const cudaError_t err = gq4::launch_fp32(call, stream);
+    return err == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
+}
+
+gq4::Call base_call(int M, int K, int N, int gs, const float *A)
+{
+    gq4::Call c;
+    std::memset(&c, 0, sizeof(c));
+    c.M = M;
+    c.K = K;
+    c.N = N;
+    c.gs = gs;
+    c.A = A;
+    c.nmat = 1;
+    c.seg_start[0] = 0;
+    c.seg_start[1] = c.seg_start[2] = c.seg_start[3] = N;
+    c.seg_len[0] = N;
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+gq4_status gq4_matvec(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
+                      const float *scales, const float *zeros, float *C, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    if (!C) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    gq4::Call call = base_call(M, K, N, group_size, A);
+    call.Bq[0] = Bq;
+    call.scales[0] = scales;
+    call.zeros[0] = zeros;
+    call.epi = gq4::kEpiStore;
+    call.out[0] = C;
+    return run(call, stream);
+}
+
+gq4_status gq4_quad_matvec(int M, int K, int N, int group_size, int n0, int n1, int n2,
+                           const float *A, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *out0, float *out1, float *out2,
+                           float *out3, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    if (!(0 <= n0 && n0 <= n1 && n1 <= n2 && n2 <= N)) return GQ4_ERR_INVALID_ARG;
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    const int start[4] = {0, n0, n1, n2};
+    const int len[4] = {n0, n1 - n0, n2 - n1, N - n2};
+    float *const outs[4] = {out0, out1, out2, out3};
+    for (int i = 0; i < 4; ++i) GQ4_TRY(check_output(outs[i], (size_t)M * (size_t)len[i], rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    gq4::Call call = base_call(M, K, N, group_size, A);
+    call.Bq[0] = Bq;
+    call.scales[0] = scales;
+    call.zeros[0] = zeros;
+    call.epi = gq4::kEpiQuad;
+    for (int i = 0; i < 4; ++i) {
+        call.out[i] = outs[i];
+        call.seg_start[i] = start[i];
+        call.seg_len[i] = len[i];
+    }
+    return run(call, stream);
+}
+
+gq4_status gq4_norm_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
+                           const float *A, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *C, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    if (!norm) return GQ4_ERR_INVALID_ARG;
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    GQ4_TRY(check_norm(norm, M, K, rs));
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    if (!C) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    gq4::Call call = base_call(M, K, N, group_size, A);
+    call.norm = norm;
+    call.Bq[0] = Bq;
+    call.scales[0] = scales;
+    call.zeros[0] = zeros;
+    call.epi = gq4::kEpiStore;
+    call.out[0] = C;
+    return run(call, stream);
+}
+
+gq4_status gq4_gated_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
+                            const float *A, const uint32_t *Bq_gate, const float *scales_gate,
+                            const float *zeros_gate, const uint32_t *Bq_up,
+                            const float *scales_up, const float *zeros_up, float *out,
+                            cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    if (norm) GQ4_TRY(check_norm(norm, M, K, rs));
+    GQ4_TRY(check_weights(Bq_gate, scales_gate, zeros_gate, K, N, group_size, rs));
+    GQ4_TRY(check_weights(Bq_up, scales_up, zeros_up, K, N, group_size, rs));
+    if (!out) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(out, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    gq4::Call call = base_call(M, K, N, group_size, A);
+    call.norm = norm;
+    call.nmat = 2;
+    call.Bq[0] = Bq_gate;
+    call.scales[0] = scales_gate;
+    call.zeros[0] = zeros_gate;
+    call.Bq[1] = Bq_up;
+    call.scales[1] = scales_up;
+    call.zeros[1] = zeros_up;
+    call.epi = gq4::kEpiGated;
+    call.out[0] = out;
+    return run(call, stream);
+}
+
+gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream)
+{
+    if (K <= 0 || N <= 0 || K % 32 != 0 || K > kMaxK) return GQ4_ERR_INVALID_ARG;
+    if (!Bq || !q) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(Bq, 16) || !aligned(q, 4)) return GQ4_ERR_MISALIGNED;
+    const size_t nk = (size_t)N * (size_t)K;
+    if (overlap(range_of(Bq, nk / 2), range_of(q, nk))) return GQ4_ERR_ALIAS;
+    return gq4::launch_unpack(K, N, Bq, q, stream) == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
+}
+
+gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const float *scales,
+                       const float *zeros, float *W, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(1, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    if (!W) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(W, 4)) return GQ4_ERR_MISALIGNED;
+    rs.output(W, (size_t)N * (size_t)K * sizeof(float));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    return gq4::launch_dequant(K, N, group_size, Bq, scales, zeros, W, stream) == cudaSuccess
+               ? GQ4_OK
+               : GQ4_ERR_CUDA;
+}
+
+const char *gq4_status_string(gq4_status status)
+{
+    switch (status) {
+    case GQ4_OK: return "ok";
+    case GQ4_ERR_INVALID_ARG: return "invalid argument";
+    case GQ4_ERR_UNSUPPORTED: return "unsupported";
+    case GQ4_ERR_ALIAS: return "output overlaps an input or another output";
+    case GQ4_ERR_CUDA: return "CUDA launch error";
+    case GQ4_ERR_MISALIGNED: return "misaligned pointer";
+    }
+    return "unknown status";
+}
+
+int gq4_version(void)
+{
+    return 100;  // 0.1.0
+}
+
+}  // extern "C"

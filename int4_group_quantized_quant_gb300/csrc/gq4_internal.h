@@ -1,0 +1,42 @@
+// gq4_internal.h -- host-side interface between the C ABI and the launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "gq4.h"
+
+namespace gq4 {
+
+enum Epilogue : int {
+    kEpiStore = 0,  // C[m][col]
+    kEpiQuad = 1,   // route col to out0..out3 at the split points
+    kEpiGated = 2,  // out[m][col] = silu(gate) * up
+};
+
+// One validated call, as the launchers see it.
+struct Call {
+    int M, K, N, gs;
+    const float *A;
+    const gq4_norm *norm;  // NULL: no prologue
+    int nmat;              // 1, or 2 for gate/up
+    const uint32_t *Bq[2];
+    const float *scales[2];
+    const float *zeros[2];
+    int epi;
+    float *out[4];
+    int seg_start[4];
+    int seg_len[4];
+};
+
+// CUDA-core fp32 path (any M <= GQ4_MAX_LANES).
+cudaError_t launch_fp32(const Call &call, cudaStream_t stream);
+
+// Test kernels.
+cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream);
+cudaError_t launch_dequant(int K, int N, int gs, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *W, cudaStream_t stream);
+
+}  // namespace gq4

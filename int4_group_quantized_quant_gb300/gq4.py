@@ -1,0 +1,225 @@
+"""Thin Python binding over the libgq4 C ABI (``include/gq4.h``).
+
+Argument marshalling only: each function checks that the torch tensors it is
+given are CUDA, contiguous and of the right dtype and shape, then passes their
+device pointers and the current CUDA stream to the C entry point of the same
+name.  Every step of the computation runs in the library's sm_103a kernels.
+There is no CPU fallback: importing this module raises if ``libgq4.so`` has
+not been built (``python -m int4_group_quantized_quant_gb300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgq4.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -m int4_group_quantized_quant_gb300.build)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+MAX_LANES = 32
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_ALIAS = 3
+ERR_CUDA = 4
+ERR_MISALIGNED = 5
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+class Norm(ctypes.Structure):
+    """``gq4_norm``: the optional residual + RMSNorm prologue."""
+    _fields_ = [("A_b", _vp), ("W_norm", _vp), ("eps", ctypes.c_float),
+                ("residual_out", _vp), ("norm_out", _vp)]
+
+
+_NormP = ctypes.POINTER(Norm)
+
+_SIGS = {
+    "gq4_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_quad_matvec": [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                        _vp, _vp],
+    "gq4_norm_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_gated_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                         _vp],
+    "gq4_unpack": [_i, _i, _vp, _vp, _vp],
+    "gq4_dequant": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _i
+    _fn.argtypes = _args
+lib.gq4_status_string.restype = ctypes.c_char_p
+lib.gq4_status_string.argtypes = [_i]
+lib.gq4_version.restype = _i
+lib.gq4_version.argtypes = []
+
+EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version"]
+
+
+class GQ4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.gq4_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise GQ4Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+_F32 = (torch.float32,)
+_WORDS = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _weights(Bq, scales, zeros, K, group_size, tag=""):
+    N = Bq.shape[0]
+    _need(Bq, "Bq" + tag, _WORDS, (N, K // 8))
+    _need(scales, "scales" + tag, _F32, (N, K // group_size))
+    _need(zeros, "zeros" + tag, _F32, (N, K // group_size))
+    return N
+
+
+def _lanes(A):
+    _need(A, "A", _F32)
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    return A.shape
+
+
+def matvec(A, Bq, scales, zeros, group_size, C=None, stream=None):
+    """C [M, N] = A [M, K] times the int4 matrix (Bq [N, K/8], scales/zeros [N, K/gs])."""
+    M, K = _lanes(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _need(C, "C", _F32, (M, N))
+    _check(lib.gq4_matvec(M, K, N, group_size, _ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros),
+                          _ptr(C), _stream(stream)), "gq4_matvec")
+    return C
+
+
+def quad_matvec(A, Bq, scales, zeros, group_size, n0, n1, n2, outs=None, stream=None):
+    """Quad-output matvec; returns the four segment outputs [M, len_i] (empty ones have 0 columns)."""
+    M, K = _lanes(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    lens = [n0, n1 - n0, n2 - n1, N - n2]
+    if outs is None:
+        outs = [torch.empty((M, max(n, 0)), dtype=torch.float32, device=A.device) for n in lens]
+    ptrs = []
+    for i, (o, n) in enumerate(zip(outs, lens)):
+        if o is None:
+            ptrs.append(None)
+            continue
+        _need(o, f"out{i}", _F32, (M, n) if n >= 0 else None)
+        ptrs.append(_ptr(o) if o.numel() else None)
+    _check(lib.gq4_quad_matvec(M, K, N, group_size, n0, n1, n2, _ptr(A), _ptr(Bq), _ptr(scales),
+                               _ptr(zeros), *ptrs, _stream(stream)), "gq4_quad_matvec")
+    return outs
+
+
+def _norm_struct(M, K, W_norm, eps, A_b, residual_out, norm_out):
+    _need(W_norm, "W_norm", _F32, (K,))
+    for name, t in (("A_b", A_b), ("residual_out", residual_out), ("norm_out", norm_out)):
+        if t is not None:
+            _need(t, name, _F32, (M, K))
+    return Norm(_ptr(A_b), _ptr(W_norm), float(eps), _ptr(residual_out), _ptr(norm_out))
+
+
+def norm_matvec(A, Bq, scales, zeros, group_size, W_norm, eps=1e-6, A_b=None,
+                residual_out=None, norm_out=None, C=None, stream=None):
+    """C = matvec of RMSNorm(A + A_b) * W_norm; optionally writes residual_out / norm_out."""
+    M, K = _lanes(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _need(C, "C", _F32, (M, N))
+    nrm = _norm_struct(M, K, W_norm, eps, A_b, residual_out, norm_out)
+    _check(lib.gq4_norm_matvec(M, K, N, group_size, ctypes.byref(nrm), _ptr(A), _ptr(Bq),
+                               _ptr(scales), _ptr(zeros), _ptr(C), _stream(stream)),
+           "gq4_norm_matvec")
+    return C
+
+
+def gated_matvec(A, Bq_gate, scales_gate, zeros_gate, Bq_up, scales_up, zeros_up, group_size,
+                 W_norm=None, eps=1e-6, A_b=None, residual_out=None, norm_out=None, out=None,
+                 stream=None):
+    """out = silu(a . Wg) * (a . Wu), a = A or RMSNorm(A + A_b) * W_norm when W_norm is given."""
+    M, K = _lanes(A)
+    N = _weights(Bq_gate, scales_gate, zeros_gate, K, group_size, "_gate")
+    if _weights(Bq_up, scales_up, zeros_up, K, group_size, "_up") != N:
+        raise ValueError("gate and up must have the same N")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _need(out, "out", _F32, (M, N))
+    nrm = None
+    if W_norm is not None:
+        nrm = _norm_struct(M, K, W_norm, eps, A_b, residual_out, norm_out)
+    elif A_b is not None or residual_out is not None or norm_out is not None:
+        raise ValueError("A_b / residual_out / norm_out need W_norm")
+    _check(lib.gq4_gated_matvec(M, K, N, group_size, ctypes.byref(nrm) if nrm else None,
+                                _ptr(A), _ptr(Bq_gate), _ptr(scales_gate), _ptr(zeros_gate),
+                                _ptr(Bq_up), _ptr(scales_up), _ptr(zeros_up), _ptr(out),
+                                _stream(stream)), "gq4_gated_matvec")
+    return out
+
+
+def unpack(Bq, K, q=None, stream=None):
+    """Integer unpack test kernel: codes [N, K] uint8."""
+    N = Bq.shape[0]
+    _need(Bq, "Bq", _WORDS, (N, K // 8))
+    if q is None:
+        q = torch.empty((N, K), dtype=torch.uint8, device=Bq.device)
+    _need(q, "q", (torch.uint8,), (N, K))
+    _check(lib.gq4_unpack(K, N, _ptr(Bq), _ptr(q), _stream(stream)), "gq4_unpack")
+    return q
+
+
+def dequant(Bq, scales, zeros, K, group_size, W=None, stream=None):
+    """Dequant test kernel: W [N, K] = fl32(fl32(q - zero) * scale)."""
+    N = _weights(Bq, scales, zeros, K, group_size)
+    if W is None:
+        W = torch.empty((N, K), dtype=torch.float32, device=Bq.device)
+    _need(W, "W", _F32, (N, K))
+    _check(lib.gq4_dequant(K, N, group_size, _ptr(Bq), _ptr(scales), _ptr(zeros), _ptr(W),
+                           _stream(stream)), "gq4_dequant")
+    return W
+
+
+def version() -> int:
+    return int(lib.gq4_version())

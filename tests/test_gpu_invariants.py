@@ -1,0 +1,136 @@
+"""GPU invariants that hold bit for bit by construction of the kernels.
+
+* quad outputs concatenated == the plain matvec on the same weights;
+* lane m of an M-lane call == the one-lane call on row m (CUDA-core path);
+* repeated calls give identical bits;
+* codes equal to integer zero points give exactly 0 at K = 11008;
+* a zero gate gives exactly 0 out of the gated call;
+* the gated call equals silu(matvec(gate)) * matvec(up) within tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_group_quantized_quant_gb300 import inputs as I
+from tests.gpu_util import check_close, dev, gq4_module, host, requires_cuda, tol_fp32, wdev
+
+pytestmark = [pytest.mark.gpu, requires_cuda]
+
+
+@pytest.fixture(scope="module")
+def gq4():
+    return gq4_module()
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_quad_equals_matvec(gq4, M):
+    K, N, gs = 2560, 1000, 64
+    w = I.quant_weights(K, N, gs, 960, M)
+    A = dev(I.activations(M, K, 960, M))
+    C = host(gq4.matvec(A, *wdev(w), gs))
+    for n0, n1, n2 in [(400, 500, 600), (0, 0, 0), (N, N, N), (1, 999, 999), (17, 33, 65)]:
+        outs = gq4.quad_matvec(A, *wdev(w), gs, n0, n1, n2)
+        cat = np.concatenate([host(o) for o in outs], axis=1)
+        assert np.array_equal(cat.view(np.uint32), C.view(np.uint32)), (M, n0, n1, n2)
+
+
+@pytest.mark.parametrize("M", [2, 4, 7, 15])
+def test_lane_equals_solo(gq4, M):
+    K, N, gs = 4096, 130, 128
+    w = I.quant_weights(K, N, gs, 961, M)
+    A = I.activations(M, K, 961, M)
+    C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    for m in range(M):
+        Cm = host(gq4.matvec(dev(A[m:m + 1]), *wdev(w), gs))
+        assert np.array_equal(C[m].view(np.uint32), Cm[0].view(np.uint32)), (M, m)
+
+
+def test_norm_lane_equals_solo(gq4):
+    M, K, N, gs = 6, 1024, 50, 64
+    w = I.quant_weights(K, N, gs, 962)
+    A, A_b = I.activations(M, K, 962), I.activations(M, K, 963)
+    W = I.norm_gain(K, 962)
+    C = host(gq4.norm_matvec(dev(A), *wdev(w), gs, dev(W), 1e-6, A_b=dev(A_b)))
+    for m in range(M):
+        Cm = host(gq4.norm_matvec(dev(A[m:m + 1]), *wdev(w), gs, dev(W), 1e-6,
+                                  A_b=dev(A_b[m:m + 1])))
+        assert np.array_equal(C[m].view(np.uint32), Cm[0].view(np.uint32)), m
+
+
+def test_deterministic(gq4):
+    M, K, N, gs = 4, 4096, 1000, 128
+    w = I.quant_weights(K, N, gs, 963)
+    A = dev(I.activations(M, K, 963))
+    first = host(gq4.matvec(A, *wdev(w), gs))
+    for _ in range(5):
+        again = host(gq4.matvec(A, *wdev(w), gs))
+        assert np.array_equal(first.view(np.uint32), again.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_zero_point_codes_give_exact_zero(gq4, M):
+    K, N, gs = 11008, 70, 128
+    G = K // gs
+    c = I.rng(964, M).integers(0, 16, size=(N, G)).astype(np.uint32)
+    # every code of a group equals the group's integer zero point
+    words = np.repeat(c * np.uint32(0x11111111), gs // 8, axis=1).astype(np.uint32)
+    zeros = c.astype(np.float32)
+    scales = I.uniform_f32((N, G), 0.005, 0.02, 964)
+    A = I.activations(M, K, 964, M)
+    C = host(gq4.matvec(dev(A), dev(words), dev(scales), dev(zeros), gs))
+    assert np.all(C == 0.0), float(np.abs(C).max())
+    # the oracle agrees exactly
+    C_ref, S = oracle.matvec(A, words, scales, zeros, K, N, gs)
+    assert np.all(C_ref == 0.0) and np.all(S == 0.0)
+
+
+def test_zero_gate_gives_zero(gq4):
+    M, K, N, gs = 2, 4096, 300, 128
+    G = K // gs
+    gate_words = np.full((N, K // 8), 0x77777777, np.uint32)
+    gate_zeros = np.full((N, G), 7.0, np.float32)
+    gate_scales = I.uniform_f32((N, G), 0.002, 0.01, 965)
+    wu = I.quant_weights(K, N, gs, 966)
+    A = dev(I.activations(M, K, 965))
+    out = host(gq4.gated_matvec(A, dev(gate_words), dev(gate_scales), dev(gate_zeros),
+                                *wdev(wu), gs))
+    assert np.all(out == 0.0)
+
+
+def test_gated_is_silu_of_matvecs(gq4):
+    M, K, N, gs = 3, 4096, 500, 128
+    wg = I.quant_weights(K, N, gs, 967, scale_range=I.SCALE_RANGE_GATED)
+    wu = I.quant_weights(K, N, gs, 968, scale_range=I.SCALE_RANGE_GATED)
+    A = dev(I.activations(M, K, 967))
+    g = host(gq4.matvec(A, *wdev(wg), gs)).astype(np.float64)
+    u = host(gq4.matvec(A, *wdev(wu), gs)).astype(np.float64)
+    out = host(gq4.gated_matvec(A, *wdev(wg), *wdev(wu), gs)).astype(np.float64)
+    expect = g / (1.0 + np.exp(-g)) * u
+    # same dot products bit for bit; only expf / division / product rounding differ
+    check_close("gated vs composed", out, expect, 4e-7 * np.abs(expect) + 1e-9)
+
+
+def test_nonfinite_activation_propagates(gq4):
+    """An Inf or NaN activation poisons exactly the outputs it feeds (no silent masking)."""
+    M, K, N, gs = 2, 256, 40, 32
+    w = I.quant_weights(K, N, gs, 969)
+    A = I.activations(M, K, 969)
+    A[1, 5] = np.nan
+    C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    assert np.all(np.isfinite(C[0])) and np.all(np.isnan(C[1]))
+
+
+def test_stream_argument(gq4):
+    """Calls run on the stream they are given and respect its ordering."""
+    M, K, N, gs = 1, 1024, 1024, 32
+    w = I.quant_weights(K, N, gs, 970)
+    A = I.activations(M, K, 970)
+    ref = host(gq4.matvec(dev(A), *wdev(w), gs))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Ad = dev(A)
+        out = gq4.matvec(Ad, *wdev(w), gs, stream=s)
+    s.synchronize()
+    assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32))
