@@ -6,25 +6,26 @@
 // it with an integer-to-float instruction, each code is masked IN PLACE and
 // OR-ed with the exponent bits of 2^23:
 //
-//     bits(f_i) = 0x4B000000 | (w & (0xF << 4*p_i))   =>   f_i = 2^23 + 16^p_i * q_i
+//     bits(f) = 0x4B000000 | (x & (0xF << 4p))   =>   f = 2^23 + 16^p * q
 //
-// which is exact for p_i <= 5 (the code stays inside the 23-bit mantissa).
-// Codes 6 and 7 (bits 24..31) are first moved down by 24 bits and then
-// masked at positions 0 and 1.  So the position scale p_i is
+// which is exact while the code stays inside the 23-bit mantissa, i.e. for
+// bit positions 0..19 (p <= 4; bit 23 is already the exponent's lowest bit).
+// Codes 0..3 are masked in w itself, codes 4..7 in t = w >> 16, so every code
+// sits at position p = i % 4:
 //
-//     p = {0, 1, 2, 3, 4, 5, 0, 1}   for codes i = 0..7 of a word,
+//     p = {0, 1, 2, 3, 0, 1, 2, 3}   for codes i = 0..7 of a word,
 //
-// one LOP3 per code (plus one shift per word).  Then
+// one LOP3 per code plus one shift per word.  Then
 //
 //     d_i = (f_i - 2^23) - 16^p_i * zero = 16^p_i * fl(q_i - zero)
 //
 // exactly: f_i - 2^23 is exact, 16^p * zero is exact (a power-of-two scale),
 // and a difference of two values both scaled by 16^p rounds to 16^p times the
 // rounded unscaled difference.  The activation that multiplies code i is
-// pre-scaled by 16^-p_i (also exact), so a * d = a_scaled_back * fl(q - zero)
+// pre-scaled by 16^-p_i (also exact), so a_scaled * d = a * fl(q - zero)
 // exactly inside the FMA.  The fp32 result is therefore bit-identical to an
-// FMA chain over fl(q - zero) * a, with two FP operations per code: one
-// subtraction pair and one FMA, issued as packed f32x2 instructions.
+// FMA chain over fl(q - zero) * a, with two FP operations per code (a
+// subtraction pair and an FMA), issued as packed f32x2 instructions.
 #pragma once
 
 #include <cstdint>
@@ -35,18 +36,13 @@ namespace gq4 {
 constexpr float kMagic = 8388608.0f;
 constexpr uint32_t kMagicBits = 0x4B000000u;
 
-// 16^-p for the eight codes of a word, split into the two float4 halves
-// (codes 0..3 and codes 4..7).
+// 16^-p for code i of a word (p = i % 4); the same for both float4 halves.
 __host__ __device__ constexpr float code_prescale(int i)
 {
-    return i == 0 ? 1.0f
-         : i == 1 ? 0.0625f
-         : i == 2 ? 0.00390625f
-         : i == 3 ? 0.000244140625f
-         : i == 4 ? 1.52587890625e-05f
-         : i == 5 ? 9.5367431640625e-07f
-         : i == 6 ? 1.0f
-                  : 0.0625f;
+    return (i & 3) == 0 ? 1.0f
+         : (i & 3) == 1 ? 0.0625f
+         : (i & 3) == 2 ? 0.00390625f
+                        : 0.000244140625f;
 }
 
 // ---------------------------------------------------------------------------
@@ -90,22 +86,23 @@ struct CodePairs {
 
 __device__ __forceinline__ CodePairs extract_word(uint32_t w)
 {
-    const uint32_t t = w >> 24;
+    const uint32_t t = w >> 16;
     CodePairs c;
-    c.p01 = pack2(__uint_as_float((w & 0x0000000Fu) | kMagicBits),
-                  __uint_as_float((w & 0x000000F0u) | kMagicBits));
-    c.p23 = pack2(__uint_as_float((w & 0x00000F00u) | kMagicBits),
-                  __uint_as_float((w & 0x0000F000u) | kMagicBits));
-    c.p45 = pack2(__uint_as_float((w & 0x000F0000u) | kMagicBits),
-                  __uint_as_float((w & 0x00F00000u) | kMagicBits));
-    c.p67 = pack2(__uint_as_float((t & 0x0000000Fu) | kMagicBits),
-                  __uint_as_float((t & 0x000000F0u) | kMagicBits));
+    c.p01 = pack2(__uint_as_float((w & 0x000Fu) | kMagicBits),
+                  __uint_as_float((w & 0x00F0u) | kMagicBits));
+    c.p23 = pack2(__uint_as_float((w & 0x0F00u) | kMagicBits),
+                  __uint_as_float((w & 0xF000u) | kMagicBits));
+    c.p45 = pack2(__uint_as_float((t & 0x000Fu) | kMagicBits),
+                  __uint_as_float((t & 0x00F0u) | kMagicBits));
+    c.p67 = pack2(__uint_as_float((t & 0x0F00u) | kMagicBits),
+                  __uint_as_float((t & 0xF000u) | kMagicBits));
     return c;
 }
 
-// Zero point scaled to each code position: (z, 16z), (256z, 4096z), (65536z, 2^20 z).
+// Zero point scaled to the code positions: (z, 16z) for p = 0, 1 and
+// (256z, 4096z) for p = 2, 3.
 struct ZeroPairs {
-    f32x2 z01, z23, z45;
+    f32x2 z01, z23;
 };
 
 __device__ __forceinline__ ZeroPairs scaled_zero(float z)
@@ -113,7 +110,6 @@ __device__ __forceinline__ ZeroPairs scaled_zero(float z)
     ZeroPairs r;
     r.z01 = pack2(z, z * 16.0f);
     r.z23 = pack2(z * 256.0f, z * 4096.0f);
-    r.z45 = pack2(z * 65536.0f, z * 1048576.0f);
     return r;
 }
 
@@ -129,8 +125,8 @@ __device__ __forceinline__ DiffPairs code_minus_zero(uint32_t w, const ZeroPairs
     DiffPairs d;
     d.d01 = sub2(sub2(c.p01, magic2), z.z01);
     d.d23 = sub2(sub2(c.p23, magic2), z.z23);
-    d.d45 = sub2(sub2(c.p45, magic2), z.z45);
-    d.d67 = sub2(sub2(c.p67, magic2), z.z01);
+    d.d45 = sub2(sub2(c.p45, magic2), z.z01);
+    d.d67 = sub2(sub2(c.p67, magic2), z.z23);
     return d;
 }
 

@@ -66,16 +66,14 @@ __device__ __forceinline__ int chunk_group(int gc, unsigned long long magic)
     return (int)(((unsigned long long)gc * magic) >> 40);
 }
 
-__device__ __forceinline__ float4 prescale(float4 v, int j)
+__device__ __forceinline__ float4 prescale(float4 v)
 {
-    // float4 j of a chunk covers codes 0..3 (j even) or 4..7 (j odd) of word j/2.
-    if ((j & 1) == 0) {
-        v.x *= code_prescale(0); v.y *= code_prescale(1);
-        v.z *= code_prescale(2); v.w *= code_prescale(3);
-    } else {
-        v.x *= code_prescale(4); v.y *= code_prescale(5);
-        v.z *= code_prescale(6); v.w *= code_prescale(7);
-    }
+    // float4 j of a chunk covers codes 0..3 (j even) or 4..7 (j odd) of word
+    // j/2; both halves sit at code positions p = 0, 1, 2, 3.
+    v.x *= code_prescale(0);
+    v.y *= code_prescale(1);
+    v.z *= code_prescale(2);
+    v.w *= code_prescale(3);
     return v;
 }
 
@@ -193,7 +191,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
                         *reinterpret_cast<float4 *>(p.norm_out + row + k) = v;
                 }
             }
-            s_act[((size_t)m * p.kct + c) * 8 + (j ^ (c & 7))] = prescale(v, j);
+            s_act[((size_t)m * p.kct + c) * 8 + (j ^ (c & 7))] = prescale(v);
         }
         __syncthreads();
 
@@ -378,7 +376,9 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream)
     }
 
     const int MB = call.M == 1 ? 1 : call.M == 2 ? 2 : call.M <= 4 ? 4 : 8;
-    const int kct_max = kSmemBudget / (MB * 8 * (int)sizeof(float4));
+    // K tiles hold a multiple of 32 chunks, so lane l owns chunks l, l+32, ...
+    // in increasing order whatever the tiling (results independent of MB).
+    const int kct_max = kSmemBudget / (MB * 8 * (int)sizeof(float4)) / 32 * 32;
     prm.kct = prm.KC < kct_max ? prm.KC : kct_max;
     prm.n_ktiles = (prm.KC + prm.kct - 1) / prm.kct;
 
