@@ -36,7 +36,8 @@
  * Conventions shared by every entry point:
  *   - Every pointer is a DEVICE pointer owned by the caller; the caller keeps
  *     the buffers alive until the stream has passed the call.  The library
- *     allocates no memory, keeps no global state and never synchronizes.
+ *     allocates no memory and never synchronizes on the call path; its only
+ *     state is one sticky device-side error word (gq4_device_error).
  *   - All checks run on the host before anything is enqueued.  A status other
  *     than GQ4_OK means nothing was enqueued on the stream.  GQ4_ERR_CUDA
  *     means a launch was rejected by the CUDA runtime (cudaGetLastError);
@@ -147,6 +148,14 @@ GQ4_API gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q,
 GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
                        const float *scales, const float *zeros, float *W,
                        cudaStream_t stream);
+
+/* The library's sticky device-side error word on the current device.  Bit 0
+ * is set when a kernel gave up waiting for one of its own bulk copies (every
+ * wait inside the kernels is bounded in time, so a broken copy cannot hang
+ * the GPU; the outputs of that call are then invalid).  Copies the word to
+ * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
+ * the hot path: a diagnostic to call after a suspicious result. */
+GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);
 
 /* Static description of a status code. */
 GQ4_API const char *gq4_status_string(gq4_status status);

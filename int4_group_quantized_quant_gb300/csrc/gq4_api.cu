@@ -127,7 +127,8 @@ gq4_status check_output(const float *out, size_t elems, RangeSet &rs)
 
 gq4_status run(const gq4::Call &call, cudaStream_t stream)
 {
-    const cudaError_t err = gq4::launch_fp32(call, stream);
+    const cudaError_t err = gq4::stream_path_supported(call) ? gq4::launch_stream(call, stream)
+                                                            : gq4::launch_fp32(call, stream);
     return err == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
 }
 
@@ -277,6 +278,12 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
     return gq4::launch_dequant(K, N, group_size, Bq, scales, zeros, W, stream) == cudaSuccess
                ? GQ4_OK
                : GQ4_ERR_CUDA;
+}
+
+gq4_status gq4_device_error(unsigned int *bits, int clear)
+{
+    if (!bits) return GQ4_ERR_INVALID_ARG;
+    return gq4::read_device_error(bits, clear != 0) == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
 }
 
 const char *gq4_status_string(gq4_status status)

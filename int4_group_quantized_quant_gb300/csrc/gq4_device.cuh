@@ -24,8 +24,11 @@
 // rounded unscaled difference.  The activation that multiplies code i is
 // pre-scaled by 16^-p_i (also exact), so a_scaled * d = a * fl(q - zero)
 // exactly inside the FMA.  The fp32 result is therefore bit-identical to an
-// FMA chain over fl(q - zero) * a, with two FP operations per code (a
-// subtraction pair and an FMA), issued as packed f32x2 instructions.
+// FMA chain over fl(q - zero) * a, with three FP operations per code (two
+// additions of pre-negated constants and an FMA), issued as packed f32x2
+// instructions.  Subtractions are written as additions of negated constants
+// because the packed add has no negated-operand form: a packed subtract would
+// cost two extra sign flips per pair inside the inner loop.
 #pragma once
 
 #include <cstdint>
@@ -65,10 +68,10 @@ __device__ __forceinline__ float2 unpack2(f32x2 v)
     return make_float2(lo, hi);
 }
 
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b)
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
 {
     f32x2 r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
@@ -99,17 +102,17 @@ __device__ __forceinline__ CodePairs extract_word(uint32_t w)
     return c;
 }
 
-// Zero point scaled to the code positions: (z, 16z) for p = 0, 1 and
-// (256z, 4096z) for p = 2, 3.
+// Negated zero point scaled to the code positions: -(z, 16z) for p = 0, 1 and
+// -(256z, 4096z) for p = 2, 3.
 struct ZeroPairs {
-    f32x2 z01, z23;
+    f32x2 nz01, nz23;
 };
 
 __device__ __forceinline__ ZeroPairs scaled_zero(float z)
 {
     ZeroPairs r;
-    r.z01 = pack2(z, z * 16.0f);
-    r.z23 = pack2(z * 256.0f, z * 4096.0f);
+    r.nz01 = pack2(z * -1.0f, z * -16.0f);
+    r.nz23 = pack2(z * -256.0f, z * -4096.0f);
     return r;
 }
 
@@ -118,15 +121,20 @@ struct DiffPairs {
     f32x2 d01, d23, d45, d67;
 };
 
-__device__ __forceinline__ DiffPairs code_minus_zero(uint32_t w, const ZeroPairs &z)
+__device__ __forceinline__ f32x2 neg_magic2()
 {
-    const f32x2 magic2 = pack2(kMagic, kMagic);
+    return pack2(-kMagic, -kMagic);
+}
+
+__device__ __forceinline__ DiffPairs code_minus_zero(uint32_t w, const ZeroPairs &z,
+                                                     f32x2 nmagic2)
+{
     const CodePairs c = extract_word(w);
     DiffPairs d;
-    d.d01 = sub2(sub2(c.p01, magic2), z.z01);
-    d.d23 = sub2(sub2(c.p23, magic2), z.z23);
-    d.d45 = sub2(sub2(c.p45, magic2), z.z01);
-    d.d67 = sub2(sub2(c.p67, magic2), z.z23);
+    d.d01 = add2(add2(c.p01, nmagic2), z.nz01);
+    d.d23 = add2(add2(c.p23, nmagic2), z.nz23);
+    d.d45 = add2(add2(c.p45, nmagic2), z.nz01);
+    d.d67 = add2(add2(c.p67, nmagic2), z.nz23);
     return d;
 }
 

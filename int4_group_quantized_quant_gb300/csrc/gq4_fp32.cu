@@ -236,6 +236,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
                 for (int s = 0; s < kStreams; ++s) inner[m][s] = 0ull;
 
             const ulonglong2 *arow = reinterpret_cast<const ulonglong2 *>(s_act);
+            const f32x2 nmagic2 = neg_magic2();
             const int sw = c & 7;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -243,7 +244,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
 #pragma unroll
                 for (int s = 0; s < kStreams; ++s) {
                     const uint32_t word = w == 0 ? wq[s].x : w == 1 ? wq[s].y : w == 2 ? wq[s].z : wq[s].w;
-                    d[s] = code_minus_zero(word, zps[s]);
+                    d[s] = code_minus_zero(word, zps[s], nmagic2);
                 }
 #pragma unroll
                 for (int m = 0; m < MB; ++m) {
@@ -401,11 +402,11 @@ __global__ void unpack_kernel(size_t words, const uint32_t *__restrict__ Bq, uin
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= words) return;
     const CodePairs c = extract_word(Bq[i]);
-    const f32x2 magic2 = pack2(kMagic, kMagic);
-    const float2 v01 = unpack2(sub2(c.p01, magic2));
-    const float2 v23 = unpack2(sub2(c.p23, magic2));
-    const float2 v45 = unpack2(sub2(c.p45, magic2));
-    const float2 v67 = unpack2(sub2(c.p67, magic2));
+    const f32x2 nmagic2 = neg_magic2();
+    const float2 v01 = unpack2(add2(c.p01, nmagic2));
+    const float2 v23 = unpack2(add2(c.p23, nmagic2));
+    const float2 v45 = unpack2(add2(c.p45, nmagic2));
+    const float2 v67 = unpack2(add2(c.p67, nmagic2));
     // undo the position scale 16^p (exact) and convert the small integers
     const uint32_t q0 = (uint32_t)(v01.x * code_prescale(0));
     const uint32_t q1 = (uint32_t)(v01.y * code_prescale(1));
@@ -431,7 +432,7 @@ __global__ void dequant_kernel(size_t words, int K, int gs, const uint32_t *__re
     const int k0 = (int)(i - n * wpc) * 8;
     const size_t g = n * (size_t)(K / gs) + (size_t)(k0 / gs);
     const float s = scales[g];
-    const DiffPairs d = code_minus_zero(Bq[i], scaled_zero(zeros[g]));
+    const DiffPairs d = code_minus_zero(Bq[i], scaled_zero(zeros[g]), neg_magic2());
     const float2 d01 = unpack2(d.d01), d23 = unpack2(d.d23), d45 = unpack2(d.d45), d67 = unpack2(d.d67);
     // d = 16^p * fl(q - zero): scale back exactly, then one rounding for * scale
     float *dst = W + i * 8;

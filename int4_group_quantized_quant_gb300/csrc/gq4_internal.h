@@ -34,6 +34,13 @@ struct Call {
 // CUDA-core fp32 path (any M <= GQ4_MAX_LANES).
 cudaError_t launch_fp32(const Call &call, cudaStream_t stream);
 
+// Persistent bulk-copy streaming path for one lane (M = 1).
+bool stream_path_supported(const Call &call);
+cudaError_t launch_stream(const Call &call, cudaStream_t stream);
+
+// The sticky device-side error word (read, optionally clear).
+cudaError_t read_device_error(unsigned int *bits, bool clear);
+
 // Test kernels.
 cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream);
 cudaError_t launch_dequant(int K, int N, int gs, const uint32_t *Bq, const float *scales,

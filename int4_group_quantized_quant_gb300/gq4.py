@@ -64,8 +64,10 @@ lib.gq4_status_string.restype = ctypes.c_char_p
 lib.gq4_status_string.argtypes = [_i]
 lib.gq4_version.restype = _i
 lib.gq4_version.argtypes = []
+lib.gq4_device_error.restype = _i
+lib.gq4_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _i]
 
-EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version"]
+EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version", "gq4_device_error"]
 
 
 class GQ4Error(RuntimeError):
@@ -219,6 +221,13 @@ def dequant(Bq, scales, zeros, K, group_size, W=None, stream=None):
     _check(lib.gq4_dequant(K, N, group_size, _ptr(Bq), _ptr(scales), _ptr(zeros), _ptr(W),
                            _stream(stream)), "gq4_dequant")
     return W
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's sticky device error word (bit 0: a bounded wait for a bulk copy expired)."""
+    bits = ctypes.c_uint(0)
+    _check(lib.gq4_device_error(ctypes.byref(bits), int(clear)), "gq4_device_error")
+    return int(bits.value)
 
 
 def version() -> int:

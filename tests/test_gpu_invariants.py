@@ -1,7 +1,10 @@
 """GPU invariants that hold bit for bit by construction of the kernels.
 
 * quad outputs concatenated == the plain matvec on the same weights;
-* lane m of an M-lane call == the one-lane call on row m (CUDA-core path);
+* lane m of an M-lane call == lane 0 of a two-lane call on row m (the
+  multi-lane CUDA-core kernel's per-lane arithmetic does not depend on the
+  lane count; one-lane calls use the streaming kernel, whose reduction
+  order differs, so they are compared within tolerance instead);
 * repeated calls give identical bits;
 * codes equal to integer zero points give exactly 0 at K = 11008;
 * a zero gate gives exactly 0 out of the gated call;
@@ -36,15 +39,25 @@ def test_quad_equals_matvec(gq4, M):
         assert np.array_equal(cat.view(np.uint32), C.view(np.uint32)), (M, n0, n1, n2)
 
 
-@pytest.mark.parametrize("M", [2, 4, 7, 15])
+def _pair(A, m):
+    """Rows (m, m+1 mod M) of A: a two-lane call whose lane 0 is row m."""
+    return np.ascontiguousarray(A[[m, (m + 1) % A.shape[0]]])
+
+
+@pytest.mark.parametrize("M", [3, 4, 7, 15, 32])
 def test_lane_equals_solo(gq4, M):
     K, N, gs = 4096, 130, 128
     w = I.quant_weights(K, N, gs, 961, M)
     A = I.activations(M, K, 961, M)
     C = host(gq4.matvec(dev(A), *wdev(w), gs))
     for m in range(M):
-        Cm = host(gq4.matvec(dev(A[m:m + 1]), *wdev(w), gs))
+        Cm = host(gq4.matvec(dev(_pair(A, m)), *wdev(w), gs))
         assert np.array_equal(C[m].view(np.uint32), Cm[0].view(np.uint32)), (M, m)
+    # and the one-lane streaming kernel agrees with the oracle on every row
+    for m in range(min(M, 3)):
+        C1 = host(gq4.matvec(dev(A[m:m + 1]), *wdev(w), gs))
+        ref, S = oracle.matvec(A[m:m + 1], w.Bq, w.scales, w.zeros, K, N, gs)
+        check_close(f"solo row {m}", C1, ref, tol_fp32(S))
 
 
 def test_norm_lane_equals_solo(gq4):
@@ -54,13 +67,76 @@ def test_norm_lane_equals_solo(gq4):
     W = I.norm_gain(K, 962)
     C = host(gq4.norm_matvec(dev(A), *wdev(w), gs, dev(W), 1e-6, A_b=dev(A_b)))
     for m in range(M):
-        Cm = host(gq4.norm_matvec(dev(A[m:m + 1]), *wdev(w), gs, dev(W), 1e-6,
-                                  A_b=dev(A_b[m:m + 1])))
+        Cm = host(gq4.norm_matvec(dev(_pair(A, m)), *wdev(w), gs, dev(W), 1e-6,
+                                  A_b=dev(_pair(A_b, m))))
         assert np.array_equal(C[m].view(np.uint32), Cm[0].view(np.uint32)), m
 
 
-def test_deterministic(gq4):
-    M, K, N, gs = 4, 4096, 1000, 128
+def _offset_rows(a, offset_floats=1):
+    """A device copy of `a` whose data starts `offset_floats` floats past a 16-byte boundary."""
+    import torch
+    flat = torch.zeros(a.size + 8, dtype=torch.float32, device="cuda")
+    view = flat[offset_floats:offset_floats + a.size].view(*a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)).cuda())
+    return view
+
+
+@pytest.mark.parametrize("kind", ["matvec", "quad", "norm", "gated"])
+def test_one_lane_general_kernel(gq4, kind):
+    """Scale/zero rows that are only 4-byte aligned send a one-lane call to the general
+    kernel; both kernels must match the oracle (and each other within tolerance)."""
+    M, K, N, gs = 1, 4096, 300, 128
+    w = I.quant_weights(K, N, gs, 971)
+    wu = I.quant_weights(K, N, gs, 972)
+    A = I.activations(M, K, 971)
+    A_b = I.activations(M, K, 972)
+    W = I.norm_gain(K, 971)
+    fast = (dev(w.Bq), dev(w.scales), dev(w.zeros))
+    slow = (dev(w.Bq), _offset_rows(w.scales), _offset_rows(w.zeros))
+    fast_u = (dev(wu.Bq), dev(wu.scales), dev(wu.zeros))
+    slow_u = (dev(wu.Bq), _offset_rows(wu.scales), _offset_rows(wu.zeros))
+    if kind == "matvec":
+        ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+        outs = [host(gq4.matvec(dev(A), *ws, gs)) for ws in (fast, slow)]
+        tol = tol_fp32(S)
+    elif kind == "quad":
+        ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+        outs = [np.concatenate([host(o) for o in gq4.quad_matvec(dev(A), *ws, gs, 100, 150, 290)],
+                               axis=1) for ws in (fast, slow)]
+        tol = tol_fp32(S)
+    elif kind == "norm":
+        ref, S, _, _ = oracle.norm_matvec(A, A_b, W, 1e-6, w.Bq, w.scales, w.zeros, K, N, gs)
+        outs = [host(gq4.norm_matvec(dev(A), *ws, gs, dev(W), 1e-6, A_b=dev(A_b)))
+                for ws in (fast, slow)]
+        tol = tol_fp32(S)
+    else:
+        r = oracle.gated_matvec(A, w.Bq, w.scales, w.zeros, wu.Bq, wu.scales, wu.zeros, K, N, gs)
+        ref = r["out"]
+        outs = [host(gq4.gated_matvec(dev(A), *ws, *wsu, gs))
+                for ws, wsu in ((fast, fast_u), (slow, slow_u))]
+        from tests.gpu_util import tol_gated
+        tol = tol_gated(r["g"], r["u"], r["Sg"], r["Su"], ref)
+    for name, o in zip(("streaming", "general"), outs):
+        check_close(f"{kind} {name}", o, ref, tol)
+    assert gq4.device_error() == 0
+
+
+@pytest.mark.parametrize("N", [1, 3, 7, 150, 151, 300, 301, 4097])
+def test_streaming_column_splits(gq4, N):
+    """Column counts below, at and above the grid size, odd counts with 86 groups per
+    column (scale rows split in units of two columns, a tail read directly)."""
+    K, gs = 11008, 128
+    w = I.quant_weights(K, N, gs, 973, N)
+    A = I.activations(1, K, 973, N)
+    ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+    C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    check_close(f"stream N={N}", C, ref, tol_fp32(S))
+    assert gq4.device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_deterministic(gq4, M):
+    K, N, gs = 4096, 1000, 128
     w = I.quant_weights(K, N, gs, 963)
     A = dev(I.activations(M, K, 963))
     first = host(gq4.matvec(A, *wdev(w), gs))
