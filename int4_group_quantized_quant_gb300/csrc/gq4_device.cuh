@@ -87,18 +87,27 @@ struct CodePairs {
     f32x2 p01, p23, p45, p67;
 };
 
-__device__ __forceinline__ CodePairs extract_word(uint32_t w)
+// (x & MASK) | magic as ONE lop3 (LUT 0xEA = a & b | c).  `magic` must come
+// from a register or a kernel parameter (constant bank): written in plain C
+// with both constants as immediates the compiler emits two logic ops per
+// code, which doubles the load on the half-rate ALU pipe.
+template <uint32_t MASK>
+__device__ __forceinline__ float masked_magic(uint32_t x, uint32_t magic)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(MASK), "r"(magic));
+    return __uint_as_float(d);
+}
+
+// `magic` is kMagicBits, passed in from a kernel parameter.
+__device__ __forceinline__ CodePairs extract_word(uint32_t w, uint32_t magic)
 {
     const uint32_t t = w >> 16;
     CodePairs c;
-    c.p01 = pack2(__uint_as_float((w & 0x000Fu) | kMagicBits),
-                  __uint_as_float((w & 0x00F0u) | kMagicBits));
-    c.p23 = pack2(__uint_as_float((w & 0x0F00u) | kMagicBits),
-                  __uint_as_float((w & 0xF000u) | kMagicBits));
-    c.p45 = pack2(__uint_as_float((t & 0x000Fu) | kMagicBits),
-                  __uint_as_float((t & 0x00F0u) | kMagicBits));
-    c.p67 = pack2(__uint_as_float((t & 0x0F00u) | kMagicBits),
-                  __uint_as_float((t & 0xF000u) | kMagicBits));
+    c.p01 = pack2(masked_magic<0x000Fu>(w, magic), masked_magic<0x00F0u>(w, magic));
+    c.p23 = pack2(masked_magic<0x0F00u>(w, magic), masked_magic<0xF000u>(w, magic));
+    c.p45 = pack2(masked_magic<0x000Fu>(t, magic), masked_magic<0x00F0u>(t, magic));
+    c.p67 = pack2(masked_magic<0x0F00u>(t, magic), masked_magic<0xF000u>(t, magic));
     return c;
 }
 
@@ -127,9 +136,9 @@ __device__ __forceinline__ f32x2 neg_magic2()
 }
 
 __device__ __forceinline__ DiffPairs code_minus_zero(uint32_t w, const ZeroPairs &z,
-                                                     f32x2 nmagic2)
+                                                     f32x2 nmagic2, uint32_t magic)
 {
-    const CodePairs c = extract_word(w);
+    const CodePairs c = extract_word(w, magic);
     DiffPairs d;
     d.d01 = add2(add2(c.p01, nmagic2), z.nz01);
     d.d23 = add2(add2(c.p23, nmagic2), z.nz23);

@@ -46,6 +46,7 @@ struct Fp32Params {
     int kct;          // chunks per staged K tile
     int n_ktiles;
     unsigned long long group_magic;  // ceil(2^40 / (gs / 32))
+    uint32_t magic_bits;             // kMagicBits, read from the parameter bank
     const float *A;
     const float *A_b;
     const float *W_norm;
@@ -244,7 +245,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
 #pragma unroll
                 for (int s = 0; s < kStreams; ++s) {
                     const uint32_t word = w == 0 ? wq[s].x : w == 1 ? wq[s].y : w == 2 ? wq[s].z : wq[s].w;
-                    d[s] = code_minus_zero(word, zps[s], nmagic2);
+                    d[s] = code_minus_zero(word, zps[s], nmagic2, p.magic_bits);
                 }
 #pragma unroll
                 for (int m = 0; m < MB; ++m) {
@@ -356,6 +357,7 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream)
     prm.G = call.K / call.gs;
     const unsigned long long cpg = (unsigned long long)(call.gs / 32);
     prm.group_magic = ((1ull << 40) + cpg - 1) / cpg;
+    prm.magic_bits = kMagicBits;
     prm.A = call.A;
     if (call.norm) {
         prm.A_b = call.norm->A_b;
@@ -397,11 +399,12 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream)
 // ---------------------------------------------------------------------------
 namespace {
 
-__global__ void unpack_kernel(size_t words, const uint32_t *__restrict__ Bq, uint8_t *__restrict__ q)
+__global__ void unpack_kernel(size_t words, const uint32_t *__restrict__ Bq, uint8_t *__restrict__ q,
+                              uint32_t magic_bits)
 {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= words) return;
-    const CodePairs c = extract_word(Bq[i]);
+    const CodePairs c = extract_word(Bq[i], magic_bits);
     const f32x2 nmagic2 = neg_magic2();
     const float2 v01 = unpack2(add2(c.p01, nmagic2));
     const float2 v23 = unpack2(add2(c.p23, nmagic2));
@@ -423,7 +426,7 @@ __global__ void unpack_kernel(size_t words, const uint32_t *__restrict__ Bq, uin
 
 __global__ void dequant_kernel(size_t words, int K, int gs, const uint32_t *__restrict__ Bq,
                                const float *__restrict__ scales, const float *__restrict__ zeros,
-                               float *__restrict__ W)
+                               float *__restrict__ W, uint32_t magic_bits)
 {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= words) return;
@@ -432,7 +435,7 @@ __global__ void dequant_kernel(size_t words, int K, int gs, const uint32_t *__re
     const int k0 = (int)(i - n * wpc) * 8;
     const size_t g = n * (size_t)(K / gs) + (size_t)(k0 / gs);
     const float s = scales[g];
-    const DiffPairs d = code_minus_zero(Bq[i], scaled_zero(zeros[g]), neg_magic2());
+    const DiffPairs d = code_minus_zero(Bq[i], scaled_zero(zeros[g]), neg_magic2(), magic_bits);
     const float2 d01 = unpack2(d.d01), d23 = unpack2(d.d23), d45 = unpack2(d.d45), d67 = unpack2(d.d67);
     // d = 16^p * fl(q - zero): scale back exactly, then one rounding for * scale
     float *dst = W + i * 8;
@@ -452,7 +455,7 @@ cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStre
 {
     const size_t words = (size_t)N * (size_t)(K / 8);
     const unsigned blocks = (unsigned)((words + 255) / 256);
-    unpack_kernel<<<blocks, 256, 0, stream>>>(words, Bq, q);
+    unpack_kernel<<<blocks, 256, 0, stream>>>(words, Bq, q, kMagicBits);
     return cudaGetLastError();
 }
 
@@ -461,7 +464,7 @@ cudaError_t launch_dequant(int K, int N, int gs, const uint32_t *Bq, const float
 {
     const size_t words = (size_t)N * (size_t)(K / 8);
     const unsigned blocks = (unsigned)((words + 255) / 256);
-    dequant_kernel<<<blocks, 256, 0, stream>>>(words, K, gs, Bq, scales, zeros, W);
+    dequant_kernel<<<blocks, 256, 0, stream>>>(words, K, gs, Bq, scales, zeros, W, kMagicBits);
     return cudaGetLastError();
 }
 

@@ -7,28 +7,32 @@
 //
 // Decomposition.  At M = 1 the path is one streaming pass over the weights,
 // so the kernel is organised around moving bytes:
-//   * Persistent grid (about 1-2 CTAs per SM).  CTA b owns one contiguous
-//     range of whole columns; ranges are balanced in units of 1, 2 or 4
-//     columns so that every copy of scale/zero rows starts 16-byte aligned.
-//     Contiguous columns are contiguous bytes in the [N][K/8] layout.
-//   * One producer warp streams the range through a ring of S shared-memory
-//     slots with cp.async.bulk (global -> shared, completion on an mbarrier).
-//     A slot holds `cps` columns of packed codes plus their scale and zero
-//     rows (of both matrices for the gated call).
-//   * Consumer warps are activation-stationary: lane (w, l) of a column
-//     group owns 32-code chunks t = 32w + l (+ 32W r) of K for every column
-//     and keeps the 32 matching activations in registers, pre-scaled by
-//     16^-p (see gq4_device.cuh).  Shared memory then carries only the
-//     weights (0.5 byte per code), read as conflict-free 128-bit loads.
-//   * The norm prologue (x = A + A_b, inverse RMS, gain) runs once per CTA
-//     while the producer's first copies are in flight.
-//   * Per slot a warp handles four weight streams (four columns, or two gate
-//     and two up columns), reduces them with an xor reduce-scatter (the same
-//     addition tree as a full butterfly for each column), and the W warps of
-//     a group combine their partials in warp order through shared memory.
-//     Results are deterministic and do not depend on the grid size.
+//   * Persistent grid, one CTA per SM.  CTA b owns one contiguous range of
+//     whole columns, balanced in units of 1, 2 or 4 columns so that every
+//     copy of scale/zero rows starts 16-byte aligned.  Contiguous columns are
+//     contiguous bytes in the [N][K/8] layout.
+//   * One producer warp streams the range with cp.async.bulk (global ->
+//     shared, completion on mbarriers): the CTA's scale and zero rows once,
+//     at the start, then the packed codes through a ring of S stages.  A
+//     stage holds the columns of WPS warp slots, one bulk copy per matrix:
+//     few, large copies (the per-SM rate of bulk-copy requests, not bytes,
+//     limits small copies).
+//   * A warp slot is SPW whole columns (or SPW/2 gate and SPW/2 up columns).
+//     Consumer warps take slots round-robin; a warp walks all of K for its
+//     slot (lane l owns 32-code chunk groups l, l+32, ...) and reduces it
+//     once with an xor reduce-scatter.  No cross-warp reduction, no group
+//     barriers in the steady state.
+//   * Activations are staged once per CTA in shared memory, pre-scaled by
+//     16^-p (see gq4_device.cuh) and XOR-swizzled so that a warp's 128-bit
+//     loads are conflict-free; every activation load serves all SPW streams.
+//     The RMSNorm prologue (x = A + A_b, inverse RMS, gain) is applied while
+//     staging, together with each chunk group's activation sum.
+//   * The integer part of each zero point is folded into the magic offset
+//     (exact), the fractional part is applied once per chunk group through
+//     the activation sum (see fold_zero).
 //   * Every mbarrier wait is bounded in time; on expiry the kernel records
 //     an error in a device word (gq4_device_error) and leaves.
+#include <atomic>
 #include <cstdint>
 
 #include "gq4_device.cuh"
@@ -42,26 +46,27 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int kStreams = 4;        // weight columns a warp reduces together per slot
-constexpr int kMaxR = 2;           // chunks per lane (K <= 32768 on this path)
-constexpr int kMaxConsumerWarps = 16;
-constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
-constexpr int kMaxStages = 8;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 32;
+constexpr uint32_t kSmemLimit = 220u * 1024u;
 
 struct StreamParams {
     int K, N, gs;
     int KC, G;
-    int W;            // K-warps per column group
-    int Gc;           // column groups
-    int cpg;          // columns per group per slot
-    int cps;          // columns per slot (Gc * cpg)
-    int S;            // ring depth
+    int KP;           // chunk groups per column (KC / R)
+    int cps;          // columns per warp slot (per matrix)
+    int wps;          // warp slots per stage
+    int S;            // ring depth (stages)
     int unit;         // column granularity of the balanced split
     int n_units;
-    uint32_t slot_bytes;
-    uint32_t off_w[2], off_s[2], off_z[2];
-    uint32_t off_red, off_norm, off_bar;
+    int max_cols;     // most columns any CTA owns (sizes the scale/zero area)
+    uint32_t stage_bytes;
+    uint32_t off_w[2];              // within a stage
+    uint32_t off_s[2], off_z[2];    // scale/zero rows of the CTA's range
+    uint32_t off_act, off_asum, off_norm, off_bar;
     unsigned long long group_magic;
+    uint32_t magic_bits;  // kMagicBits, read from the parameter bank
     const float *A;
     const float *A_b;
     const float *W_norm;
@@ -91,19 +96,70 @@ __device__ __forceinline__ void record_error(unsigned int bits)
     atomicOr(&g_device_error, bits);
 }
 
-template <int NMAT, bool NORM, int EPI, int R>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+// Per (column, group) zero-point constants.  The integer part of the zero
+// is folded into the magic offset, exactly: with zi = round(clamp(z, 0, 15)),
+//   f - (2^23 + 16^p zi) = 16^p (q - zi)          (an exact small integer),
+// and the fractional part dz = zi - z multiplies the chunk's activation sum:
+//   sum_k a_k (q_k - z) = sum_k a_k (q_k - zi) + dz * sum_k a_k.
+// When the zero is an integer in 0..15 (as for codes equal to their zero),
+// dz is exactly 0 and so is the correction.
+struct ZeroFold {
+    f32x2 nc01, nc23;  // -(2^23 + 16^p zi) for p = 0, 1 and p = 2, 3
+    float dz;
+};
+
+__device__ __forceinline__ ZeroFold fold_zero(float z)
+{
+    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
+    const float rz = zc + kMagic;  // 2^23 + round(zc)
+    const uint32_t rb = __float_as_uint(rz);
+    const uint32_t zi = rb - kMagicBits;
+    const uint32_t nb = rb | 0x80000000u;  // bits of -(2^23 + zi)
+    ZeroFold f;
+    f.nc01 = pack2(__uint_as_float(nb), __uint_as_float(nb + zi * 15u));
+    f.nc23 = pack2(__uint_as_float(nb + zi * 255u), __uint_as_float(nb + zi * 4095u));
+    f.dz = (rz - kMagic) - z;
+    return f;
+}
+
+// Shared-memory slot of activation float4 j (0..7) of chunk t: chunk groups
+// of R chunks are XOR-swizzled so that 32 lanes reading 32 consecutive
+// groups hit distinct banks.
+template <int R>
+__device__ __forceinline__ int act_index(int t, int j)
+{
+    return t * 8 + (j ^ ((t / R) & 7));
+}
+
+// R: consecutive 32-code chunks per chunk group (R = 2 only when a scale
+// group holds at least 64 codes, so both chunks share one scale and zero).
+// SPW: weight streams per warp per slot (columns, or gate and up columns).
+// NS: chunk-group steps per lane per slot when the slot's packed words are
+// copied to registers (the stage is then released at once, so the ring keeps
+// the DRAM busy while the warp computes); NS = 0 computes from shared memory.
+template <int NMAT, bool NORM, int EPI, int R, int SPW, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
 stream_matvec_kernel(const __grid_constant__ StreamParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
     uint64_t *empty = full + kMaxStages;
-    float *red = reinterpret_cast<float *>(smem + p.off_red);      // [2][Gc][W][4]
-    float *red_norm = reinterpret_cast<float *>(smem + p.off_norm); // [Gc][W]
+    uint64_t *ready = empty + kMaxStages;  // consumers' prologue done
+    uint64_t *srows = ready + 1;           // scale/zero rows landed
+    // Sequence number of the stage a ring entry currently holds.  Entries are
+    // shared by warps taking slots round-robin, so a warp first waits for its
+    // stage's number (the previous occupant's barrier phase is then complete)
+    // and only then for the barrier phase: a parity wait alone could match the
+    // phase two steps back while the previous occupant is still landing.
+    int *s_seq = reinterpret_cast<int *>(srows + 1);
+    float4 *s_act = reinterpret_cast<float4 *>(smem + p.off_act);
+    float *s_asum = reinterpret_cast<float *>(smem + p.off_asum);
+    float *s_norm = reinterpret_cast<float *>(smem + p.off_norm);
 
-    const int n_consumer_warps = p.Gc * p.W;
+    constexpr int CPS = NMAT == 2 ? SPW / 2 : SPW;  // columns per warp slot (per matrix)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int ctid = threadIdx.x;                   // consumer thread id (< kConsumerWarps*32)
 
     // ---- this CTA's column range (whole units) ----
     const int u0 = (int)((long long)p.n_units * blockIdx.x / gridDim.x);
@@ -111,49 +167,82 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     const int col_begin = u0 * p.unit;
     const int col_end = min(u1 * p.unit, p.N);
     if (col_begin >= col_end) return;  // uniform for the CTA, before any barrier
-    const int n_slots_total = (col_end - col_begin + p.cps - 1) / p.cps;
+    const int ncols = col_end - col_begin;
+    const int stage_cols = p.wps * CPS;
+    const int n_stages = (ncols + stage_cols - 1) / stage_cols;
+    const int n_slots = (ncols + CPS - 1) / CPS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], n_consumer_warps);
+            mbar_init(&empty[s], p.wps);
+            s_seq[s] = -1;
         }
+        mbar_init(ready, 1);
+        mbar_init(srows, 1);
         mbar_fence_init();
     }
     __syncthreads();
 
     // =====================================================================
-    // Producer warp: stream the column range through the ring.
+    // Producer warp.
     // =====================================================================
-    if (warp == n_consumer_warps) {
+    if (warp == kConsumerWarps) {
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
-            for (int i = 0; i < n_slots_total; ++i) {
+            // scale and zero rows of the whole range: one copy per array (the
+            // range starts 16-byte aligned; a ragged tail of the arrays, when
+            // N*G is not a multiple of 4, is loaded plainly first)
+            {
+                const uint32_t s_all = (uint32_t)ncols * (uint32_t)p.G * 4u;
+                const uint32_t s_bytes = s_all & ~15u;
+                for (uint32_t b = s_bytes; b < s_all; b += 4) {
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        const size_t e = (size_t)col_begin * p.G + b / 4;
+                        *reinterpret_cast<float *>(smem + p.off_s[m] + b) = p.scales[m][e];
+                        *reinterpret_cast<float *>(smem + p.off_z[m] + b) = p.zeros[m][e];
+                    }
+                }
+                mbar_arrive_expect_tx(srows, (uint32_t)NMAT * 2u * s_bytes);
+                if (s_bytes) {
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        bulk_g2s(smem + p.off_s[m], p.scales[m] + (size_t)col_begin * p.G, s_bytes, srows);
+                        bulk_g2s(smem + p.off_z[m], p.zeros[m] + (size_t)col_begin * p.G, s_bytes, srows);
+                    }
+                }
+            }
+            for (int i = 0; ok && i < n_stages; ++i) {
                 const int slot = i % p.S;
+                // Two stages go out at once; the rest wait for the consumers'
+                // prologue, so its activation loads are not queued behind every
+                // CTA's whole ring of weight copies.
+                if (i == 2 && !mbar_wait(ready, 0)) {
+                    record_error(1u);
+                    ok = false;
+                    break;
+                }
                 if (i >= p.S && !mbar_wait(&empty[slot], ((i / p.S) - 1) & 1)) {
                     record_error(1u);
                     ok = false;
                     break;
                 }
-                const int c0 = col_begin + i * p.cps;
-                const int nc = min(p.cps, col_end - c0);
+                const int c0 = col_begin + i * stage_cols;
+                const int nc = min(stage_cols, col_end - c0);
                 const uint32_t w_bytes = (uint32_t)nc * (uint32_t)p.KC * 16u;
-                const uint32_t s_bytes = ((uint32_t)nc * (uint32_t)p.G * 4u) & ~15u;
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)NMAT * (w_bytes + 2u * s_bytes));
-                unsigned char *dst = smem + (size_t)slot * p.slot_bytes;
+                unsigned char *dst = smem + (size_t)slot * p.stage_bytes;
+                s_seq[slot] = i;  // published by the release of the arrive below
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)NMAT * w_bytes);
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
+                for (int m = 0; m < NMAT; ++m)
                     bulk_g2s(dst + p.off_w[m], p.Bq[m] + (size_t)c0 * p.KC, w_bytes, &full[slot]);
-                    if (s_bytes) {
-                        bulk_g2s(dst + p.off_s[m], p.scales[m] + (size_t)c0 * p.G, s_bytes, &full[slot]);
-                        bulk_g2s(dst + p.off_z[m], p.zeros[m] + (size_t)c0 * p.G, s_bytes, &full[slot]);
-                    }
-                }
                 issued = i + 1;
             }
             if (!ok) {
                 // leave no copy in flight into this CTA's shared memory
+                (void)mbar_wait(srows, 0);
                 for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
                     (void)mbar_wait(&full[i % p.S], (i / p.S) & 1);
             }
@@ -162,198 +251,295 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     }
 
     // =====================================================================
-    // Consumer warps.
+    // Consumer warps: prologue (activations into shared memory).
     // =====================================================================
-    const int g = warp / p.W;     // column group
-    const int w = warp - g * p.W; // K-warp within the group
-    const int bar_id = 1 + g;
-    const int group_threads = p.W * 32;
-
-    int t[R];
-    bool has[R];
-    int grp[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        t[r] = w * 32 + lane + r * p.W * 32;
-        has[r] = t[r] < p.KC;
-        grp[r] = has[r] ? chunk_group(t[r], p.group_magic) : 0;
-    }
-
-    // ---- activations of the owned chunks, in registers ----
-    f32x2 act[R][16];
-    float sumsq = 0.0f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has[r]) {
-                const size_t k = (size_t)t[r] * 32 + (size_t)j * 4;
-                v = *reinterpret_cast<const float4 *>(p.A + k);
-                if constexpr (NORM) {
-                    if (p.A_b) {
-                        const float4 b = *reinterpret_cast<const float4 *>(p.A_b + k);
-                        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
-                    }
-                    sumsq = fmaf(v.x, v.x, sumsq);
-                    sumsq = fmaf(v.y, v.y, sumsq);
-                    sumsq = fmaf(v.z, v.z, sumsq);
-                    sumsq = fmaf(v.w, v.w, sumsq);
-                }
-            }
-            act[r][2 * j] = pack2(v.x, v.y);
-            act[r][2 * j + 1] = pack2(v.z, v.w);
-        }
-    }
-
+    constexpr int kCT = kConsumerWarps * 32;
+    const int K4 = p.K >> 2;
     if constexpr (NORM) {
-        // inverse RMS over all K: warp butterfly, then warps in order
+        // One global pass: x = A + A_b (to shared memory, unscaled), its
+        // square sum, and the gain (kept in registers for the second pass).
+        constexpr int kPer = 4;  // float4s per thread kept in registers (K <= 4 * 4 * kCT)
+        float4 gn[kPer];
+        float part = 0.0f;
+        const bool write_res = blockIdx.x == 0 && p.residual_out;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
-        if (p.W > 1) {
-            if (lane == 0) red_norm[g * p.W + w] = sumsq;
-            named_barrier(bar_id, group_threads);
-            sumsq = 0.0f;
-            for (int i = 0; i < p.W; ++i) sumsq += red_norm[g * p.W + i];
+        for (int u = 0; u < kPer; ++u) {
+            const int v = ctid + u * kCT;
+            if (v < K4) {
+                float4 x = reinterpret_cast<const float4 *>(p.A)[v];
+                if (p.A_b) {
+                    const float4 b = reinterpret_cast<const float4 *>(p.A_b)[v];
+                    x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+                }
+                gn[u] = reinterpret_cast<const float4 *>(p.W_norm)[v];
+                if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x;
+                part = fmaf(x.x, x.x, part);
+                part = fmaf(x.y, x.y, part);
+                part = fmaf(x.z, x.z, part);
+                part = fmaf(x.w, x.w, part);
+                s_act[act_index<R>(v >> 3, v & 7)] = x;
+            }
         }
-        const float inv = 1.0f / sqrtf(sumsq / (float)p.K + p.eps);
-        const bool write_side = blockIdx.x == 0 && g == 0;
+        // K beyond the register-resident part (large K): gain reloaded below
+        for (int v = ctid + kPer * kCT; v < K4; v += kCT) {
+            float4 x = reinterpret_cast<const float4 *>(p.A)[v];
+            if (p.A_b) {
+                const float4 b = reinterpret_cast<const float4 *>(p.A_b)[v];
+                x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+            }
+            if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x;
+            part = fmaf(x.x, x.x, part);
+            part = fmaf(x.y, x.y, part);
+            part = fmaf(x.z, x.z, part);
+            part = fmaf(x.w, x.w, part);
+            s_act[act_index<R>(v >> 3, v & 7)] = x;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) s_norm[warp] = part;
+        named_barrier(1, kCT);
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) sum += s_norm[w];
+        const float inv = 1.0f / sqrtf(sum / (float)p.K + p.eps);
+        const bool write_norm = blockIdx.x == 0 && p.norm_out;
+        for (int v = ctid, u = 0; v < K4; v += kCT, ++u) {
+            float4 x = s_act[act_index<R>(v >> 3, v & 7)];
+            float4 g;
+            if (u < kPer) {
+                g = u == 0 ? gn[0] : u == 1 ? gn[1] : u == 2 ? gn[2] : gn[3];
+            } else {
+                g = reinterpret_cast<const float4 *>(p.W_norm)[v];
+            }
+            x.x = (x.x * inv) * g.x; x.y = (x.y * inv) * g.y;
+            x.z = (x.z * inv) * g.z; x.w = (x.w * inv) * g.w;
+            if (write_norm) reinterpret_cast<float4 *>(p.norm_out)[v] = x;
+            // pre-scale by 16^-p (exact): both halves of a word sit at p = 0..3
+            x.x *= code_prescale(0);
+            x.y *= code_prescale(1);
+            x.z *= code_prescale(2);
+            x.w *= code_prescale(3);
+            s_act[act_index<R>(v >> 3, v & 7)] = x;
+        }
+    } else {
+        for (int v = ctid; v < K4; v += kCT) {
+            float4 x = reinterpret_cast<const float4 *>(p.A)[v];
+            x.x *= code_prescale(0);
+            x.y *= code_prescale(1);
+            x.z *= code_prescale(2);
+            x.w *= code_prescale(3);
+            s_act[act_index<R>(v >> 3, v & 7)] = x;
+        }
+    }
+    named_barrier(1, kCT);
+    // activation sum of each chunk group (unscaled, fixed order)
+    for (int jg = ctid; jg < p.KP; jg += kCT) {
+        float a = 0.0f;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (!has[r]) continue;
+            const int t = jg * R + r;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const size_t k = (size_t)t[r] * 32 + (size_t)j * 4;
-                const float2 lo = unpack2(act[r][2 * j]);
-                const float2 hi = unpack2(act[r][2 * j + 1]);
-                float4 x = make_float4(lo.x, lo.y, hi.x, hi.y);
-                if (write_side && p.residual_out) *reinterpret_cast<float4 *>(p.residual_out + k) = x;
-                const float4 gn = *reinterpret_cast<const float4 *>(p.W_norm + k);
-                x.x = (x.x * inv) * gn.x; x.y = (x.y * inv) * gn.y;
-                x.z = (x.z * inv) * gn.z; x.w = (x.w * inv) * gn.w;
-                if (write_side && p.norm_out) *reinterpret_cast<float4 *>(p.norm_out + k) = x;
-                act[r][2 * j] = pack2(x.x, x.y);
-                act[r][2 * j + 1] = pack2(x.z, x.w);
+                const float4 x = s_act[act_index<R>(t, j)];
+                a += x.x * (1.0f / code_prescale(0));
+                a += x.y * (1.0f / code_prescale(1));
+                a += x.z * (1.0f / code_prescale(2));
+                a += x.w * (1.0f / code_prescale(3));
             }
         }
+        s_asum[jg] = a;
     }
-    // pre-scale by 16^-p (exact): both halves of a word sit at p = 0, 1, 2, 3
-    {
-        const f32x2 ps01 = pack2(code_prescale(0), code_prescale(1));
-        const f32x2 ps23 = pack2(code_prescale(2), code_prescale(3));
-        const f32x2 zero2 = pack2(0.0f, 0.0f);
+    named_barrier(1, kCT);
+    if (ctid == 0) mbar_arrive(ready);
+
+    // =====================================================================
+    // Consumer warps: slots round-robin.
+    // =====================================================================
+    // A consumer whose bounded wait expires stops waiting and reading (its
+    // outputs become NaN) but still releases its stages.
+    bool failed = !mbar_wait(srows, 0);
+    if (failed) record_error(1u);
+    const uint32_t magic = p.magic_bits;
+    const float *srow[NMAT];
+    const float *zrow[NMAT];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) act[r][j] = fma2(act[r][j], (j & 1) ? ps23 : ps01, zero2);
+    for (int m = 0; m < NMAT; ++m) {
+        srow[m] = reinterpret_cast<const float *>(smem + p.off_s[m]);
+        zrow[m] = reinterpret_cast<const float *>(smem + p.off_z[m]);
     }
 
-    const f32x2 nmagic2 = neg_magic2();
-    // A consumer whose bounded wait expires keeps walking the slots (releasing
-    // them and joining its group's barriers, so no sibling warp is left
-    // waiting) but stops waiting and reading; its outputs become NaN.
-    bool failed = false;
-
-    for (int i = 0; i < n_slots_total; ++i) {
-        const int slot = i % p.S;
-        const int c0 = col_begin + i * p.cps;
-        const int nc = min(p.cps, col_end - c0);
-        if (!failed && !mbar_wait(&full[slot], (i / p.S) & 1)) {
+    for (int i = warp; i < n_slots; i += kConsumerWarps) {
+        const int stage = i / p.wps;
+        const int sub = i - stage * p.wps;
+        const int ring = stage % p.S;
+        const int lc0 = i * CPS;  // first column of the slot, relative to col_begin
+        const int nc = min(CPS, ncols - lc0);
+        if (!failed &&
+            !(wait_shared_eq(&s_seq[ring], stage) && mbar_wait(&full[ring], (stage / p.S) & 1))) {
             record_error(1u);
             failed = true;
         }
-        const unsigned char *sl = smem + (size_t)slot * p.slot_bytes;
-        const int s_smem_floats = (int)((((uint32_t)nc * (uint32_t)p.G * 4u) & ~15u) >> 2);
+        const unsigned char *sl = smem + (size_t)ring * p.stage_bytes;
 
-        float part[kStreams];
+        float acc[SPW];
 #pragma unroll
-        for (int q = 0; q < kStreams; ++q) {
-            const int mat = NMAT == 2 ? (q >> 1) : 0;
-            const int lc = NMAT == 2 ? g * 2 + (q & 1) : g * 4 + q;  // column within the slot
-            float acc = 0.0f;
-            if (lc < nc && !failed) {
-                const uint4 *wsm = reinterpret_cast<const uint4 *>(sl + p.off_w[mat]);
-                const float *ssm = reinterpret_cast<const float *>(sl + p.off_s[mat]);
-                const float *zsm = reinterpret_cast<const float *>(sl + p.off_z[mat]);
+        for (int q = 0; q < SPW; ++q) acc[q] = 0.0f;
+
+        // The slot's packed words of matrix `mat`, column `lc` (a short last
+        // slot repeats its column 0, whose result is then discarded).
+        auto slot_words = [&](int q) -> const uint4 * {
+            const int mat = NMAT == 2 ? (q / CPS) : 0;
+            int lc = NMAT == 2 ? (q % CPS) : q;
+            lc = lc < nc ? lc : 0;
+            return reinterpret_cast<const uint4 *>(sl + p.off_w[mat]) + (size_t)(sub * CPS + lc) * p.KC;
+        };
+        // One chunk group (R chunks) of all SPW streams.
+        auto chunk_group_dot = [&](int jg, const uint4 (&wq)[SPW][R]) {
+            const int t0 = jg * R;
+            const int grp = chunk_group(t0, p.group_magic);
+            const float asum = s_asum[jg];
+            float sc[SPW];
+            ZeroFold zf[SPW];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    if (!has[r]) continue;
-                    const uint4 wq = wsm[(size_t)lc * p.KC + t[r]];
-                    const int si = lc * p.G + grp[r];
-                    float sc, zr;
-                    if (si < s_smem_floats) {
-                        sc = ssm[si];
-                        zr = zsm[si];
-                    } else {  // the last few floats of the arrays when N*G is not a multiple of 4
-                        sc = __ldg(p.scales[mat] + (size_t)c0 * p.G + si);
-                        zr = __ldg(p.zeros[mat] + (size_t)c0 * p.G + si);
+            for (int q = 0; q < SPW; ++q) {
+                const int mat = NMAT == 2 ? (q / CPS) : 0;
+                int lc = NMAT == 2 ? (q % CPS) : q;
+                lc = lc < nc ? lc : 0;
+                const int si = (lc0 + lc) * p.G + grp;
+                sc[q] = srow[mat][si];
+                zf[q] = fold_zero(zrow[mat][si]);
+            }
+            // two independent accumulators per stream (words 0-1 and 2-3)
+            f32x2 in0[SPW], in1[SPW];
+#pragma unroll
+            for (int q = 0; q < SPW; ++q) {
+                in0[q] = pack2(0.0f, 0.0f);
+                in1[q] = pack2(0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                // the chunk's 32 activations, loaded before any use
+                ulonglong2 av[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    av[j] = reinterpret_cast<const ulonglong2 *>(s_act)[act_index<R>(t0 + r, j)];
+#pragma unroll
+                for (int wd = 0; wd < 4; ++wd) {
+                    const ulonglong2 lo = av[2 * wd];
+                    const ulonglong2 hi = av[2 * wd + 1];
+#pragma unroll
+                    for (int q = 0; q < SPW; ++q) {
+                        const uint32_t word = wd == 0 ? wq[q][r].x : wd == 1 ? wq[q][r].y
+                                            : wd == 2 ? wq[q][r].z : wq[q][r].w;
+                        const CodePairs c = extract_word(word, magic);
+                        f32x2 a = wd < 2 ? in0[q] : in1[q];
+                        a = fma2(lo.x, add2(c.p01, zf[q].nc01), a);
+                        a = fma2(lo.y, add2(c.p23, zf[q].nc23), a);
+                        a = fma2(hi.x, add2(c.p45, zf[q].nc01), a);
+                        a = fma2(hi.y, add2(c.p67, zf[q].nc23), a);
+                        if (wd < 2) in0[q] = a; else in1[q] = a;
                     }
-                    const ZeroPairs zp = scaled_zero(zr);
-                    f32x2 inner = pack2(0.0f, 0.0f);
-#pragma unroll
-                    for (int wd = 0; wd < 4; ++wd) {
-                        const uint32_t word = wd == 0 ? wq.x : wd == 1 ? wq.y : wd == 2 ? wq.z : wq.w;
-                        const DiffPairs d = code_minus_zero(word, zp, nmagic2);
-                        inner = fma2(act[r][4 * wd + 0], d.d01, inner);
-                        inner = fma2(act[r][4 * wd + 1], d.d23, inner);
-                        inner = fma2(act[r][4 * wd + 2], d.d45, inner);
-                        inner = fma2(act[r][4 * wd + 3], d.d67, inner);
-                    }
-                    const float2 v = unpack2(inner);
-                    acc = fmaf(sc, v.x + v.y, acc);
                 }
             }
-            part[q] = acc;
-        }
-        // the slot's shared memory has been read: release it to the producer
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-
-        // ---- reduce-scatter of the four streams across the warp ----
-        // step 16: lanes < 16 keep streams 0,1; lanes >= 16 keep streams 2,3
-        const bool hi16 = (lane & 16) != 0;
-        float k0 = hi16 ? part[2] : part[0];
-        float k1 = hi16 ? part[3] : part[1];
-        const float s0 = hi16 ? part[0] : part[2];
-        const float s1 = hi16 ? part[1] : part[3];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-        // step 8: lanes with bit 3 clear keep the first, others the second
-        const bool hi8 = (lane & 8) != 0;
-        float v = hi8 ? k1 : k0;
-        v += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+            f32x2 inner[SPW];
 #pragma unroll
-        for (int off = 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        // lane 0 -> stream 0, lane 8 -> stream 1, lane 16 -> stream 2, lane 24 -> stream 3
-        const int q_of_lane = ((lane >> 4) << 1) | ((lane >> 3) & 1);
-
-        float total = v;
-        if (p.W > 1) {
-            float *rb = red + ((size_t)(i & 1) * p.Gc + g) * p.W * kStreams;
-            if ((lane & 7) == 0) rb[w * kStreams + q_of_lane] = v;
-            named_barrier(bar_id, group_threads);
-            if (w != 0) continue;
-            if ((lane & 7) == 0) {
-                total = 0.0f;
-                for (int k = 0; k < p.W; ++k) total += rb[k * kStreams + q_of_lane];
+            for (int q = 0; q < SPW; ++q) inner[q] = add2(in0[q], in1[q]);
+#pragma unroll
+            for (int q = 0; q < SPW; ++q) {
+                const float2 v = unpack2(inner[q]);
+                acc[q] = fmaf(sc[q], fmaf(zf[q].dz, asum, v.x + v.y), acc[q]);
             }
+        };
+
+        if constexpr (NS > 0) {
+            // copy the slot to registers, release the stage, then compute
+            uint4 wreg[NS][SPW][R];
+            const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < SPW; ++q) {
+                const uint4 *w = slot_words(q);
+#pragma unroll
+                for (int st = 0; st < NS; ++st) {
+                    const int jg = lane + 32 * st;
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        wreg[st][q][r] = (!failed && jg < p.KP) ? w[jg * R + r] : zero4;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[ring]);
+            if (!failed) {
+#pragma unroll
+                for (int st = 0; st < NS; ++st) {
+                    const int jg = lane + 32 * st;
+                    if (jg < p.KP) chunk_group_dot(jg, wreg[st]);
+                }
+            }
+        } else {
+            if (!failed) {
+                for (int jg = lane; jg < p.KP; jg += 32) {
+                    uint4 wq[SPW][R];
+#pragma unroll
+                    for (int q = 0; q < SPW; ++q) {
+                        const uint4 *w = slot_words(q);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + r];
+                    }
+                    chunk_group_dot(jg, wq);
+                }
+            }
+            // this warp's part of the stage has been read: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[ring]);
         }
 
+        // ---- reduce-scatter of the SPW streams across the warp ----
+        float total;
+        int q_of_lane;
+        if constexpr (SPW == 4) {
+            // step 16: lanes < 16 keep streams 0,1; lanes >= 16 keep streams 2,3
+            const bool hi16 = (lane & 16) != 0;
+            float k0 = hi16 ? acc[2] : acc[0];
+            float k1 = hi16 ? acc[3] : acc[1];
+            const float s0 = hi16 ? acc[0] : acc[2];
+            const float s1 = hi16 ? acc[1] : acc[3];
+            k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+            k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+            // step 8: lanes with bit 3 clear keep the first, others the second
+            const bool hi8 = (lane & 8) != 0;
+            total = hi8 ? k1 : k0;
+            total += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+            // lane 0 -> stream 0, lane 8 -> 1, lane 16 -> 2, lane 24 -> 3
+            q_of_lane = ((lane >> 4) << 1) | ((lane >> 3) & 1);
+        } else {
+            // step 16: lanes < 16 keep stream 0, lanes >= 16 keep stream 1
+            const bool hi16 = (lane & 16) != 0;
+            total = hi16 ? acc[1] : acc[0];
+            total += __shfl_xor_sync(0xffffffffu, hi16 ? acc[0] : acc[1], 16);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+            q_of_lane = lane >> 4;  // lane 0 -> stream 0, lane 16 -> stream 1
+        }
         if (failed) total = __int_as_float(0x7fffffff);
 
-        // ---- epilogue: lanes 0, 8, 16, 24 of warp 0 of the group ----
+        // ---- epilogue ----
+        constexpr int kLaneStride = 32 / SPW;  // lanes holding one stream's total
+        const int c0 = col_begin + lc0;
         if constexpr (EPI == kEpiGated) {
-            const float u = __shfl_down_sync(0xffffffffu, total, 16);  // up partner
-            if ((lane & 7) == 0 && lane < 16) {
-                const int lc = g * 2 + (lane >> 3);
+            // streams 0 .. CPS-1 are gate columns, CPS .. 2*CPS-1 the up columns
+            const float u = __shfl_down_sync(0xffffffffu, total, 16);
+            if ((lane % kLaneStride) == 0 && lane < 16) {
+                const int lc = q_of_lane;
                 if (lc < nc) {
                     const float gv = total;
                     p.out[0][c0 + lc] = gv / (1.0f + expf(-gv)) * u;
                 }
             }
         } else {
-            if ((lane & 7) == 0) {
-                const int lc = g * 4 + q_of_lane;
+            if ((lane % kLaneStride) == 0) {
+                const int lc = q_of_lane;
                 if (lc < nc) {
                     const int col = c0 + lc;
                     if constexpr (EPI == kEpiQuad) {
@@ -384,34 +570,123 @@ uint32_t round_up(uint32_t x, uint32_t a)
     return (x + a - 1) / a * a;
 }
 
-template <int NMAT, bool NORM, int EPI, int R>
-cudaError_t launch_stream_variant(const StreamParams &prm, int threads, size_t smem,
-                                  cudaStream_t stream)
+template <int NMAT, bool NORM, int EPI, int R, int SPW, int NS>
+cudaError_t launch_stream_variant(const StreamParams &prm, size_t smem, cudaStream_t stream)
 {
-    auto kern = stream_matvec_kernel<NMAT, NORM, EPI, R>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
-    int dev = 0, sms = 0, per_sm = 0;
+    auto kern = stream_matvec_kernel<NMAT, NORM, EPI, R, SPW, NS>;
+    int dev = 0, sms = 0;
+    cudaError_t err;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    // Raise this kernel's dynamic shared-memory limit once per device (the
+    // flags are per template instance: one kernel each).
+    constexpr int kMaxDevices = 64;
+    static std::atomic<unsigned char> smem_ready[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices || !smem_ready[dev].load(std::memory_order_acquire)) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)(kSmemLimit + 4096u));
+        if (err != cudaSuccess) return err;
+        if (dev >= 0 && dev < kMaxDevices) smem_ready[dev].store(1, std::memory_order_release);
+    }
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return err;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem)) !=
-        cudaSuccess)
-        return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    int grid = sms * (per_sm > 2 ? 2 : per_sm);
+    int grid = sms;
     if (grid > prm.n_units) grid = prm.n_units;
-    kern<<<grid, threads, smem, stream>>>(prm);
+    kern<<<grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
 template <int NMAT, bool NORM, int EPI>
-cudaError_t launch_stream_r(const StreamParams &prm, int R, int threads, size_t smem,
-                            cudaStream_t stream)
+cudaError_t launch_stream_rs(const StreamParams &prm, int R, int spw, int ns, size_t smem,
+                             cudaStream_t stream)
 {
-    return R == 1 ? launch_stream_variant<NMAT, NORM, EPI, 1>(prm, threads, smem, stream)
-                  : launch_stream_variant<NMAT, NORM, EPI, 2>(prm, threads, smem, stream);
+    if (ns == 0) {
+        if (R == 2)
+            return spw == 4 ? launch_stream_variant<NMAT, NORM, EPI, 2, 4, 0>(prm, smem, stream)
+                            : launch_stream_variant<NMAT, NORM, EPI, 2, 2, 0>(prm, smem, stream);
+        return spw == 4 ? launch_stream_variant<NMAT, NORM, EPI, 1, 4, 0>(prm, smem, stream)
+                        : launch_stream_variant<NMAT, NORM, EPI, 1, 2, 0>(prm, smem, stream);
+    }
+    switch (ns) {
+    case 1: return launch_stream_variant<NMAT, NORM, EPI, 2, 4, 1>(prm, smem, stream);
+    case 2: return launch_stream_variant<NMAT, NORM, EPI, 2, 4, 2>(prm, smem, stream);
+    case 4: return launch_stream_variant<NMAT, NORM, EPI, 2, 2, 4>(prm, smem, stream);
+    default: return launch_stream_variant<NMAT, NORM, EPI, 2, 2, 6>(prm, smem, stream);
+    }
+}
+
+// Ring geometry for a call; false when the call does not fit this path.
+bool plan_stream(const Call &call, StreamParams &prm, int &R, int &spw, int &ns, size_t &smem,
+                 int grid)
+{
+    prm.K = call.K;
+    prm.N = call.N;
+    prm.gs = call.gs;
+    prm.KC = call.K / 32;
+    prm.G = call.K / call.gs;
+    // two consecutive chunks per chunk group when a scale group spans them
+    R = (call.gs >= 64 && prm.KC % 2 == 0) ? 2 : 1;
+    prm.KP = prm.KC / R;
+    prm.unit = 4 / gcd_int(prm.G, 4);
+    prm.n_units = (call.N + prm.unit - 1) / prm.unit;
+    if (grid > prm.n_units) grid = prm.n_units;
+    prm.max_cols = ((prm.n_units + grid - 1) / grid) * prm.unit;
+    const uint32_t act_bytes = round_up((uint32_t)prm.KC * 128u, 128u);
+    const uint32_t asum_bytes = round_up((uint32_t)prm.KP * 4u, 128u);
+    const uint32_t rows_bytes = round_up((uint32_t)prm.max_cols * prm.G * 4u, 128u);
+    const uint32_t fixed = act_bytes + asum_bytes + 2u * call.nmat * rows_bytes + 128u +
+                           (2 * kMaxStages + 2) * 8u + kMaxStages * 4u;
+    // Register-resident slots (ns > 0) for long columns (3 to 6 chunk-group
+    // steps per lane: the stage is released before the long computation);
+    // otherwise compute from shared memory (ns = 0), which measured faster
+    // for short columns.
+    const int steps = (prm.KP + 31) / 32;
+    ns = 0;
+    int spw_first = 4, spw_last = 2;
+    if (R == 2 && steps > 2 && steps <= 6) {
+        ns = steps <= 4 ? 4 : 6;
+        spw_first = spw_last = 2;
+    }
+    for (spw = spw_first; spw >= spw_last; spw /= 2) {
+        const int cps = call.nmat == 2 ? spw / 2 : spw;
+        // warp slots per stage: aim at ~32-48 KB per bulk copy round
+        const uint32_t slot_bytes = (uint32_t)call.nmat * cps * prm.KC * 16u;
+        for (int wps = kConsumerWarps; wps >= 1; wps /= 2) {
+            const uint32_t stage = round_up(slot_bytes * wps, 128u);
+            if (wps > 1 && stage > 48u * 1024u) continue;
+            // at least two stages (with fewer warp slots in the ring than
+            // consumer warps, the extra warps simply wait their turn)
+            if (fixed + stage * 2u > kSmemLimit) continue;
+            int S = (int)((kSmemLimit - fixed) / stage);
+            if (S > kMaxStages) S = kMaxStages;
+            prm.S = S;
+            prm.cps = cps;
+            prm.wps = wps;
+            prm.stage_bytes = stage;
+            for (int m = 0; m < call.nmat; ++m) prm.off_w[m] = (uint32_t)m * cps * wps * prm.KC * 16u;
+            uint32_t off = round_up((uint32_t)S * stage, 128u);
+            for (int m = 0; m < call.nmat; ++m) {
+                prm.off_s[m] = off;
+                off += rows_bytes;
+                prm.off_z[m] = off;
+                off += rows_bytes;
+            }
+            prm.off_act = off;
+            prm.off_asum = prm.off_act + act_bytes;
+            prm.off_norm = prm.off_asum + asum_bytes;
+            prm.off_bar = prm.off_norm + 128u;
+            smem = prm.off_bar + (2 * kMaxStages + 2) * sizeof(uint64_t) + kMaxStages * sizeof(int);
+            return smem <= kSmemLimit + 4096u;
+        }
+    }
+    return false;
+}
+
+int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
 }
 
 }  // namespace
@@ -419,59 +694,27 @@ cudaError_t launch_stream_r(const StreamParams &prm, int R, int threads, size_t 
 bool stream_path_supported(const Call &call)
 {
     if (call.M != 1) return false;
-    const int KC = call.K / 32;
-    if (KC > kMaxR * kMaxConsumerWarps * 32) return false;
     for (int m = 0; m < call.nmat; ++m) {
         if ((reinterpret_cast<uintptr_t>(call.scales[m]) & 15u) != 0) return false;
         if ((reinterpret_cast<uintptr_t>(call.zeros[m]) & 15u) != 0) return false;
     }
-    return true;
+    StreamParams prm{};
+    int R, spw, ns;
+    size_t smem;
+    const int sms = sm_count();
+    return sms > 0 && plan_stream(call, prm, R, spw, ns, smem, sms);
 }
 
 cudaError_t launch_stream(const Call &call, cudaStream_t stream)
 {
     StreamParams prm{};
-    prm.K = call.K;
-    prm.N = call.N;
-    prm.gs = call.gs;
-    prm.KC = call.K / 32;
-    prm.G = call.K / call.gs;
+    int R = 1, spw = 4, ns = 0;
+    size_t smem = 0;
+    const int sms = sm_count();
+    if (sms <= 0 || !plan_stream(call, prm, R, spw, ns, smem, sms)) return cudaErrorInvalidValue;
     const unsigned long long cpgrp = (unsigned long long)(call.gs / 32);
     prm.group_magic = ((1ull << 40) + cpgrp - 1) / cpgrp;
-
-    int R = (prm.KC + 32 * kMaxConsumerWarps - 1) / (32 * kMaxConsumerWarps);
-    if (R < 1) R = 1;
-    prm.W = (prm.KC + 32 * R - 1) / (32 * R);
-    prm.Gc = prm.W >= 8 ? 1 : 8 / prm.W;
-    prm.cpg = call.nmat == 2 ? 2 : 4;
-    prm.cps = prm.Gc * prm.cpg;
-    prm.unit = 4 / gcd_int(prm.G, 4);
-    if (prm.cps % prm.unit != 0) return cudaErrorInvalidValue;  // not reached for cpg >= 2 and unit <= 2
-    prm.n_units = (call.N + prm.unit - 1) / prm.unit;
-
-    // slot layout
-    uint32_t off = 0;
-    const uint32_t sz_bytes = round_up((uint32_t)prm.cps * prm.G * 4u, 16u);
-    for (int m = 0; m < call.nmat; ++m) {
-        prm.off_w[m] = off;
-        off += (uint32_t)prm.cps * prm.KC * 16u;
-        prm.off_s[m] = off;
-        off += sz_bytes;
-        prm.off_z[m] = off;
-        off += sz_bytes;
-    }
-    prm.slot_bytes = round_up(off, 128u);
-    const uint32_t budget = (prm.Gc * prm.W <= 8) ? 96u * 1024u : 192u * 1024u;
-    int S = (int)(budget / prm.slot_bytes);
-    if (S > kMaxStages) S = kMaxStages;
-    if (S < 2) S = 2;
-    prm.S = S;
-    prm.off_red = round_up((uint32_t)S * prm.slot_bytes, 128u);
-    prm.off_norm = prm.off_red + round_up(2u * prm.Gc * prm.W * kStreams * 4u, 16u);
-    prm.off_bar = prm.off_norm + round_up((uint32_t)prm.Gc * prm.W * 4u, 16u);
-    const size_t smem = prm.off_bar + 2 * kMaxStages * sizeof(uint64_t);
-    if (smem > 227u * 1024u) return cudaErrorInvalidValue;
-
+    prm.magic_bits = kMagicBits;
     prm.A = call.A;
     if (call.norm) {
         prm.A_b = call.norm->A_b;
@@ -491,17 +734,16 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream)
         prm.seg_start[i] = call.seg_start[i];
         prm.seg_len[i] = call.seg_len[i];
     }
-    const int threads = (prm.Gc * prm.W + 1) * 32;
     const bool norm = call.norm != nullptr;
     switch (call.epi) {
     case kEpiStore:
-        return norm ? launch_stream_r<1, true, kEpiStore>(prm, R, threads, smem, stream)
-                    : launch_stream_r<1, false, kEpiStore>(prm, R, threads, smem, stream);
+        return norm ? launch_stream_rs<1, true, kEpiStore>(prm, R, spw, ns, smem, stream)
+                    : launch_stream_rs<1, false, kEpiStore>(prm, R, spw, ns, smem, stream);
     case kEpiQuad:
-        return launch_stream_r<1, false, kEpiQuad>(prm, R, threads, smem, stream);
+        return launch_stream_rs<1, false, kEpiQuad>(prm, R, spw, ns, smem, stream);
     case kEpiGated:
-        return norm ? launch_stream_r<2, true, kEpiGated>(prm, R, threads, smem, stream)
-                    : launch_stream_r<2, false, kEpiGated>(prm, R, threads, smem, stream);
+        return norm ? launch_stream_rs<2, true, kEpiGated>(prm, R, spw, ns, smem, stream)
+                    : launch_stream_rs<2, false, kEpiGated>(prm, R, spw, ns, smem, stream);
     default:
         return cudaErrorInvalidValue;
     }

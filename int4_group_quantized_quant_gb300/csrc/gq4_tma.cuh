@@ -73,6 +73,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     return true;
 }
 
+// Wait until the shared int at `p` equals `want` (bounded; false on expiry).
+__device__ __forceinline__ bool wait_shared_eq(const int *p, int want)
+{
+    int v;
+    asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    if (v == want) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+        if (v == want) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Hint: fetch `bytes` (multiple of 16, 16-byte aligned) of global memory into
+// L2 (no completion tracking, no shared memory).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
