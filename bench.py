@@ -176,18 +176,21 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(names=None):
+    """First 16 hex digits of the SHA-256 of the named kernel sources (all when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int4_group_quantized_quant_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    if names is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h"))]
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel_tag: str):
-    """DRAM bytes per launch recorded by an ncu capture, if the kernels are unchanged since."""
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel's sources (the
+    files the summary lists) are unchanged since."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     try:
         text = open(path).read()
@@ -195,7 +198,14 @@ def profiled_traffic(kernel_tag: str):
         return None
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
-    if not m_bytes or not m_hash or m_hash.group(1) != kernel_source_hash():
+    m_src = re.search(r"kernel_sources:\s*([^\n]+)", text)
+    if not m_bytes or not m_hash or not m_src:
+        return None
+    try:
+        digest = kernel_source_hash(m_src.group(1).split())
+    except OSError:
+        return None
+    if m_hash.group(1) != digest:
         return None
     return int(m_bytes.group(1))
 
@@ -369,7 +379,7 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "roofline": {
-            "kernel": "gq4 gated gate/up + RMSNorm prologue, 4096 -> 2 x 11008 (fp32 CUDA-core)",
+            "kernel": "gq4 gated gate/up + RMSNorm prologue, 4096 -> 2 x 11008 (one-lane streaming kernel, CUDA cores)",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

@@ -37,7 +37,9 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStreams = 2;                 // weight streams per warp
-constexpr int kSmemBudget = 48 * 1024;      // activation tile, bytes
+// Activation tile, bytes: dynamic shared memory plus the kernel's static
+// arrays must stay within the 48 KB a launch gets without opting in.
+constexpr int kSmemBudget = 47 * 1024;
 
 struct Fp32Params {
     int M, K, N, gs;

@@ -100,6 +100,8 @@ NORM_CASES = [
     (1, 256, 19, 32, False),
     (3, 1024, 40, 128, True),
     (8, 4096, 33, 64, True),                   # K tiles at M=8
+    (4, 4096, 50, 128, True),                  # stack hidden size at M=4 (largest K tile)
+    (2, 11008, 30, 128, True),                 # ffn size at M=2 (largest K tile)
     (32, 512, 20, 32, True),
 ]
 
@@ -145,6 +147,7 @@ GATED_CASES = [
     (1, 4096, 11008, 128, True),               # with the norm prologue (stack form)
     (1, 256, 21, 32, False),
     (4, 1024, 70, 64, True),
+    (4, 4096, 300, 128, True),                 # the stack's gated call at M=4
     (16, 512, 24, 128, False),
     (32, 256, 20, 32, True),
 ]
