@@ -37,7 +37,8 @@
  *   - Every pointer is a DEVICE pointer owned by the caller; the caller keeps
  *     the buffers alive until the stream has passed the call.  The library
  *     allocates no memory and never synchronizes on the call path; its only
- *     state is one sticky device-side error word (gq4_device_error).
+ *     state is its sticky device-side error bits (gq4_device_error) and a
+ *     per-device cache of launch geometry.
  *   - All checks run on the host before anything is enqueued.  A status other
  *     than GQ4_OK means nothing was enqueued on the stream.  GQ4_ERR_CUDA
  *     means a launch was rejected by the CUDA runtime (cudaGetLastError);
@@ -50,6 +51,12 @@
  *   - Outputs must not overlap each other or any input (GQ4_ERR_ALIAS).
  *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
  *   - Results are deterministic: the same inputs give the same bits.
+ *   - Arithmetic: with M = 1 or 2 <= M <= 15 lanes every product and sum is
+ *     f32 (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot
+ *     product).  With 16 <= M <= 32 lanes on sm_103 the weights and the
+ *     activations are rounded to bf16 and multiplied on the tensor core with
+ *     f32 accumulation (|error| <= 2e-2 * sum_k |a_k w_k| + 1e-6); the norm
+ *     prologue's side outputs stay f32.
  * ---------------------------------------------------------------------------
  */
 #ifndef GQ4_H
@@ -149,10 +156,12 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
                        const float *scales, const float *zeros, float *W,
                        cudaStream_t stream);
 
-/* The library's sticky device-side error word on the current device.  Bit 0
- * is set when a kernel gave up waiting for one of its own bulk copies (every
- * wait inside the kernels is bounded in time, so a broken copy cannot hang
- * the GPU; the outputs of that call are then invalid).  Copies the word to
+/* The library's sticky device-side error bits on the current device.  Bit 0
+ * is set when the one-lane kernel gave up waiting for one of its own bulk
+ * copies, bit 1 when the tensor-core kernel gave up waiting for a copy, an
+ * MMA or a peer CTA of its cluster (every wait inside the kernels is bounded
+ * in time, so a broken copy cannot hang the GPU; the outputs of that call are
+ * then invalid).  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);

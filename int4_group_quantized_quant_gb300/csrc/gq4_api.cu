@@ -127,8 +127,16 @@ gq4_status check_output(const float *out, size_t elems, RangeSet &rs)
 
 gq4_status run(const gq4::Call &call, cudaStream_t stream)
 {
-    const cudaError_t err = gq4::stream_path_supported(call) ? gq4::launch_stream(call, stream)
-                                                            : gq4::launch_fp32(call, stream);
+    // one lane: the persistent streaming kernel; 16..32 lanes: the bf16
+    // tensor-core kernel; otherwise (and for shapes those do not take) the
+    // fp32 CUDA-core kernel
+    cudaError_t err;
+    if (gq4::stream_path_supported(call))
+        err = gq4::launch_stream(call, stream);
+    else if (gq4::tc_path_supported(call))
+        err = gq4::launch_tc(call, stream);
+    else
+        err = gq4::launch_fp32(call, stream);
     return err == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
 }
 
@@ -283,7 +291,11 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
 gq4_status gq4_device_error(unsigned int *bits, int clear)
 {
     if (!bits) return GQ4_ERR_INVALID_ARG;
-    return gq4::read_device_error(bits, clear != 0) == cudaSuccess ? GQ4_OK : GQ4_ERR_CUDA;
+    unsigned int a = 0, b = 0;
+    if (gq4::read_device_error(&a, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    if (gq4::read_tc_device_error(&b, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b;
+    return GQ4_OK;
 }
 
 const char *gq4_status_string(gq4_status status)

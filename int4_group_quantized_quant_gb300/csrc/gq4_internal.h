@@ -38,8 +38,14 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream);
 bool stream_path_supported(const Call &call);
 cudaError_t launch_stream(const Call &call, cudaStream_t stream);
 
-// The sticky device-side error word (read, optionally clear).
+// bf16 tensor-core path for 16 <= M <= 32 lanes (sm_103).
+bool tc_path_supported(const Call &call);
+cudaError_t launch_tc(const Call &call, cudaStream_t stream);
+
+// The sticky device-side error words (read, optionally clear): the one-lane
+// streaming path's and the tensor-core path's.
 cudaError_t read_device_error(unsigned int *bits, bool clear);
+cudaError_t read_tc_device_error(unsigned int *bits, bool clear);
 
 // Test kernels.
 cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream);

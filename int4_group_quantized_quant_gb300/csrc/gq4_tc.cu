@@ -1,0 +1,931 @@
+// gq4_tc.cu -- the batched-lane (16 <= M <= 32) int4 group-quantized matvec
+// family on the 5th-generation tensor core: plain, quad routing, RMSNorm
+// prologue and SiLU-gated gate/up.
+//
+// Operation (gerbil moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4 and
+// WGSL_NORM_MATVEC_INT4, batched over decode lanes): C[m][n] = sum_k
+// a[m][k] * (q(n,k) - z) * s.  With M lanes sharing every weight the product
+// is a small GEMM, D[n][m] = W[n][:] . A[m][:], computed here in bf16 with f32
+// accumulation: the weights are dequantized in registers to bf16 and the MMA
+// runs with the weight tile as the M=128 operand and the lanes as N (16/32).
+//
+// Decomposition.
+//   * Tiles of TR <= 128 weight columns (one MMA row per column).  A thread-
+//     block cluster of KS CTAs owns a tile; its CTAs split K in whole 256-code
+//     stages, and their f32 partial tiles are summed through distributed
+//     shared memory in rank order (deterministic, no global scratch).
+//   * Producer warps (4): one thread issues a 2-D tensor-map copy of the
+//     tile's packed codes for a stage (TR rows x 128 bytes, 128-byte swizzle,
+//     zero fill past K and N); every thread owns one row and turns that row's
+//     scales and zeros for the stage into bf16 pairs (128 + zi, s, (zi-z)*s),
+//     loaded two stages ahead.
+//   * Dequant warps (8): two per TMEM lane quarter.  A thread owns one row
+//     and half of each 64-code K-block: per word, four LOP3 magic extractions
+//     give bf16 pairs (128+q), an exact bf16 subtraction gives q - zi, and an
+//     fma gives (q - zi)*s + (zi - z)*s = (q - z)*s rounded once to bf16.  The
+//     16 results go straight to tensor memory (tcgen05.st): the dequantized
+//     tile never touches shared memory.
+//   * One MMA thread: per K-block, four tcgen05.mma (kind::f16, 128 x N x 16)
+//     per matrix, A from tensor memory, B (the lanes' activations) from
+//     shared memory, D accumulating in tensor memory; tcgen05.commit frees
+//     the K-block's tensor-memory slot and, per tile, hands the accumulator
+//     to the epilogue.
+//   * Epilogue warps (4): tcgen05.ld of the accumulator, the split-K sum
+//     across the cluster, then the store / quad routing / silu(g)*u.
+//   * Activations (and the RMSNorm prologue) for the CTA's K range are
+//     staged once, in bf16, in the canonical K-major 128-byte swizzled layout
+//     the MMA reads.  The codes of a word are stored in the order
+//     (0,4,1,5,2,6,3,7) -- the order the magic extraction yields -- and the
+//     activations are permuted the same way, so the dot product is unchanged.
+//   * Every wait is bounded; on expiry the kernel records an error in a
+//     device word (gq4_device_error), stops waiting and leaves.
+#include <cuda.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "gq4_internal.h"
+#include "gq4_tcgen05.cuh"
+
+namespace gq4 {
+
+// Sticky device-side error word of this path (bit 1: a wait timed out).
+__device__ unsigned int g_tc_error = 0;
+
+namespace {
+
+constexpr int kDqWarps = 8;     // warps 0..7
+constexpr int kEpWarps = 4;     // warps 8..11
+constexpr int kPrWarps = 4;     // warps 12..15
+constexpr int kMmaWarp = 16;    // warp 16
+constexpr int kThreads = 17 * 32;
+constexpr int kEpBase = kDqWarps * 32;
+constexpr int kPrBase = (kDqWarps + kEpWarps) * 32;
+constexpr int kNW = 4;          // tensor-memory slots of dequantized K-blocks
+constexpr int kStageK = 256;    // codes per stage along K
+constexpr int kBlockK = 64;     // codes per K-block (one 128-byte bf16 row)
+constexpr int kMaxStages = 16;
+constexpr int kMaxGps = 8;      // scale groups a stage can touch (gs >= 32)
+constexpr uint32_t kMinSmem = 120u * 1024u;  // forces one CTA per SM (tensor memory)
+
+struct TcParams {
+    CUtensorMap codes[2];          // [N][K/8] u32, box {32, TR}, 128-byte swizzle
+    int M, K, N, gs, G;
+    int TR;                        // rows per tile
+    int n_tiles, n_clusters, ks;
+    int n_st;                      // stages over K
+    int S;                         // ring depth
+    int gps;                       // constant rows per stage (max groups a stage touches)
+    uint32_t off_act, off_ring, stage_bytes, codes_bytes, cst_bytes;
+    uint32_t off_red, off_misc, off_bar;
+    uint32_t magic_bf16;           // 0x43004300, read from the parameter bank
+    const float *A;
+    const float *A_b;
+    const float *W_norm;
+    float eps;
+    float *residual_out;
+    float *norm_out;
+    const float *scales[2];
+    const float *zeros[2];
+    float *out[4];
+    int seg_start[4];
+    int seg_len[4];
+};
+
+struct Shared {
+    uint64_t *full, *empty, *w_full, *w_empty, *acc_full, *acc_empty;
+    uint64_t *act_ready, *red_full, *red_empty, *norm_full, *drain;
+    float *part;      // [32] this CTA's norm partial sums
+    uint32_t *tmem;   // allocated tensor-memory base
+    int *abort;
+};
+
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Gives up (false) when another thread of
+// the CTA has already given up, or after the time limit (then it records the
+// error and tells the CTA).  `cluster` waits acquire at cluster scope.
+__device__ __noinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, bool cluster)
+{
+    auto ready = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (ready()) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (ready()) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(&g_tc_error, 2u);
+            return false;
+        }
+    }
+}
+
+// Wait without giving up early on another thread's abort (used to drain
+// copies and MMAs in flight before the CTA leaves); still bounded.
+__device__ __forceinline__ void tc_drain_wait(uint64_t *bar, uint32_t parity)
+{
+    (void)mbar_wait(bar, parity);
+}
+
+// Output epilogue for one (lane, column).
+template <int EPI>
+__device__ __forceinline__ void store_out(const TcParams &p, int m, int col, float v0, float v1)
+{
+    if constexpr (EPI == kEpiGated) {
+        p.out[0][(size_t)m * p.N + col] = v0 / (1.0f + expf(-v0)) * v1;
+    } else if constexpr (EPI == kEpiQuad) {
+        const int seg = col < p.seg_start[1] ? 0 : col < p.seg_start[2] ? 1 : col < p.seg_start[3] ? 2 : 3;
+        p.out[seg][(size_t)m * p.seg_len[seg] + (col - p.seg_start[seg])] = v0;
+    } else {
+        p.out[0][(size_t)m * p.N + col] = v0;
+    }
+}
+
+// Eight activations a[0..7] of one 8-code chunk as bf16 in the word's code
+// order (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ uint4 pack_chunk(const float4 &lo, const float4 &hi)
+{
+    uint4 r;
+    r.x = bf16x2_pack(lo.x, hi.x);
+    r.y = bf16x2_pack(lo.y, hi.y);
+    r.z = bf16x2_pack(lo.z, hi.z);
+    r.w = bf16x2_pack(lo.w, hi.w);
+    return r;
+}
+
+// Byte offset of chunk c (0..7) of lane row m in one K-block of the
+// activation operand (MP rows of 128 bytes, 8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint32_t act_chunk_offset(int m, int c)
+{
+    return (uint32_t)((m >> 3) * 1024 + (m & 7) * 128 + ((c ^ (m & 7)) << 4));
+}
+
+template <int MP, int NMAT, bool NORM, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte aligned base (128-byte swizzle atoms)
+    const uint32_t raw_s = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+
+    Shared sh;
+    {
+        uint64_t *b = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+        sh.full = b;
+        sh.empty = b + kMaxStages;
+        sh.w_full = b + 2 * kMaxStages;
+        sh.w_empty = sh.w_full + kNW;
+        sh.acc_full = sh.w_empty + kNW;
+        sh.acc_empty = sh.acc_full + 2;
+        sh.act_ready = sh.acc_empty + 2;
+        sh.red_full = sh.act_ready + 1;
+        sh.red_empty = sh.red_full + 1;
+        sh.norm_full = sh.red_empty + 1;
+        sh.drain = sh.norm_full + 1;
+        sh.part = reinterpret_cast<float *>(smem + p.off_misc);
+        sh.tmem = reinterpret_cast<uint32_t *>(smem + p.off_misc + 128);
+        sh.abort = reinterpret_cast<int *>(smem + p.off_misc + 132);
+    }
+    volatile int *abort = sh.abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ks = p.ks;
+    const int rank = ks > 1 ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / ks;
+    // this rank's stages along K
+    const int st0 = (int)((long long)p.n_st * rank / ks);
+    const int st1 = (int)((long long)p.n_st * (rank + 1) / ks);
+    const int spr = st1 - st0;
+    const int KBr = spr * (kStageK / kBlockK);
+    // this cluster's tiles: cid, cid + n_clusters, ...
+    const int n_tl = cid < p.n_tiles ? (p.n_tiles - cid + p.n_clusters - 1) / p.n_clusters : 0;
+    const int n_stages_total = n_tl * spr;
+    constexpr uint32_t kTmemCols = NMAT == 1 ? 256u : 512u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.S; ++s) {
+            mbar_init(&sh.full[s], kPrWarps * 32);
+            mbar_init(&sh.empty[s], kDqWarps);
+        }
+        for (int s = 0; s < kNW; ++s) {
+            mbar_init(&sh.w_full[s], kDqWarps);
+            mbar_init(&sh.w_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.acc_full[b], 1);
+            mbar_init(&sh.acc_empty[b], kEpWarps);
+        }
+        mbar_init(sh.act_ready, kDqWarps);
+        mbar_init(sh.red_full, ks);
+        mbar_init(sh.red_empty, ks);
+        mbar_init(sh.norm_full, ks);
+        mbar_init(sh.drain, 1);
+        *sh.abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(sh.tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *sh.tmem;
+    if (ks > 1) cluster_sync_all();  // peers' barriers are initialised
+
+    // tensor-memory columns: W slots, then two accumulators per matrix
+    auto w_col = [](int mat, int slot) { return (uint32_t)((mat * kNW + slot) * 32); };
+    auto acc_col = [](int mat, int b) { return (uint32_t)(NMAT * kNW * 32 + (mat * 2 + b) * 32); };
+
+    // =====================================================================
+    // Producer warps: codes (tensor-map copies) and per-row bf16 constants.
+    // =====================================================================
+    if (warp >= kPrBase / 32 && warp < kPrBase / 32 + kPrWarps) {
+        const int r = threadIdx.x - kPrBase;  // row of the tile
+        const bool row_in_tile = r < p.TR;
+        struct Regs {
+            float s[NMAT][kMaxGps], z[NMAT][kMaxGps];
+        };
+        // scales/zeros of stage i for this row (zeros past N or K)
+        auto load = [&](Regs &R, int i) {
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat)
+#pragma unroll
+                for (int gl = 0; gl < kMaxGps; ++gl) {
+                    R.s[mat][gl] = 0.0f;
+                    R.z[mat][gl] = 0.0f;
+                }
+            if (i >= n_stages_total || !row_in_tile) return;
+            const int tl = i / spr;
+            const int k0 = (st0 + (i - tl * spr)) * kStageK;
+            const int row = (cid + tl * p.n_clusters) * p.TR + r;
+            if (row >= p.N || k0 >= p.K) return;
+            const int g0 = k0 / p.gs;
+            const int g_last = (min(k0 + kStageK, p.K) - 1) / p.gs;
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat)
+#pragma unroll
+                for (int gl = 0; gl < kMaxGps; ++gl) {
+                    if (gl < p.gps && g0 + gl <= g_last) {
+                        const size_t e = (size_t)row * p.G + g0 + gl;
+                        R.s[mat][gl] = __ldg(p.scales[mat] + e);
+                        R.z[mat][gl] = __ldg(p.zeros[mat] + e);
+                    }
+                }
+        };
+        bool ok = true;
+        int issued = 0;
+        auto produce = [&](const Regs &R, int i) {
+            const int slot = i % p.S;
+            if (i >= p.S && !tc_wait(&sh.empty[slot], ((i / p.S) - 1) & 1, abort, false)) {
+                ok = false;
+                return;
+            }
+            unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+            if (r == 0) {
+                const int tl = i / spr;
+                const int k0 = (st0 + (i - tl * spr)) * kStageK;
+                const int row0 = (cid + tl * p.n_clusters) * p.TR;
+                mbar_expect_tx(&sh.full[slot], (uint32_t)NMAT * p.codes_bytes);
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat)
+                    tma_load_2d(stage + mat * p.codes_bytes, &p.codes[mat], k0 / 8, row0, &sh.full[slot]);
+            }
+            if (row_in_tile) {
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat) {
+                    uint4 *cst = reinterpret_cast<uint4 *>(stage + NMAT * p.codes_bytes + mat * p.cst_bytes);
+#pragma unroll
+                    for (int gl = 0; gl < kMaxGps; ++gl) {
+                        if (gl < p.gps) {
+                            const float s = R.s[mat][gl];
+                            const float z = R.z[mat][gl];
+                            const float zi = rintf(fminf(fmaxf(z, 0.0f), 15.0f));
+                            const float dzs = (zi - z) * s;
+                            uint4 c;
+                            c.x = bf16x2_pack(128.0f + zi, 128.0f + zi);
+                            c.y = bf16x2_pack(s, s);
+                            c.z = bf16x2_pack(dzs, dzs);
+                            c.w = 0u;
+                            cst[gl * 128 + r] = c;
+                        }
+                    }
+                }
+            }
+            mbar_arrive(&sh.full[slot]);
+            issued = i + 1;
+        };
+        Regs R0, R1;
+        load(R0, 0);
+        load(R1, 1);
+        for (int i = 0; ok && i < n_stages_total; i += 2) {
+            produce(R0, i);
+            if (!ok) break;
+            load(R0, i + 2);
+            if (i + 1 < n_stages_total) {
+                produce(R1, i + 1);
+                if (!ok) break;
+                load(R1, i + 3);
+            }
+        }
+        if (!ok && r == 0) {
+            // leave no copy in flight into this CTA's shared memory
+            for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
+                tc_drain_wait(&sh.full[i % p.S], (i / p.S) & 1);
+        }
+    }
+
+    // =====================================================================
+    // Dequant warps: activation staging first, then K-blocks into TMEM.
+    // =====================================================================
+    else if (warp < kDqWarps) {
+        const int tid = threadIdx.x;
+        const int k_base = st0 * kStageK;
+        const int n_chunks = KBr * 8;                 // 8-code chunks of this rank's K range
+        constexpr int TPL = (kDqWarps * 32) / MP;     // threads per lane row
+        const int m = tid / TPL;
+        const int sub = tid % TPL;
+        unsigned char *act = smem + p.off_act;
+        const bool writer = cid == 0;                 // cluster 0 writes the side outputs
+        bool ok = true;
+        if constexpr (NORM) {
+            // pass 1: x = A + A_b, its square sum over this rank's K range
+            float part = 0.0f;
+            if (m < p.M) {
+                for (int c = sub; c < n_chunks; c += TPL) {
+                    const int k = k_base + 8 * c;
+                    if (k >= p.K) break;
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
+                    float4 x0 = a4[0], x1 = a4[1];
+                    if (p.A_b) {
+                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + k);
+                        const float4 b0 = b4[0], b1 = b4[1];
+                        x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
+                        x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
+                    }
+                    if (writer && p.residual_out) {
+                        float4 *ro = reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + k);
+                        ro[0] = x0;
+                        ro[1] = x1;
+                    }
+                    part = fmaf(x0.x, x0.x, part); part = fmaf(x0.y, x0.y, part);
+                    part = fmaf(x0.z, x0.z, part); part = fmaf(x0.w, x0.w, part);
+                    part = fmaf(x1.x, x1.x, part); part = fmaf(x1.y, x1.y, part);
+                    part = fmaf(x1.z, x1.z, part); part = fmaf(x1.w, x1.w, part);
+                }
+            }
+            // fixed-order sum over the TPL threads of the row (consecutive lanes)
+#pragma unroll
+            for (int off = TPL / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (sub == 0) sh.part[m] = part;
+            fence_acq_rel_cluster();
+            named_barrier(1, kDqWarps * 32);
+            if (tid == 0) {
+                for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.norm_full), j));
+            }
+            ok = __all_sync(0xffffffffu, tc_wait(sh.norm_full, 0, abort, true));
+            float total = 0.0f;
+            if (ok && m < p.M) {
+                for (int j = 0; j < ks; ++j) total += dsmem_ld_f32(dsmem_addr(smem_addr(&sh.part[m]), j));
+            }
+            const float inv = 1.0f / sqrtf(total / (float)p.K + p.eps);
+            // pass 2: a = x * inv * W_norm, to bf16
+            for (int c = sub; c < n_chunks; c += TPL) {
+                const int k = k_base + 8 * c;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (ok && m < p.M && k < p.K) {
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
+                    float4 x0 = a4[0], x1 = a4[1];
+                    if (p.A_b) {
+                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + k);
+                        const float4 b0 = b4[0], b1 = b4[1];
+                        x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
+                        x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
+                    }
+                    const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + k);
+                    const float4 g0 = w4[0], g1 = w4[1];
+                    x0.x = (x0.x * inv) * g0.x; x0.y = (x0.y * inv) * g0.y;
+                    x0.z = (x0.z * inv) * g0.z; x0.w = (x0.w * inv) * g0.w;
+                    x1.x = (x1.x * inv) * g1.x; x1.y = (x1.y * inv) * g1.y;
+                    x1.z = (x1.z * inv) * g1.z; x1.w = (x1.w * inv) * g1.w;
+                    if (writer && p.norm_out) {
+                        float4 *no = reinterpret_cast<float4 *>(p.norm_out + (size_t)m * p.K + k);
+                        no[0] = x0;
+                        no[1] = x1;
+                    }
+                    v = pack_chunk(x0, x1);
+                }
+                *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) = v;
+            }
+        } else {
+            for (int c = sub; c < n_chunks; c += TPL) {
+                const int k = k_base + 8 * c;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (m < p.M && k < p.K) {
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
+                    v = pack_chunk(a4[0], a4[1]);
+                }
+                *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sh.act_ready);
+
+        // ---- K-blocks ----
+        const int q4 = warp & 3;
+        const int h = warp >> 2;
+        const int r = 32 * q4 + lane;
+        const bool warp_live = 32 * q4 < p.TR;   // warp-uniform
+        const bool row_in_tile = r < p.TR;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const uint32_t magic = p.magic_bf16;
+        int kbg = 0;  // K-blocks so far (tensor-memory slot sequence)
+        for (int i = 0; ok && i < n_stages_total; ++i) {
+            const int slot = i % p.S;
+            // warp-uniform outcome: the collective tensor-memory stores below
+            // need every lane
+            if (!__all_sync(0xffffffffu, tc_wait(&sh.full[slot], (i / p.S) & 1, abort, false))) {
+                ok = false;
+                break;
+            }
+            const int tl = i / spr;
+            const int k0 = (st0 + (i - tl * spr)) * kStageK;
+            const int g0 = k0 / p.gs;
+            const unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+#pragma unroll 1
+            for (int j = 0; j < kStageK / kBlockK; ++j, ++kbg) {
+                const int ws = kbg % kNW;
+                if (kbg >= kNW &&
+                    !__all_sync(0xffffffffu, tc_wait(&sh.w_empty[ws], ((kbg / kNW) - 1) & 1, abort, false))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (warp_live) {
+                    const int gl = (k0 + j * kBlockK + 32 * h) / p.gs - g0;
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+                        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+                        uint4 cs = make_uint4(0x43004300u, 0u, 0u, 0u);
+                        if (row_in_tile) {
+                            const unsigned char *cb = stage + mat * p.codes_bytes;
+                            wv = *reinterpret_cast<const uint4 *>(cb + r * 128 + (((2 * j + h) ^ (r & 7)) << 4));
+                            cs = reinterpret_cast<const uint4 *>(stage + NMAT * p.codes_bytes + mat * p.cst_bytes)[gl * 128 + r];
+                        }
+                        uint32_t o[16];
+                        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const uint32_t w = words[wi];
+                            const uint32_t t0 = bf16_code_pair(w, magic);
+                            const uint32_t t1 = bf16_code_pair(w >> 4, magic);
+                            const uint32_t t2 = bf16_code_pair(w >> 8, magic);
+                            const uint32_t t3 = bf16_code_pair(w >> 12, magic);
+                            o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(t0, cs.x), cs.y, cs.z);
+                            o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(t1, cs.x), cs.y, cs.z);
+                            o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(t2, cs.x), cs.y, cs.z);
+                            o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(t3, cs.x), cs.y, cs.z);
+                        }
+                        tmem_st16(tmem_base + lane_off + w_col(mat, ws) + 16 * h, o);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.w_full[ws]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[slot]);
+        }
+    }
+
+    // =====================================================================
+    // MMA warp (one thread issues).
+    // =====================================================================
+    else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, MP);
+            const uint32_t act_s = smem_addr(smem + p.off_act);
+            bool ok = tc_wait(sh.act_ready, 0, abort, false);
+            bool any = false;
+            int kbg = 0;
+            for (int tl = 0; ok && tl < n_tl; ++tl) {
+                const int b = tl & 1;
+                if (tl >= 2 && !tc_wait(&sh.acc_empty[b], ((tl >> 1) - 1) & 1, abort, false)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                for (int kb = 0; kb < KBr; ++kb, ++kbg) {
+                    const int ws = kbg % kNW;
+                    if (!tc_wait(&sh.w_full[ws], (kbg / kNW) & 1, abort, false)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+#pragma unroll
+                        for (int jj = 0; jj < kBlockK / 16; ++jj) {
+                            const uint64_t bdesc =
+                                smem_desc_sw128(act_s + (uint32_t)kb * (MP * 128) + jj * 32, 1024);
+                            tc_mma_ts(tmem_base + acc_col(mat, b), tmem_base + w_col(mat, ws) + 8 * jj,
+                                      bdesc, idesc, (kb | jj) != 0 ? 1u : 0u);
+                        }
+                    }
+                    any = true;
+                    tc_commit(&sh.w_empty[ws]);
+                }
+                if (!ok) break;
+                tc_commit(&sh.acc_full[b]);
+            }
+            if (!ok && any) {
+                // let the MMAs in flight finish before tensor memory is freed
+                tc_commit(sh.drain);
+                tc_drain_wait(sh.drain, 0);
+            }
+        }
+        __syncwarp();
+    }
+
+    // =====================================================================
+    // Epilogue warps: accumulator -> (cluster split-K sum) -> outputs.
+    // =====================================================================
+    else {
+        const int et = threadIdx.x - kEpBase;  // 0..127
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        float *red = reinterpret_cast<float *>(smem + p.off_red);
+        // A thread whose wait fails keeps walking the loop (skipping work) so
+        // that the group's named barriers are always reached by all 128.
+        bool ok = true;
+        for (int tl = 0; tl < n_tl; ++tl) {
+            const int b = tl & 1;
+            if (ok) ok = __all_sync(0xffffffffu, tc_wait(&sh.acc_full[b], (tl >> 1) & 1, abort, false));
+            float v[NMAT][MP];
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat) {
+#pragma unroll
+                    for (int c = 0; c < MP / 16; ++c) {
+                        uint32_t u[16];
+                        tmem_ld16(tmem_base + lane_off + acc_col(mat, b) + 16 * c, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[mat][16 * c + e] = __uint_as_float(u[e]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.acc_empty[b]);
+            }
+            const int row0 = (cid + tl * p.n_clusters) * p.TR;
+            if (ks == 1) {
+                const int col = row0 + r;
+                if (ok && r < p.TR && col < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (m < p.M) store_out<EPI>(p, m, col, v[0][m], v[NMAT - 1][m]);
+                    }
+                }
+                continue;
+            }
+            // split-K: partial tile to shared memory, then every rank sums its
+            // share of the rows over all ranks in rank order
+            if (ok && tl >= 1) ok = tc_wait(sh.red_empty, (tl - 1) & 1, abort, true);
+            if (ok) {
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat)
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) red[(mat * MP + m) * 128 + r] = v[mat][m];
+            }
+            fence_acq_rel_cluster();
+            named_barrier(2, kEpWarps * 32);
+            if (et == 0) {
+                for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.red_full), j));
+            }
+            if (ok) ok = tc_wait(sh.red_full, tl & 1, abort, true);
+            if (ok) {
+                const int sh0 = p.TR * rank / ks;
+                const int sh1 = p.TR * (rank + 1) / ks;
+                const int rows = sh1 - sh0;
+                const uint32_t red_s = smem_addr(red);
+                for (int idx = et; idx < rows * p.M; idx += kEpWarps * 32) {
+                    const int m = idx / rows;
+                    const int rr = sh0 + (idx - m * rows);
+                    const int col = row0 + rr;
+                    if (col >= p.N) continue;
+                    float sum[NMAT];
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+                        const uint32_t off = (uint32_t)(((mat * MP + m) * 128 + rr) * 4);
+                        float acc = 0.0f;
+                        for (int j = 0; j < ks; ++j) acc += dsmem_ld_f32(dsmem_addr(red_s + off, j));
+                        sum[mat] = acc;
+                    }
+                    store_out<EPI>(p, m, col, sum[0], sum[NMAT - 1]);
+                }
+            }
+            named_barrier(2, kEpWarps * 32);
+            if (et == 0) {
+                for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.red_empty), j));
+            }
+        }
+        // every peer has finished reading this CTA's last partial tile
+        if (ks > 1 && n_tl > 0) (void)tc_wait(sh.red_empty, (n_tl - 1) & 1, abort, true);
+    }
+
+    // ---- teardown ----
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if (ks > 1) cluster_sync_all();  // no peer reads this CTA's shared memory any more
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+uint32_t round_up(uint32_t x, uint32_t a)
+{
+    return (x + a - 1) / a * a;
+}
+
+struct TcPlan {
+    int ks, TR, n_tiles, n_clusters, S, gps;
+    uint32_t smem;
+};
+
+// Most scale groups one 256-code stage (starting at a multiple of 256) spans,
+// counted without clipping at K, so every K-block of a stage -- including
+// those past K in the last stage -- finds its constant row in the stage.
+int groups_per_stage(int gs)
+{
+    int most = 1;
+    for (int k0 = 0; k0 < kStageK * gs; k0 += kStageK) {
+        const int g = (k0 + kStageK - 1) / gs - k0 / gs + 1;
+        most = g > most ? g : most;
+        if (k0 % gs == 0 && k0 > 0) break;  // the pattern repeats
+    }
+    return most;
+}
+
+constexpr int kMaxDevices = 64;
+
+// Co-resident clusters of `ks` one-CTA-per-SM blocks (queried once per device).
+int max_clusters(int dev, int ks, const void *kern)
+{
+    static std::atomic<int> cache[kMaxDevices][9];
+    static std::once_flag init_flag;
+    std::call_once(init_flag, []() {
+        for (int d = 0; d < kMaxDevices; ++d)
+            for (int k = 0; k < 9; ++k) cache[d][k].store(-1);
+    });
+    if (dev < 0 || dev >= kMaxDevices || ks < 1 || ks > 8) return 0;
+    int v = cache[dev][ks].load(std::memory_order_acquire);
+    if (v >= 0) return v;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cfg.gridDim = dim3((unsigned)(sms / ks * ks > 0 ? sms / ks * ks : ks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 200u * 1024u;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    cache[dev][ks].store(n, std::memory_order_release);
+    return n;
+}
+
+bool plan_tc(const Call &call, int MP, int dev, const void *kern, int smem_optin, TcPlan &best)
+{
+    const int n_st = (call.K + kStageK - 1) / kStageK;
+    const int gps = groups_per_stage(call.gs);
+    if (gps > kMaxGps) return false;
+    const int nmat = call.nmat;
+    double best_cost = 0.0;
+    bool found = false;
+    for (int ks = 1; ks <= 8 && ks <= n_st; ++ks) {
+        const int clusters_max = max_clusters(dev, ks, kern);
+        if (clusters_max <= 0) continue;
+        const int spr_max = (n_st + ks - 1) / ks;
+        const uint32_t act = (uint32_t)spr_max * (kStageK / kBlockK) * MP * 128u;
+        const uint32_t red = ks > 1 ? (uint32_t)nmat * MP * 128u * 4u : 0u;
+        for (int TR = 128; TR >= 16; TR -= 8) {
+            const uint32_t codes = (uint32_t)TR * 128u;
+            const uint32_t cst = (uint32_t)gps * 128u * 16u;
+            const uint32_t stage = round_up((uint32_t)nmat * (codes + cst), 1024u);
+            const uint32_t fixed = 1024u + act + round_up(red, 1024u) + 1024u;
+            if (fixed + 2u * stage > (uint32_t)smem_optin) continue;
+            int S = (int)(((uint32_t)smem_optin - fixed) / stage);
+            if (S > kMaxStages) S = kMaxStages;
+            const int n_tiles = (call.N + TR - 1) / TR;
+            const int clusters = n_tiles < clusters_max ? n_tiles : clusters_max;
+            const int waves = (n_tiles + clusters - 1) / clusters;
+            // critical-path work of one CTA, in codes: its tiles' share of K,
+            // the per-tile pipeline fill and epilogue, and the activation staging
+            const double per_tile = (double)TR * spr_max * kStageK * nmat + 24576.0 * nmat;
+            const double staging = (double)spr_max * kStageK * MP * (call.norm ? 3.0 : 1.5);
+            const double cost = waves * per_tile + staging;
+            if (!found || cost < best_cost * 0.999) {
+                found = true;
+                best_cost = cost;
+                best.ks = ks;
+                best.TR = TR;
+                best.n_tiles = n_tiles;
+                best.n_clusters = clusters;
+                best.S = S;
+                best.gps = gps;
+                uint32_t smem = fixed + (uint32_t)S * stage;
+                best.smem = smem < kMinSmem ? kMinSmem : smem;
+            }
+        }
+    }
+    return found;
+}
+
+template <int MP, int NMAT, bool NORM, int EPI>
+cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
+{
+    auto kern = tc_matvec_kernel<MP, NMAT, NORM, EPI>;
+    int dev = 0;
+    cudaError_t err;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    int optin = 0;
+    if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return err;
+    // the 1024-byte alignment pad is part of every plan
+    static std::atomic<unsigned char> ready[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices || !ready[dev].load(std::memory_order_acquire)) {
+        if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)) != cudaSuccess)
+            return err;
+        if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_release);
+    }
+    TcPlan pl{};
+    if (!plan_tc(call, MP, dev, reinterpret_cast<const void *>(kern), optin, pl)) return cudaErrorInvalidValue;
+
+    TcParams prm{};
+    EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return cudaErrorNotSupported;
+    for (int mat = 0; mat < NMAT; ++mat) {
+        const cuuint64_t dims[2] = {(cuuint64_t)(call.K / 8), (cuuint64_t)call.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)call.K / 2};
+        const cuuint32_t box[2] = {32u, (cuuint32_t)pl.TR};
+        const cuuint32_t estr[2] = {1u, 1u};
+        if (encode(&prm.codes[mat], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2,
+                   const_cast<uint32_t *>(call.Bq[mat]), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    prm.M = call.M;
+    prm.K = call.K;
+    prm.N = call.N;
+    prm.gs = call.gs;
+    prm.G = call.K / call.gs;
+    prm.TR = pl.TR;
+    prm.n_tiles = pl.n_tiles;
+    prm.n_clusters = pl.n_clusters;
+    prm.ks = pl.ks;
+    prm.n_st = (call.K + kStageK - 1) / kStageK;
+    prm.S = pl.S;
+    prm.gps = pl.gps;
+    const int spr_max = (prm.n_st + pl.ks - 1) / pl.ks;
+    prm.codes_bytes = (uint32_t)pl.TR * 128u;
+    prm.cst_bytes = (uint32_t)pl.gps * 128u * 16u;
+    prm.stage_bytes = round_up((uint32_t)NMAT * (prm.codes_bytes + prm.cst_bytes), 1024u);
+    prm.off_act = 0;
+    const uint32_t act = (uint32_t)spr_max * (kStageK / kBlockK) * MP * 128u;
+    const uint32_t red = pl.ks > 1 ? (uint32_t)NMAT * MP * 128u * 4u : 0u;
+    prm.off_ring = round_up(act, 1024u);
+    prm.off_red = prm.off_ring + (uint32_t)pl.S * prm.stage_bytes;
+    prm.off_misc = prm.off_red + round_up(red, 1024u);
+    prm.off_bar = prm.off_misc + 256u;
+    if (prm.off_bar + 64u * 8u + 1024u > pl.smem) return cudaErrorInvalidValue;
+    prm.magic_bf16 = 0x43004300u;
+    prm.A = call.A;
+    if (call.norm) {
+        prm.A_b = call.norm->A_b;
+        prm.W_norm = call.norm->W_norm;
+        prm.eps = call.norm->eps;
+        prm.residual_out = call.norm->residual_out;
+        prm.norm_out = call.norm->norm_out;
+    }
+    for (int mat = 0; mat < 2; ++mat) {
+        const int src = mat < call.nmat ? mat : 0;
+        prm.scales[mat] = call.scales[src];
+        prm.zeros[mat] = call.zeros[src];
+    }
+    for (int i = 0; i < 4; ++i) {
+        prm.out[i] = call.out[i];
+        prm.seg_start[i] = call.seg_start[i];
+        prm.seg_len[i] = call.seg_len[i];
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(pl.n_clusters * pl.ks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, kern, prm)) != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+template <int MP>
+cudaError_t dispatch_tc(const Call &call, cudaStream_t stream)
+{
+    const bool norm = call.norm != nullptr;
+    switch (call.epi) {
+    case kEpiStore:
+        return norm ? launch_tc_variant<MP, 1, true, kEpiStore>(call, stream)
+                    : launch_tc_variant<MP, 1, false, kEpiStore>(call, stream);
+    case kEpiQuad:
+        return launch_tc_variant<MP, 1, false, kEpiQuad>(call, stream);
+    case kEpiGated:
+        return norm ? launch_tc_variant<MP, 2, true, kEpiGated>(call, stream)
+                    : launch_tc_variant<MP, 2, false, kEpiGated>(call, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool tc_path_supported(const Call &call)
+{
+    if (call.M < 16 || call.M > 32) return false;
+    if (groups_per_stage(call.gs) > kMaxGps) return false;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3 && encode_tiled_fn() != nullptr;
+}
+
+cudaError_t launch_tc(const Call &call, cudaStream_t stream)
+{
+    return call.M == 16 ? dispatch_tc<16>(call, stream) : dispatch_tc<32>(call, stream);
+}
+
+cudaError_t read_tc_device_error(unsigned int *bits, bool clear)
+{
+    cudaError_t err = cudaMemcpyFromSymbol(bits, g_tc_error, sizeof(unsigned int));
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace gq4

@@ -224,7 +224,8 @@ def dequant(Bq, scales, zeros, K, group_size, W=None, stream=None):
 
 
 def device_error(clear: bool = True) -> int:
-    """The library's sticky device error word (bit 0: a bounded wait for a bulk copy expired)."""
+    """The library's sticky device error bits (bit 0: the one-lane kernel, bit 1: the
+    tensor-core kernel gave up a bounded wait)."""
     bits = ctypes.c_uint(0)
     _check(lib.gq4_device_error(ctypes.byref(bits), int(clear)), "gq4_device_error")
     return int(bits.value)
