@@ -14,13 +14,17 @@
 //     block cluster of KS CTAs owns a tile; its CTAs split K in whole 256-code
 //     stages, and their f32 partial tiles are summed through distributed
 //     shared memory in rank order (deterministic, no global scratch).
-//   * Producer warps (4): one thread issues a 2-D tensor-map copy of the
-//     tile's packed codes for a stage (TR rows x 128 bytes, 128-byte swizzle,
-//     zero fill past K and N); every thread owns one row and turns that row's
-//     scales and zeros for the stage into bf16 pairs (128 + zi, s, (zi-z)*s),
-//     loaded two stages ahead.
+//   * Producer warp: lane 0 issues a 2-D tensor-map copy of the tile's packed
+//     codes for a stage (TR rows x 128 bytes, 128-byte swizzle, zero fill
+//     past K and N) as soon as a ring slot is free; the 32 lanes copy the
+//     stage's raw scales and zeros with 4-byte cp.async (zero fill past N and
+//     K), whose completion arrives on the same barrier as the tensor copy.
+//     (Scale rows of K/gs floats need not be 16-byte multiples, so they are
+//     not described by a tensor map.)
 //   * Dequant warps (8): two per TMEM lane quarter.  A thread owns one row
-//     and half of each 64-code K-block: per word, four LOP3 magic extractions
+//     and half of each 64-code K-block; when its scale group changes it turns
+//     (s, z) into bf16 pairs (128 + zi, s, (zi - z) * s) with zi =
+//     round(clamp(z, 0, 15)).  Per word, four LOP3 magic extractions
 //     give bf16 pairs (128+q), an exact bf16 subtraction gives q - zi, and an
 //     fma gives (q - zi)*s + (zi - z)*s = (q - z)*s rounded once to bf16.  The
 //     16 results go straight to tensor memory (tcgen05.st): the dequantized
@@ -57,12 +61,12 @@ namespace {
 
 constexpr int kDqWarps = 8;     // warps 0..7
 constexpr int kEpWarps = 4;     // warps 8..11
-constexpr int kPrWarps = 4;     // warps 12..15
-constexpr int kMmaWarp = 16;    // warp 16
-constexpr int kThreads = 17 * 32;
+constexpr int kPrWarp = 12;     // warp 12
+constexpr int kMmaWarp = 13;    // warp 13
+constexpr int kThreads = 14 * 32;
 constexpr int kEpBase = kDqWarps * 32;
-constexpr int kPrBase = (kDqWarps + kEpWarps) * 32;
-constexpr int kNW = 4;          // tensor-memory slots of dequantized K-blocks
+constexpr int kMaxNW = 8;       // tensor-memory slots of dequantized K-blocks (most)
+constexpr int kMaxKs = 8;       // CTAs per cluster (split-K ranks), most
 constexpr int kStageK = 256;    // codes per stage along K
 constexpr int kBlockK = 64;     // codes per K-block (one 128-byte bf16 row)
 constexpr int kMaxStages = 16;
@@ -71,13 +75,19 @@ constexpr uint32_t kMinSmem = 120u * 1024u;  // forces one CTA per SM (tensor me
 
 struct TcParams {
     CUtensorMap codes[2];          // [N][K/8] u32, box {32, TR}, 128-byte swizzle
+    CUtensorMap sz[2][2];          // scales / zeros [mat][s|z] as super-rows of P rows:
+                                   // [Q][P*G] f32, box {BW, TR/P}
     int M, K, N, gs, G;
     int TR;                        // rows per tile
     int n_tiles, n_clusters, ks;
     int n_st;                      // stages over K
     int S;                         // ring depth
-    int gps;                       // constant rows per stage (max groups a stage touches)
-    uint32_t off_act, off_ring, stage_bytes, codes_bytes, cst_bytes;
+    int gps;                       // most groups a stage touches
+    int P, Q, BW;                  // rows per super-row, whole super-rows, box width (groups)
+    int logP;                      // log2(P)
+    unsigned long long gmagic;     // ceil(2^40 / (gs/32)): chunk index -> group, exactly
+    uint32_t off_act, off_ring, stage_bytes, codes_bytes;
+    uint32_t sz_box_bytes, sz_box_stride, off_sz, off_tail;
     uint32_t off_red, off_misc, off_bar;
     uint32_t magic_bf16;           // 0x43004300, read from the parameter bank
     const float *A;
@@ -137,6 +147,12 @@ __device__ __forceinline__ void tc_drain_wait(uint64_t *bar, uint32_t parity)
     (void)mbar_wait(bar, parity);
 }
 
+// Scale group of 32-code chunk c (c < 2^19): c / (gs/32) by multiply-shift.
+__device__ __forceinline__ int chunk_group(int c, unsigned long long gmagic)
+{
+    return (int)(((unsigned long long)c * gmagic) >> 40);
+}
+
 // Output epilogue for one (lane, column).
 template <int EPI>
 __device__ __forceinline__ void store_out(const TcParams &p, int m, int col, float v0, float v1)
@@ -184,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         sh.full = b;
         sh.empty = b + kMaxStages;
         sh.w_full = b + 2 * kMaxStages;
-        sh.w_empty = sh.w_full + kNW;
-        sh.acc_full = sh.w_empty + kNW;
+        sh.w_empty = sh.w_full + kMaxNW;
+        sh.acc_full = sh.w_empty + kMaxNW;
         sh.acc_empty = sh.acc_full + 2;
         sh.act_ready = sh.acc_empty + 2;
         sh.red_full = sh.act_ready + 1;
@@ -211,11 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
     // this cluster's tiles: cid, cid + n_clusters, ...
     const int n_tl = cid < p.n_tiles ? (p.n_tiles - cid + p.n_clusters - 1) / p.n_clusters : 0;
     const int n_stages_total = n_tl * spr;
-    constexpr uint32_t kTmemCols = NMAT == 1 ? 256u : 512u;
+    // tensor memory: kNW dequantized K-blocks per matrix, two accumulators per matrix
+    constexpr int kNW = NMAT == 1 ? 8 : 6;
+    constexpr uint32_t kTmemCols = 512u;
+    static_assert(NMAT * kNW * 32 + NMAT * 2 * 32 <= (int)kTmemCols, "tensor-memory map");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.S; ++s) {
-            mbar_init(&sh.full[s], kPrWarps * 32);
+            mbar_init(&sh.full[s], 32);  // the producer lanes' cp.async arrivals
             mbar_init(&sh.empty[s], kDqWarps);
         }
         for (int s = 0; s < kNW; ++s) {
@@ -242,104 +261,90 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *sh.tmem;
-    if (ks > 1) cluster_sync_all();  // peers' barriers are initialised
+    // Cluster barrier in two halves: every thread arrives now; a thread waits
+    // (peers' barriers initialised) only before its first access to a peer,
+    // so the copies start at once.
+    if (ks > 1) cluster_arrive();
+    bool cwaited = false;
 
     // tensor-memory columns: W slots, then two accumulators per matrix
-    auto w_col = [](int mat, int slot) { return (uint32_t)((mat * kNW + slot) * 32); };
-    auto acc_col = [](int mat, int b) { return (uint32_t)(NMAT * kNW * 32 + (mat * 2 + b) * 32); };
+    auto w_col = [&](int mat, int slot) { return (uint32_t)((mat * kNW + slot) * 32); };
+    auto acc_col = [&](int mat, int b) { return (uint32_t)(NMAT * kNW * 32 + (mat * 2 + b) * 32); };
 
     // =====================================================================
-    // Producer warps: codes (tensor-map copies) and per-row bf16 constants.
+    // Producer warp: codes, scales and zeros (tensor-map copies; cp.async
+    // for the at most P-1 rows past the last whole super-row).
     // =====================================================================
-    if (warp >= kPrBase / 32 && warp < kPrBase / 32 + kPrWarps) {
-        const int r = threadIdx.x - kPrBase;  // row of the tile
-        const bool row_in_tile = r < p.TR;
-        struct Regs {
-            float s[NMAT][kMaxGps], z[NMAT][kMaxGps];
-        };
-        // scales/zeros of stage i for this row (zeros past N or K)
-        auto load = [&](Regs &R, int i) {
+    if (warp == kPrWarp) {
+        if (lane == 0) {
 #pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-                for (int gl = 0; gl < kMaxGps; ++gl) {
-                    R.s[mat][gl] = 0.0f;
-                    R.z[mat][gl] = 0.0f;
-                }
-            if (i >= n_stages_total || !row_in_tile) return;
-            const int tl = i / spr;
-            const int k0 = (st0 + (i - tl * spr)) * kStageK;
-            const int row = (cid + tl * p.n_clusters) * p.TR + r;
-            if (row >= p.N || k0 >= p.K) return;
-            const int g0 = k0 / p.gs;
-            const int g_last = (min(k0 + kStageK, p.K) - 1) / p.gs;
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-                for (int gl = 0; gl < kMaxGps; ++gl) {
-                    if (gl < p.gps && g0 + gl <= g_last) {
-                        const size_t e = (size_t)row * p.G + g0 + gl;
-                        R.s[mat][gl] = __ldg(p.scales[mat] + e);
-                        R.z[mat][gl] = __ldg(p.zeros[mat] + e);
-                    }
-                }
-        };
-        bool ok = true;
-        int issued = 0;
-        auto produce = [&](const Regs &R, int i) {
-            const int slot = i % p.S;
-            if (i >= p.S && !tc_wait(&sh.empty[slot], ((i / p.S) - 1) & 1, abort, false)) {
-                ok = false;
-                return;
-            }
-            unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
-            if (r == 0) {
-                const int tl = i / spr;
-                const int k0 = (st0 + (i - tl * spr)) * kStageK;
-                const int row0 = (cid + tl * p.n_clusters) * p.TR;
-                mbar_expect_tx(&sh.full[slot], (uint32_t)NMAT * p.codes_bytes);
-#pragma unroll
-                for (int mat = 0; mat < NMAT; ++mat)
-                    tma_load_2d(stage + mat * p.codes_bytes, &p.codes[mat], k0 / 8, row0, &sh.full[slot]);
-            }
-            if (row_in_tile) {
-#pragma unroll
-                for (int mat = 0; mat < NMAT; ++mat) {
-                    uint4 *cst = reinterpret_cast<uint4 *>(stage + NMAT * p.codes_bytes + mat * p.cst_bytes);
-#pragma unroll
-                    for (int gl = 0; gl < kMaxGps; ++gl) {
-                        if (gl < p.gps) {
-                            const float s = R.s[mat][gl];
-                            const float z = R.z[mat][gl];
-                            const float zi = rintf(fminf(fmaxf(z, 0.0f), 15.0f));
-                            const float dzs = (zi - z) * s;
-                            uint4 c;
-                            c.x = bf16x2_pack(128.0f + zi, 128.0f + zi);
-                            c.y = bf16x2_pack(s, s);
-                            c.z = bf16x2_pack(dzs, dzs);
-                            c.w = 0u;
-                            cst[gl * 128 + r] = c;
-                        }
-                    }
-                }
-            }
-            mbar_arrive(&sh.full[slot]);
-            issued = i + 1;
-        };
-        Regs R0, R1;
-        load(R0, 0);
-        load(R1, 1);
-        for (int i = 0; ok && i < n_stages_total; i += 2) {
-            produce(R0, i);
-            if (!ok) break;
-            load(R0, i + 2);
-            if (i + 1 < n_stages_total) {
-                produce(R1, i + 1);
-                if (!ok) break;
-                load(R1, i + 3);
+            for (int mat = 0; mat < NMAT; ++mat) {
+                prefetch_tensormap(&p.codes[mat]);
+                prefetch_tensormap(&p.sz[mat][0]);
+                prefetch_tensormap(&p.sz[mat][1]);
             }
         }
-        if (!ok && r == 0) {
+        bool ok = true;
+        int issued = 0;
+        // ring position and (tile, stage-in-rank) of stage i, kept incrementally
+        int slot = 0, phase = 0, tl = 0, sir = 0;
+        for (int i = 0; i < n_stages_total; ++i) {
+            if (i >= p.S) {
+                bool got = true;
+                if (lane == 0) got = tc_wait(&sh.empty[slot], phase ^ 1, abort, false);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+            const int k0 = (st0 + sir) * kStageK;
+            const int row0 = (cid + tl * p.n_clusters) * p.TR;
+            const int g0 = chunk_group(k0 >> 5, p.gmagic);
+            if (lane == 0) {
+                mbar_expect_tx(&sh.full[slot], (uint32_t)NMAT * (p.codes_bytes + 2u * p.P * p.sz_box_bytes));
+#pragma unroll
+                for (int mat = 0; mat < NMAT; ++mat) {
+                    tma_load_2d(stage + mat * p.codes_bytes, &p.codes[mat], k0 / 8, row0, &sh.full[slot]);
+#pragma unroll
+                    for (int arr = 0; arr < 2; ++arr)
+                        for (int rho = 0; rho < p.P; ++rho) {
+                            const int x = (rho * p.G + g0) & ~3;
+                            tma_load_2d(stage + p.off_sz + ((mat * 2 + arr) * p.P + rho) * p.sz_box_stride,
+                                        &p.sz[mat][arr], x, row0 >> p.logP, &sh.full[slot]);
+                        }
+                }
+            }
+            // rows past the last whole super-row (only in the last tile)
+            const int tail0 = p.P * p.Q;
+            if (tail0 < p.N && row0 + p.TR > tail0) {
+                const int n_tail = p.N - tail0;  // < P
+                const int g_last = chunk_group((min(k0 + kStageK, p.K) - 1) >> 5, p.gmagic);
+                const int per = n_tail * p.gps;
+                for (int it = lane; it < NMAT * 2 * per; it += 32) {
+                    const int ma = it / per;            // mat * 2 + arr
+                    const int rem = it - ma * per;
+                    const int t = rem / p.gps;
+                    const int gl = rem - t * p.gps;
+                    const int off = (t * p.G + g0) & 3;
+                    const bool valid = k0 < p.K && g0 + gl <= g_last;
+                    const float *src = (ma & 1) ? p.zeros[ma >> 1] : p.scales[ma >> 1];
+                    float *d = reinterpret_cast<float *>(stage + p.off_tail) + (ma * 4 + t) * p.BW + off + gl;
+                    cp_async_4(d, src + (valid ? (size_t)(tail0 + t) * p.G + g0 + gl : 0), valid);
+                }
+            }
+            cp_async_mbar_arrive(&sh.full[slot]);
+            issued = i + 1;
+            if (++slot == p.S) {
+                slot = 0;
+                phase ^= 1;
+            }
+            if (++sir == spr) {
+                sir = 0;
+                ++tl;
+            }
+        }
+        if (!ok && lane == 0) {
             // leave no copy in flight into this CTA's shared memory
             for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
                 tc_drain_wait(&sh.full[i % p.S], (i / p.S) & 1);
@@ -357,41 +362,76 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         const int m = tid / TPL;
         const int sub = tid % TPL;
         unsigned char *act = smem + p.off_act;
-        const bool writer = cid == 0;                 // cluster 0 writes the side outputs
+        // the norm's side outputs are written once, spread over the clusters:
+        // chunk c of lane m by cluster (m * n_chunks + c) mod n_clusters
+        auto writer = [&](int mm, int c) { return (mm * n_chunks + c) % p.n_clusters == cid; };
         bool ok = true;
         if constexpr (NORM) {
-            // pass 1: x = A + A_b, its square sum over this rank's K range
-            float part = 0.0f;
-            if (m < p.M) {
-                for (int c = sub; c < n_chunks; c += TPL) {
+            // One pass over A and A_b: x = A + A_b to bf16 in place (and x
+            // itself to residual_out), its square sum; then the staged x is
+            // scaled by the inverse RMS and the gain in place.  The operand is
+            // thus bf16(bf16(x) * inv * W) on every cluster; norm_out is
+            // written exactly, in f32, from x recomputed.
+            constexpr int kU = 4;
+            const size_t row_off = (size_t)(m < p.M ? m : 0) * p.K;
+            auto load_x = [&](int c0, float4 (&x)[kU][2]) {
+                float4 b[kU][2];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + u * TPL;
                     const int k = k_base + 8 * c;
-                    if (k >= p.K) break;
-                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
-                    float4 x0 = a4[0], x1 = a4[1];
-                    if (p.A_b) {
-                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + k);
-                        const float4 b0 = b4[0], b1 = b4[1];
-                        x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
-                        x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
+                    const bool in = c < n_chunks && m < p.M && k < p.K;
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + row_off + (in ? k : 0));
+                    const float4 *b4 = reinterpret_cast<const float4 *>(
+                        (p.A_b ? p.A_b : p.A) + row_off + (in ? k : 0));
+                    const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    x[u][0] = in ? __ldg(a4) : z4;
+                    x[u][1] = in ? __ldg(a4 + 1) : z4;
+                    b[u][0] = in && p.A_b ? __ldg(b4) : z4;
+                    b[u][1] = in && p.A_b ? __ldg(b4 + 1) : z4;
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        x[u][v].x += b[u][v].x; x[u][v].y += b[u][v].y;
+                        x[u][v].z += b[u][v].z; x[u][v].w += b[u][v].w;
                     }
-                    if (writer && p.residual_out) {
-                        float4 *ro = reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + k);
-                        ro[0] = x0;
-                        ro[1] = x1;
+            };
+            float part = 0.0f;
+            for (int c0 = sub; c0 < n_chunks; c0 += kU * TPL) {
+                float4 x[kU][2];
+                load_x(c0, x);
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + u * TPL;
+                    if (c >= n_chunks) continue;
+                    const int k = k_base + 8 * c;
+                    if (p.residual_out && m < p.M && k < p.K && writer(m, c)) {
+                        float4 *ro = reinterpret_cast<float4 *>(p.residual_out + row_off + k);
+                        ro[0] = x[u][0];
+                        ro[1] = x[u][1];
                     }
-                    part = fmaf(x0.x, x0.x, part); part = fmaf(x0.y, x0.y, part);
-                    part = fmaf(x0.z, x0.z, part); part = fmaf(x0.w, x0.w, part);
-                    part = fmaf(x1.x, x1.x, part); part = fmaf(x1.y, x1.y, part);
-                    part = fmaf(x1.z, x1.z, part); part = fmaf(x1.w, x1.w, part);
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        part = fmaf(x[u][v].x, x[u][v].x, part);
+                        part = fmaf(x[u][v].y, x[u][v].y, part);
+                        part = fmaf(x[u][v].z, x[u][v].z, part);
+                        part = fmaf(x[u][v].w, x[u][v].w, part);
+                    }
+                    *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) =
+                        pack_chunk(x[u][0], x[u][1]);
                 }
             }
             // fixed-order sum over the TPL threads of the row (consecutive lanes)
 #pragma unroll
             for (int off = TPL / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
             if (sub == 0) sh.part[m] = part;
-            fence_acq_rel_cluster();
             named_barrier(1, kDqWarps * 32);
+            if (ks > 1) cluster_wait();  // peers' barriers are initialised
+            cwaited = true;
             if (tid == 0) {
+                fence_acq_rel_cluster();
                 for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.norm_full), j));
             }
             ok = __all_sync(0xffffffffu, tc_wait(sh.norm_full, 0, abort, true));
@@ -400,43 +440,67 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                 for (int j = 0; j < ks; ++j) total += dsmem_ld_f32(dsmem_addr(smem_addr(&sh.part[m]), j));
             }
             const float inv = 1.0f / sqrtf(total / (float)p.K + p.eps);
-            // pass 2: a = x * inv * W_norm, to bf16
+            // scale the staged x in place: element order in a chunk is
+            // (0,4,1,5,2,6,3,7), low half first
             for (int c = sub; c < n_chunks; c += TPL) {
                 const int k = k_base + 8 * c;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (ok && m < p.M && k < p.K) {
-                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
-                    float4 x0 = a4[0], x1 = a4[1];
+                uint4 *slot_p = reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7));
+                if (!(ok && m < p.M && k < p.K)) {
+                    *slot_p = make_uint4(0u, 0u, 0u, 0u);
+                    continue;
+                }
+                const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + k);
+                const float4 g0 = __ldg(w4), g1 = __ldg(w4 + 1);
+                const uint4 xv = *slot_p;
+                auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+                auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+                uint4 o;
+                o.x = bf16x2_pack(lo(xv.x) * inv * g0.x, hi(xv.x) * inv * g1.x);
+                o.y = bf16x2_pack(lo(xv.y) * inv * g0.y, hi(xv.y) * inv * g1.y);
+                o.z = bf16x2_pack(lo(xv.z) * inv * g0.z, hi(xv.z) * inv * g1.z);
+                o.w = bf16x2_pack(lo(xv.w) * inv * g0.w, hi(xv.w) * inv * g1.w);
+                *slot_p = o;
+                if (p.norm_out && writer(m, c)) {
+                    // exact f32 side output from x recomputed
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + row_off + k);
+                    float4 x0 = __ldg(a4), x1 = __ldg(a4 + 1);
                     if (p.A_b) {
-                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + k);
-                        const float4 b0 = b4[0], b1 = b4[1];
+                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + row_off + k);
+                        const float4 b0 = __ldg(b4), b1 = __ldg(b4 + 1);
                         x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
                         x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
                     }
-                    const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + k);
-                    const float4 g0 = w4[0], g1 = w4[1];
-                    x0.x = (x0.x * inv) * g0.x; x0.y = (x0.y * inv) * g0.y;
-                    x0.z = (x0.z * inv) * g0.z; x0.w = (x0.w * inv) * g0.w;
-                    x1.x = (x1.x * inv) * g1.x; x1.y = (x1.y * inv) * g1.y;
-                    x1.z = (x1.z * inv) * g1.z; x1.w = (x1.w * inv) * g1.w;
-                    if (writer && p.norm_out) {
-                        float4 *no = reinterpret_cast<float4 *>(p.norm_out + (size_t)m * p.K + k);
-                        no[0] = x0;
-                        no[1] = x1;
-                    }
-                    v = pack_chunk(x0, x1);
+                    float4 *no = reinterpret_cast<float4 *>(p.norm_out + row_off + k);
+                    no[0] = make_float4((x0.x * inv) * g0.x, (x0.y * inv) * g0.y, (x0.z * inv) * g0.z,
+                                        (x0.w * inv) * g0.w);
+                    no[1] = make_float4((x1.x * inv) * g1.x, (x1.y * inv) * g1.y, (x1.z * inv) * g1.z,
+                                        (x1.w * inv) * g1.w);
                 }
-                *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) = v;
             }
         } else {
-            for (int c = sub; c < n_chunks; c += TPL) {
-                const int k = k_base + 8 * c;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (m < p.M && k < p.K) {
-                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k);
-                    v = pack_chunk(a4[0], a4[1]);
+            // batches of kU chunks: all loads issued before the first conversion
+            constexpr int kU = 4;
+            const float4 *arow = reinterpret_cast<const float4 *>(p.A + (size_t)(m < p.M ? m : 0) * p.K);
+            for (int c0 = sub; c0 < n_chunks; c0 += kU * TPL) {
+                float4 x[kU][2];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + u * TPL;
+                    const int k = k_base + 8 * c;
+                    if (c < n_chunks && m < p.M && k < p.K) {
+                        x[u][0] = __ldg(arow + k / 4);
+                        x[u][1] = __ldg(arow + k / 4 + 1);
+                    } else {
+                        x[u][0] = x[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
                 }
-                *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) = v;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + u * TPL;
+                    if (c < n_chunks)
+                        *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) =
+                            pack_chunk(x[u][0], x[u][1]);
+                }
             }
         }
         fence_proxy_async_smem();
@@ -452,62 +516,137 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         const uint32_t magic = p.magic_bf16;
         int kbg = 0;  // K-blocks so far (tensor-memory slot sequence)
+        const int rho = r & (p.P - 1);
+        const int srow = r >> p.logP;
+        int slot = 0, phase = 0, tl = 0, sir = 0;
         for (int i = 0; ok && i < n_stages_total; ++i) {
-            const int slot = i % p.S;
             // warp-uniform outcome: the collective tensor-memory stores below
             // need every lane
-            if (!__all_sync(0xffffffffu, tc_wait(&sh.full[slot], (i / p.S) & 1, abort, false))) {
+            if (!__all_sync(0xffffffffu, tc_wait(&sh.full[slot], phase, abort, false))) {
                 ok = false;
                 break;
             }
-            const int tl = i / spr;
-            const int k0 = (st0 + (i - tl * spr)) * kStageK;
-            const int g0 = k0 / p.gs;
+            const int k0 = (st0 + sir) * kStageK;
+            const int c0 = k0 >> 5;  // first 32-code chunk of the stage
+            const int g0 = chunk_group(c0, p.gmagic);
             const unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+            // this row's scales and zeros in the stage: box of residue r % P,
+            // super-row r / P (or the tail area), columns from `off`
+            const int g_last = chunk_group((min(k0 + kStageK, p.K) - 1) >> 5, p.gmagic);
+            const int R = (cid + tl * p.n_clusters) * p.TR + r;
+            const bool row_valid = row_in_tile && R < p.N && k0 < p.K;
+            const int off = (rho * p.G + g0) & 3;
+            const float *s_src[NMAT], *z_src[NMAT];
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat) {
+                if (R >= p.P * p.Q) {
+                    const int t = R - p.P * p.Q;
+                    const float *tail = reinterpret_cast<const float *>(stage + p.off_tail);
+                    s_src[mat] = tail + ((mat * 2 + 0) * 4 + t) * p.BW + off;
+                    z_src[mat] = tail + ((mat * 2 + 1) * 4 + t) * p.BW + off;
+                } else {
+                    const float *box0 = reinterpret_cast<const float *>(
+                        stage + p.off_sz + ((mat * 2 + 0) * p.P + rho) * p.sz_box_stride);
+                    const float *box1 = reinterpret_cast<const float *>(
+                        stage + p.off_sz + ((mat * 2 + 1) * p.P + rho) * p.sz_box_stride);
+                    s_src[mat] = box0 + srow * p.BW + off;
+                    z_src[mat] = box1 + srow * p.BW + off;
+                }
+            }
+            // bf16 constants of the current group, per matrix: (128 + zi) twice,
+            // the scale twice, (zi - z) * scale twice; rows and groups past the
+            // matrix keep (128, 0, 0), which dequantizes any code to 0
+            int cur_gl = -1;
+            uint32_t c2[NMAT], s2[NMAT], d2[NMAT];
+#pragma unroll
+            for (int mat = 0; mat < NMAT; ++mat) {
+                c2[mat] = 0x43004300u;
+                s2[mat] = 0u;
+                d2[mat] = 0u;
+            }
+            // KPS K-blocks per step (the whole stage for one matrix, pairs for
+            // gate/up, whose tensor-memory ring is shorter): the step's codes
+            // are loaded first, its tensor-memory stores are in flight
+            // together, then one wait, then its slots go to the MMA
+            constexpr int KPS = NMAT == 1 ? 4 : 2;
 #pragma unroll 1
-            for (int j = 0; j < kStageK / kBlockK; ++j, ++kbg) {
-                const int ws = kbg % kNW;
-                if (kbg >= kNW &&
-                    !__all_sync(0xffffffffu, tc_wait(&sh.w_empty[ws], ((kbg / kNW) - 1) & 1, abort, false))) {
+            for (int jp = 0; jp < kStageK / kBlockK; jp += KPS, kbg += KPS) {
+                bool got = true;
+#pragma unroll
+                for (int e = 0; e < KPS; ++e) {
+                    const int kb = kbg + e;
+                    if (got && kb >= kNW) got = tc_wait(&sh.w_empty[kb % kNW], ((kb / kNW) - 1) & 1, abort, false);
+                }
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 if (warp_live) {
-                    const int gl = (k0 + j * kBlockK + 32 * h) / p.gs - g0;
+                    uint4 wv[KPS][NMAT];
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat) {
-                        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-                        uint4 cs = make_uint4(0x43004300u, 0u, 0u, 0u);
-                        if (row_in_tile) {
-                            const unsigned char *cb = stage + mat * p.codes_bytes;
-                            wv = *reinterpret_cast<const uint4 *>(cb + r * 128 + (((2 * j + h) ^ (r & 7)) << 4));
-                            cs = reinterpret_cast<const uint4 *>(stage + NMAT * p.codes_bytes + mat * p.cst_bytes)[gl * 128 + r];
-                        }
-                        uint32_t o[16];
-                        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                    for (int e = 0; e < KPS; ++e)
 #pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const uint32_t w = words[wi];
-                            const uint32_t t0 = bf16_code_pair(w, magic);
-                            const uint32_t t1 = bf16_code_pair(w >> 4, magic);
-                            const uint32_t t2 = bf16_code_pair(w >> 8, magic);
-                            const uint32_t t3 = bf16_code_pair(w >> 12, magic);
-                            o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(t0, cs.x), cs.y, cs.z);
-                            o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(t1, cs.x), cs.y, cs.z);
-                            o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(t2, cs.x), cs.y, cs.z);
-                            o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(t3, cs.x), cs.y, cs.z);
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            wv[e][mat] = make_uint4(0u, 0u, 0u, 0u);
+                            if (row_in_tile)
+                                wv[e][mat] = *reinterpret_cast<const uint4 *>(
+                                    stage + mat * p.codes_bytes + r * 128 + (((2 * (jp + e) + h) ^ (r & 7)) << 4));
                         }
-                        tmem_st16(tmem_base + lane_off + w_col(mat, ws) + 16 * h, o);
+#pragma unroll
+                    for (int e = 0; e < KPS; ++e) {
+                        const int ws = (kbg + e) % kNW;
+                        const int gl = chunk_group(c0 + 2 * (jp + e) + h, p.gmagic) - g0;
+                        if (row_valid && gl != cur_gl && g0 + gl <= g_last) {
+                            cur_gl = gl;
+#pragma unroll
+                            for (int mat = 0; mat < NMAT; ++mat) {
+                                const float sv = s_src[mat][gl], zv = z_src[mat][gl];
+                                const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
+                                const float dzs = (zi - zv) * sv;
+                                c2[mat] = bf16x2_pack(128.0f + zi, 128.0f + zi);
+                                s2[mat] = bf16x2_pack(sv, sv);
+                                d2[mat] = bf16x2_pack(dzs, dzs);
+                            }
+                        }
+#pragma unroll
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            uint32_t o[16];
+                            const uint32_t words[4] = {wv[e][mat].x, wv[e][mat].y, wv[e][mat].z, wv[e][mat].w};
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                const uint32_t w = words[wi];
+                                const uint32_t t0 = bf16_code_pair(w, magic);
+                                const uint32_t t1 = bf16_code_pair(w >> 4, magic);
+                                const uint32_t t2 = bf16_code_pair(w >> 8, magic);
+                                const uint32_t t3 = bf16_code_pair(w >> 12, magic);
+                                o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(t0, c2[mat]), s2[mat], d2[mat]);
+                                o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(t1, c2[mat]), s2[mat], d2[mat]);
+                                o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(t2, c2[mat]), s2[mat], d2[mat]);
+                                o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(t3, c2[mat]), s2[mat], d2[mat]);
+                            }
+                            tmem_st16(tmem_base + lane_off + w_col(mat, ws) + 16 * h, o);
+                        }
                     }
                     tmem_wait_st();
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.w_full[ws]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int e = 0; e < KPS; ++e) mbar_arrive(&sh.w_full[(kbg + e) % kNW]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[slot]);
+            if (++slot == p.S) {
+                slot = 0;
+                phase ^= 1;
+            }
+            if (++sir == spr) {
+                sir = 0;
+                ++tl;
+            }
         }
     }
 
@@ -572,10 +711,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         // A thread whose wait fails keeps walking the loop (skipping work) so
         // that the group's named barriers are always reached by all 128.
         bool ok = true;
+        if (ks > 1) cluster_wait();
+        cwaited = true;
         for (int tl = 0; tl < n_tl; ++tl) {
             const int b = tl & 1;
-            if (ok) ok = __all_sync(0xffffffffu, tc_wait(&sh.acc_full[b], (tl >> 1) & 1, abort, false));
-            float v[NMAT][MP];
+            // every outcome is made warp-uniform: the tensor-memory loads are
+            // collective
+            ok = __all_sync(0xffffffffu, ok && tc_wait(&sh.acc_full[b], (tl >> 1) & 1, abort, false));
+            // accumulator -> this CTA's partial tile in shared memory, 16
+            // columns at a time: red[mat][lane m][row r]
+            if (tl >= 1 && ks > 1)
+                ok = __all_sync(0xffffffffu, ok && tc_wait(sh.red_empty, (tl - 1) & 1, abort, true));
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -586,58 +732,71 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                         tmem_ld16(tmem_base + lane_off + acc_col(mat, b) + 16 * c, u);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) v[mat][16 * c + e] = __uint_as_float(u[e]);
+                        for (int e = 0; e < 16; ++e) red[(mat * MP + 16 * c + e) * 128 + r] = __uint_as_float(u[e]);
                     }
                 }
                 tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.acc_empty[b]);
             }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&sh.acc_empty[b]);
             const int row0 = (cid + tl * p.n_clusters) * p.TR;
             if (ks == 1) {
+                // the thread reads back only what it wrote (its row)
                 const int col = row0 + r;
                 if (ok && r < p.TR && col < p.N) {
-#pragma unroll
-                    for (int m = 0; m < MP; ++m) {
-                        if (m < p.M) store_out<EPI>(p, m, col, v[0][m], v[NMAT - 1][m]);
-                    }
+                    for (int m = 0; m < p.M; ++m)
+                        store_out<EPI>(p, m, col, red[m * 128 + r], red[((NMAT - 1) * MP + m) * 128 + r]);
                 }
                 continue;
             }
-            // split-K: partial tile to shared memory, then every rank sums its
-            // share of the rows over all ranks in rank order
-            if (ok && tl >= 1) ok = tc_wait(sh.red_empty, (tl - 1) & 1, abort, true);
-            if (ok) {
-#pragma unroll
-                for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-                    for (int m = 0; m < MP; ++m) red[(mat * MP + m) * 128 + r] = v[mat][m];
-            }
-            fence_acq_rel_cluster();
+            // split-K: every rank sums its share of the rows over all ranks,
+            // in rank order
             named_barrier(2, kEpWarps * 32);
             if (et == 0) {
+                // the group's partial-tile writes (ordered by the barrier) are
+                // released to the peers at cluster scope
+                fence_acq_rel_cluster();
                 for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.red_full), j));
             }
-            if (ok) ok = tc_wait(sh.red_full, tl & 1, abort, true);
+            ok = __all_sync(0xffffffffu, ok && tc_wait(sh.red_full, tl & 1, abort, true));
             if (ok) {
-                const int sh0 = p.TR * rank / ks;
-                const int sh1 = p.TR * (rank + 1) / ks;
-                const int rows = sh1 - sh0;
+                // this rank's share: whole groups of 4 rows; per group and lane,
+                // every rank's 16-byte partial is loaded before the rank-order sum
+                const int g4 = p.TR / 4;
+                const int q0 = 4 * (g4 * rank / ks);
+                const int q1 = 4 * (g4 * (rank + 1) / ks);
+                const int n4 = (q1 - q0) / 4;
                 const uint32_t red_s = smem_addr(red);
-                for (int idx = et; idx < rows * p.M; idx += kEpWarps * 32) {
-                    const int m = idx / rows;
-                    const int rr = sh0 + (idx - m * rows);
-                    const int col = row0 + rr;
-                    if (col >= p.N) continue;
-                    float sum[NMAT];
+                for (int idx = et; idx < n4 * p.M; idx += kEpWarps * 32) {
+                    const int m = idx / n4;
+                    const int rr = q0 + 4 * (idx - m * n4);
+                    float4 sum[NMAT];
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
                         const uint32_t off = (uint32_t)(((mat * MP + m) * 128 + rr) * 4);
-                        float acc = 0.0f;
-                        for (int j = 0; j < ks; ++j) acc += dsmem_ld_f32(dsmem_addr(red_s + off, j));
-                        sum[mat] = acc;
+                        float4 part[kMaxKs];
+#pragma unroll
+                        for (int j = 0; j < kMaxKs; ++j)
+                            if (j < ks) part[j] = dsmem_ld_f32x4(dsmem_addr(red_s + off, j));
+                        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                        for (int j = 0; j < kMaxKs; ++j) {
+                            if (j < ks) {
+                                a.x += part[j].x;
+                                a.y += part[j].y;
+                                a.z += part[j].z;
+                                a.w += part[j].w;
+                            }
+                        }
+                        sum[mat] = a;
                     }
-                    store_out<EPI>(p, m, col, sum[0], sum[NMAT - 1]);
+                    const float g[4] = {sum[0].x, sum[0].y, sum[0].z, sum[0].w};
+                    const float u4[4] = {sum[NMAT - 1].x, sum[NMAT - 1].y, sum[NMAT - 1].z, sum[NMAT - 1].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = row0 + rr + e;
+                        if (rr + e < p.TR && col < p.N) store_out<EPI>(p, m, col, g[e], u4[e]);
+                    }
                 }
             }
             named_barrier(2, kEpWarps * 32);
@@ -656,7 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-    if (ks > 1) cluster_sync_all();  // no peer reads this CTA's shared memory any more
+    if (ks > 1) {
+        if (!cwaited) cluster_wait();
+        cluster_sync_all();  // no peer reads this CTA's shared memory any more
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -692,6 +854,39 @@ struct TcPlan {
     int ks, TR, n_tiles, n_clusters, S, gps;
     uint32_t smem;
 };
+
+// Shared-memory layout of one ring stage: packed codes of every matrix
+// (TR rows x 128 bytes each), then per matrix and array (scale, zero) and row
+// residue one box of TR/P super-rows x BW floats, then the tail rows.
+struct StageGeom {
+    int P, BW;
+    uint32_t codes_bytes, sz_box_bytes, sz_box_stride, off_sz, off_tail, stage_bytes;
+};
+
+int gcd_int(int a, int b)
+{
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+StageGeom stage_geom(int TR, int nmat, int G, int gps)
+{
+    StageGeom g;
+    g.P = 4 / gcd_int(G, 4);                    // P rows of G floats: a 16-byte multiple
+    g.BW = (3 + gps + 3) / 4 * 4;                // a stage's groups from a 16-byte aligned start
+    g.codes_bytes = (uint32_t)TR * 128u;
+    g.sz_box_bytes = (uint32_t)(TR / g.P) * (uint32_t)g.BW * 4u;
+    g.sz_box_stride = (g.sz_box_bytes + 127u) / 128u * 128u;
+    g.off_sz = (uint32_t)nmat * g.codes_bytes;
+    g.off_tail = g.off_sz + (uint32_t)nmat * 2u * (uint32_t)g.P * g.sz_box_stride;
+    const uint32_t tail = (uint32_t)nmat * 2u * 4u * (uint32_t)g.BW * 4u;
+    g.stage_bytes = (g.off_tail + tail + 1023u) / 1024u * 1024u;
+    return g;
+}
 
 // Most scale groups one 256-code stage (starting at a multiple of 256) spans,
 // counted without clipping at K, so every K-block of a stage -- including
@@ -756,11 +951,9 @@ bool plan_tc(const Call &call, int MP, int dev, const void *kern, int smem_optin
         if (clusters_max <= 0) continue;
         const int spr_max = (n_st + ks - 1) / ks;
         const uint32_t act = (uint32_t)spr_max * (kStageK / kBlockK) * MP * 128u;
-        const uint32_t red = ks > 1 ? (uint32_t)nmat * MP * 128u * 4u : 0u;
+        const uint32_t red = (uint32_t)nmat * MP * 128u * 4u;
         for (int TR = 128; TR >= 16; TR -= 8) {
-            const uint32_t codes = (uint32_t)TR * 128u;
-            const uint32_t cst = (uint32_t)gps * 128u * 16u;
-            const uint32_t stage = round_up((uint32_t)nmat * (codes + cst), 1024u);
+            const uint32_t stage = stage_geom(TR, nmat, call.K / call.gs, gps).stage_bytes;
             const uint32_t fixed = 1024u + act + round_up(red, 1024u) + 1024u;
             if (fixed + 2u * stage > (uint32_t)smem_optin) continue;
             int S = (int)(((uint32_t)smem_optin - fixed) / stage);
@@ -770,8 +963,10 @@ bool plan_tc(const Call &call, int MP, int dev, const void *kern, int smem_optin
             const int waves = (n_tiles + clusters - 1) / clusters;
             // critical-path work of one CTA, in codes: its tiles' share of K,
             // the per-tile pipeline fill and epilogue, and the activation staging
-            const double per_tile = (double)TR * spr_max * kStageK * nmat + 24576.0 * nmat;
-            const double staging = (double)spr_max * kStageK * MP * (call.norm ? 3.0 : 1.5);
+            // (staging: the lanes' f32 activations of the K range, read at
+            // roughly 100 GB/s per SM, against ~75 G codes/s of dequant)
+            const double per_tile = (double)TR * spr_max * kStageK * nmat + 49152.0 * nmat;
+            const double staging = 0.77 * (double)spr_max * kStageK * call.M * 4.0 * (call.norm ? 2.0 : 1.0);
             const double cost = waves * per_tile + staging;
             if (!found || cost < best_cost * 0.999) {
                 found = true;
@@ -824,6 +1019,24 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    {
+        // scales / zeros as [Q][P*G] super-rows (row stride a 16-byte multiple)
+        const int P = 4 / gcd_int(call.K / call.gs, 4);
+        const int G = call.K / call.gs;
+        const int BW = (3 + pl.gps + 3) / 4 * 4;
+        const cuuint64_t dims[2] = {(cuuint64_t)P * G, (cuuint64_t)(call.N / P)};
+        const cuuint64_t strides[1] = {(cuuint64_t)P * G * 4u};
+        const cuuint32_t box[2] = {(cuuint32_t)BW, (cuuint32_t)(pl.TR / P)};
+        const cuuint32_t estr[2] = {1u, 1u};
+        for (int mat = 0; mat < NMAT; ++mat)
+            for (int arr = 0; arr < 2; ++arr) {
+                const float *base = arr == 0 ? call.scales[mat] : call.zeros[mat];
+                if (encode(&prm.sz[mat][arr], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                    return cudaErrorInvalidValue;
+            }
+    }
     prm.M = call.M;
     prm.K = call.K;
     prm.N = call.N;
@@ -837,12 +1050,24 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
     prm.S = pl.S;
     prm.gps = pl.gps;
     const int spr_max = (prm.n_st + pl.ks - 1) / pl.ks;
-    prm.codes_bytes = (uint32_t)pl.TR * 128u;
-    prm.cst_bytes = (uint32_t)pl.gps * 128u * 16u;
-    prm.stage_bytes = round_up((uint32_t)NMAT * (prm.codes_bytes + prm.cst_bytes), 1024u);
+    const StageGeom sg = stage_geom(pl.TR, NMAT, prm.G, pl.gps);
+    prm.P = sg.P;
+    prm.logP = sg.P == 1 ? 0 : sg.P == 2 ? 1 : 2;
+    prm.Q = call.N / sg.P;
+    {
+        const unsigned long long d = (unsigned long long)(call.gs / 32);
+        prm.gmagic = ((1ull << 40) + d - 1) / d;
+    }
+    prm.BW = sg.BW;
+    prm.codes_bytes = sg.codes_bytes;
+    prm.sz_box_bytes = sg.sz_box_bytes;
+    prm.sz_box_stride = sg.sz_box_stride;
+    prm.off_sz = sg.off_sz;
+    prm.off_tail = sg.off_tail;
+    prm.stage_bytes = sg.stage_bytes;
     prm.off_act = 0;
     const uint32_t act = (uint32_t)spr_max * (kStageK / kBlockK) * MP * 128u;
-    const uint32_t red = pl.ks > 1 ? (uint32_t)NMAT * MP * 128u * 4u : 0u;
+    const uint32_t red = (uint32_t)NMAT * MP * 128u * 4u;
     prm.off_ring = round_up(act, 1024u);
     prm.off_red = prm.off_ring + (uint32_t)pl.S * prm.stage_bytes;
     prm.off_misc = prm.off_red + round_up(red, 1024u);
@@ -907,6 +1132,14 @@ cudaError_t dispatch_tc(const Call &call, cudaStream_t stream)
 bool tc_path_supported(const Call &call)
 {
     if (call.M < 16 || call.M > 32) return false;
+    // scales and zeros are read by tensor-map copies of whole super-rows of
+    // P = 4 / gcd(G, 4) rows (16-byte aligned bases, at least one super-row)
+    const int P = 4 / gcd_int(call.K / call.gs, 4);
+    if (call.N < P) return false;
+    for (int m = 0; m < call.nmat; ++m) {
+        if ((reinterpret_cast<uintptr_t>(call.scales[m]) & 15u) != 0) return false;
+        if ((reinterpret_cast<uintptr_t>(call.zeros[m]) & 15u) != 0) return false;
+    }
     if (groups_per_stage(call.gs) > kMaxGps) return false;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;

@@ -144,6 +144,29 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
                  : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared; when `valid` is false nothing is
+// read and the destination is filled with zeros.
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected arrival count includes this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bring a tensor map (kernel-parameter, constant or global space, generic
+// address) into the descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // 2-D tiled bulk copy global -> shared through a tensor map; x is the inner
 // (contiguous) coordinate.  Out-of-range elements are filled with zeros.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar)
@@ -182,6 +205,17 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr)
     return v;
 }
 
+// 16-byte load from distributed shared memory (address 16-byte aligned).
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier of any CTA of the cluster (address from dsmem_addr),
 // releasing this thread's prior shared-memory writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar)
@@ -195,12 +229,23 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return done != 0;
+}
+
+// Split cluster barrier: every thread of every CTA arrives, then waits.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // All threads of all CTAs of the cluster.

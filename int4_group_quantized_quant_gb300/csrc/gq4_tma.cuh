@@ -12,6 +12,9 @@
 namespace gq4 {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Longest a single try_wait may suspend the thread (the hardware wakes it
+// as soon as the phase completes); waiting threads then use no issue slots.
+constexpr uint32_t kSuspendHintNs = 50000u;  // 50 us
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -53,10 +56,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return done != 0;
 }

@@ -6,8 +6,9 @@ with f32 accumulation, so outputs are compared against the oracle under
 f32 and keep their f32 bounds).  Cases cover the 7B-shaped stack's four calls
 at 16 and 32 lanes, ragged K (a final partial 256-code stage), ragged N
 (partial tiles), group sizes 32..1024 including one that does not divide the
-stage, lane counts that are not a multiple of 16, the norm prologue with and
-without its second addend, determinism, lane-order independence and NaN
+stage, scale rows that are not 16-byte multiples (read as super-rows of 2 or 4
+rows, with tail rows), lane counts that are not a multiple of 16, the norm
+prologue with and without its second addend, determinism, lane-order independence and NaN
 propagation.  The error word must stay clear.
 """
 
@@ -43,7 +44,10 @@ MATVEC_CASES = [
     (32, 4096, 4096, 128),
     (32, 11008, 4096, 128),   # the stack's down projection (86 groups per column)
     (16, 11008, 4096, 128),
-    (16, 32, 1, 32),          # one chunk, one column, K inside one partial stage
+    (16, 32, 1, 32),          # one chunk, one column (too few rows for the tensor-core path)
+    (16, 64, 4, 32),          # K inside one partial stage, scale rows in pairs
+    (16, 160, 9, 32),         # 5 groups per column: scale rows in fours, one tail row
+    (20, 11008, 3, 128),      # 86 groups per column: scale rows in pairs, one tail row
     (17, 96, 7, 96),          # group size that does not divide the 256-code stage
     (31, 288, 130, 32),       # partial last stage, partial tile
     (32, 12800, 19, 256),     # many stages, few columns
@@ -108,6 +112,7 @@ def test_tc_quad_splits(gq4, M, K, N, gs, n0, n1, n2):
     (32, 4096, 300, 128, False),
     (20, 11008, 64, 128, True),     # the ffn width as K
     (32, 96, 9, 32, True),          # one partial stage
+    (32, 480, 130, 96, True),       # 5 groups per column, two tail rows
 ])
 def test_tc_norm(gq4, M, K, N, gs, with_b):
     w = I.quant_weights(K, N, gs, 1103, M, K, N)
@@ -132,6 +137,7 @@ def test_tc_norm(gq4, M, K, N, gs, with_b):
     (16, 4096, 11008, 128, False),   # the gated workload at 16 lanes
     (16, 256, 20, 32, False),
     (27, 1024, 130, 64, True),
+    (32, 96, 5, 32, True),           # 3 groups per column, one tail row
 ])
 def test_tc_gated(gq4, M, K, N, gs, use_norm):
     wg = I.quant_weights(K, N, gs, 1105, M, K, N, scale_range=I.SCALE_RANGE_GATED)
