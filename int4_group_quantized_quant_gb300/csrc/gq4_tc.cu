@@ -65,7 +65,7 @@ constexpr int kPrWarp = 12;     // warp 12
 constexpr int kMmaWarp = 13;    // warp 13
 constexpr int kThreads = 14 * 32;
 constexpr int kEpBase = kDqWarps * 32;
-constexpr int kMaxNW = 8;       // tensor-memory slots of dequantized K-blocks (most)
+constexpr int kMaxNW = 12;      // tensor-memory slots of dequantized K-blocks (most)
 constexpr int kMaxKs = 8;       // CTAs per cluster (split-K ranks), most
 constexpr int kStageK = 256;    // codes per stage along K
 constexpr int kBlockK = 64;     // codes per K-block (one 128-byte bf16 row)
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
     const int n_tl = cid < p.n_tiles ? (p.n_tiles - cid + p.n_clusters - 1) / p.n_clusters : 0;
     const int n_stages_total = n_tl * spr;
     // tensor memory: kNW dequantized K-blocks per matrix, two accumulators per matrix
-    constexpr int kNW = NMAT == 1 ? 8 : 6;
+    constexpr int kNW = NMAT == 1 ? 12 : 6;
     constexpr uint32_t kTmemCols = 512u;
     static_assert(NMAT * kNW * 32 + NMAT * 2 * 32 <= (int)kTmemCols, "tensor-memory map");
 
@@ -657,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, MP);
             const uint32_t act_s = smem_addr(smem + p.off_act);
+            const uint64_t desc_base = smem_desc_sw128(act_s, 1024);
             bool ok = tc_wait(sh.act_ready, 0, abort, false);
             bool any = false;
             int kbg = 0;
@@ -674,15 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after_sync();
+                    // descriptors advance by whole 16-byte units: one add per MMA
+                    const uint64_t bdesc0 = desc_base + (uint64_t)((uint32_t)kb * (MP * 128) >> 4);
 #pragma unroll
                     for (int mat = 0; mat < NMAT; ++mat) {
+                        const uint32_t a0 = tmem_base + w_col(mat, ws);
+                        const uint32_t d = tmem_base + acc_col(mat, b);
 #pragma unroll
-                        for (int jj = 0; jj < kBlockK / 16; ++jj) {
-                            const uint64_t bdesc =
-                                smem_desc_sw128(act_s + (uint32_t)kb * (MP * 128) + jj * 32, 1024);
-                            tc_mma_ts(tmem_base + acc_col(mat, b), tmem_base + w_col(mat, ws) + 8 * jj,
-                                      bdesc, idesc, (kb | jj) != 0 ? 1u : 0u);
-                        }
+                        for (int jj = 0; jj < kBlockK / 16; ++jj)
+                            tc_mma_ts(d, a0 + 8 * jj, bdesc0 + (uint64_t)(2 * jj), idesc, (kb | jj) != 0 ? 1u : 0u);
                     }
                     any = true;
                     tc_commit(&sh.w_empty[ws]);
@@ -1072,7 +1073,7 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
     prm.off_red = prm.off_ring + (uint32_t)pl.S * prm.stage_bytes;
     prm.off_misc = prm.off_red + round_up(red, 1024u);
     prm.off_bar = prm.off_misc + 256u;
-    if (prm.off_bar + 64u * 8u + 1024u > pl.smem) return cudaErrorInvalidValue;
+    if (prm.off_bar + 80u * 8u + 1024u > pl.smem) return cudaErrorInvalidValue;
     prm.magic_bf16 = 0x43004300u;
     prm.A = call.A;
     if (call.norm) {
