@@ -255,44 +255,39 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // =====================================================================
     constexpr int kCT = kConsumerWarps * 32;
     const int K4 = p.K >> 2;
+    // Activation loads are read-only (__ldg) and issued in batches of kB per
+    // thread before any use, so their latency is paid once per batch rather
+    // than once per element (the side-output stores in between would
+    // otherwise keep the compiler from hoisting them).
+    constexpr int kB = 6;
+    const float4 *A4 = reinterpret_cast<const float4 *>(p.A);
     if constexpr (NORM) {
         // One global pass: x = A + A_b (to shared memory, unscaled), its
-        // square sum, and the gain (kept in registers for the second pass).
-        constexpr int kPer = 4;  // float4s per thread kept in registers (K <= 4 * 4 * kCT)
-        float4 gn[kPer];
+        // square sum; the gain is read in the second pass.
+        const float4 *B4 = reinterpret_cast<const float4 *>(p.A_b);
         float part = 0.0f;
         const bool write_res = blockIdx.x == 0 && p.residual_out;
+        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
+            float4 x[kB], b[kB];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int v = ctid + u * kCT;
-            if (v < K4) {
-                float4 x = reinterpret_cast<const float4 *>(p.A)[v];
-                if (p.A_b) {
-                    const float4 b = reinterpret_cast<const float4 *>(p.A_b)[v];
-                    x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
-                }
-                gn[u] = reinterpret_cast<const float4 *>(p.W_norm)[v];
-                if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x;
-                part = fmaf(x.x, x.x, part);
-                part = fmaf(x.y, x.y, part);
-                part = fmaf(x.z, x.z, part);
-                part = fmaf(x.w, x.w, part);
-                s_act[act_index<R>(v >> 3, v & 7)] = x;
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + u * kCT;
+                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                x[u] = v < K4 ? __ldg(A4 + v) : z4;
+                b[u] = (v < K4 && B4) ? __ldg(B4 + v) : z4;
             }
-        }
-        // K beyond the register-resident part (large K): gain reloaded below
-        for (int v = ctid + kPer * kCT; v < K4; v += kCT) {
-            float4 x = reinterpret_cast<const float4 *>(p.A)[v];
-            if (p.A_b) {
-                const float4 b = reinterpret_cast<const float4 *>(p.A_b)[v];
-                x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + u * kCT;
+                if (v >= K4) continue;
+                x[u].x += b[u].x; x[u].y += b[u].y; x[u].z += b[u].z; x[u].w += b[u].w;
+                if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x[u];
+                part = fmaf(x[u].x, x[u].x, part);
+                part = fmaf(x[u].y, x[u].y, part);
+                part = fmaf(x[u].z, x[u].z, part);
+                part = fmaf(x[u].w, x[u].w, part);
+                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
             }
-            if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x;
-            part = fmaf(x.x, x.x, part);
-            part = fmaf(x.y, x.y, part);
-            part = fmaf(x.z, x.z, part);
-            part = fmaf(x.w, x.w, part);
-            s_act[act_index<R>(v >> 3, v & 7)] = x;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -303,32 +298,48 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
         for (int w = 0; w < kConsumerWarps; ++w) sum += s_norm[w];
         const float inv = 1.0f / sqrtf(sum / (float)p.K + p.eps);
         const bool write_norm = blockIdx.x == 0 && p.norm_out;
-        for (int v = ctid, u = 0; v < K4; v += kCT, ++u) {
-            float4 x = s_act[act_index<R>(v >> 3, v & 7)];
-            float4 g;
-            if (u < kPer) {
-                g = u == 0 ? gn[0] : u == 1 ? gn[1] : u == 2 ? gn[2] : gn[3];
-            } else {
-                g = reinterpret_cast<const float4 *>(p.W_norm)[v];
+        const float4 *W4 = reinterpret_cast<const float4 *>(p.W_norm);
+        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
+            float4 g[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + u * kCT;
+                g[u] = v < K4 ? __ldg(W4 + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
-            x.x = (x.x * inv) * g.x; x.y = (x.y * inv) * g.y;
-            x.z = (x.z * inv) * g.z; x.w = (x.w * inv) * g.w;
-            if (write_norm) reinterpret_cast<float4 *>(p.norm_out)[v] = x;
-            // pre-scale by 16^-p (exact): both halves of a word sit at p = 0..3
-            x.x *= code_prescale(0);
-            x.y *= code_prescale(1);
-            x.z *= code_prescale(2);
-            x.w *= code_prescale(3);
-            s_act[act_index<R>(v >> 3, v & 7)] = x;
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + u * kCT;
+                if (v >= K4) continue;
+                float4 x = s_act[act_index<R>(v >> 3, v & 7)];
+                x.x = (x.x * inv) * g[u].x; x.y = (x.y * inv) * g[u].y;
+                x.z = (x.z * inv) * g[u].z; x.w = (x.w * inv) * g[u].w;
+                if (write_norm) reinterpret_cast<float4 *>(p.norm_out)[v] = x;
+                // pre-scale by 16^-p (exact): both halves of a word sit at p = 0..3
+                x.x *= code_prescale(0);
+                x.y *= code_prescale(1);
+                x.z *= code_prescale(2);
+                x.w *= code_prescale(3);
+                s_act[act_index<R>(v >> 3, v & 7)] = x;
+            }
         }
     } else {
-        for (int v = ctid; v < K4; v += kCT) {
-            float4 x = reinterpret_cast<const float4 *>(p.A)[v];
-            x.x *= code_prescale(0);
-            x.y *= code_prescale(1);
-            x.z *= code_prescale(2);
-            x.w *= code_prescale(3);
-            s_act[act_index<R>(v >> 3, v & 7)] = x;
+        for (int v0 = ctid; v0 < K4; v0 += 2 * kB * kCT) {
+            float4 x[2 * kB];
+#pragma unroll
+            for (int u = 0; u < 2 * kB; ++u) {
+                const int v = v0 + u * kCT;
+                x[u] = v < K4 ? __ldg(A4 + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < 2 * kB; ++u) {
+                const int v = v0 + u * kCT;
+                if (v >= K4) continue;
+                x[u].x *= code_prescale(0);
+                x[u].y *= code_prescale(1);
+                x[u].z *= code_prescale(2);
+                x[u].w *= code_prescale(3);
+                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
+            }
         }
     }
     named_barrier(1, kCT);
