@@ -92,6 +92,17 @@ def barrier(world):
         dist.barrier()
 
 
+def job_throughput(bytes_per_rank_step: float, ms_local: float, steps: int, world: int,
+                   device="cpu"):
+    """(ms per step of the slowest rank, whole-job GB/s).
+
+    Every rank runs its own replica of the stack over the same number of
+    steps, so the job moves world * bytes_per_rank_step bytes per step and
+    takes as long as its slowest rank."""
+    ms_step = max_over_ranks(ms_local, world, device) / steps
+    return ms_step, world * bytes_per_rank_step / (ms_step / 1e3) / 1e9
+
+
 def max_over_ranks(x: float, world: int, device="cpu") -> float:
     if world == 1:
         return x
@@ -310,8 +321,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier(world)
     ms = ev0.elapsed_time(ev1)
-    ms_max = max_over_ranks(ms, world, device="cuda")
-    ms_step = ms_max / args.steps
+    sbytes = step_bytes(M, layers)
+    ms_step, value = job_throughput(sbytes, ms, args.steps, world, device="cuda")
 
     # ---- roofline: average launch duration of the dominant kernel ----
     # the gated gate/up call with its norm prologue (about half the step's bytes),
@@ -350,8 +361,6 @@ def run_ours(args, rank, world, local_rank):
     t1 = time.perf_counter()
     e2e_s = max_over_ranks((t1 - t0) / e2e_steps, world, device="cuda")
 
-    sbytes = step_bytes(M, layers)
-    value = world * sbytes / (ms_step / 1e3) / 1e9
     peak, peak_src = hbm_peak()
     achieved = gated_bytes / gated_avg_s / 1e9
     line = {
