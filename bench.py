@@ -258,6 +258,23 @@ class Stack:
     def launches_per_step(self):
         return 4 * len(self.layers)
 
+    def sequence(self):
+        """The step as one call sequence (one lane): the calls of layer() in
+        order, for gq4_run_sequence."""
+        gq4, calls = self.gq4, []
+        h = self.h0
+        for li in range(len(self.layers)):
+            L, h_next = self.layers[li], self.hbuf[li % 2]
+            calls += [
+                gq4.seq_quad(h, *L["qkv"], GS, self.n0, self.n1, self.n2, [self.q, self.k, self.v, None]),
+                gq4.seq_matvec(self.q, *L["o"], GS, self.o),
+                gq4.seq_gated(h, *L["gate"], *L["up"], GS, self.f, W_norm=L["W_norm"], eps=EPS,
+                              A_b=self.o, residual_out=self.res),
+                gq4.seq_matvec(self.f, *L["down"], GS, h_next),
+            ]
+            h = h_next
+        return calls, h
+
     def layer(self, li, h, h_next, stream):
         gq4, L = self.gq4, self.layers[li]
         gq4.quad_matvec(h, *L["qkv"], GS, self.n0, self.n1, self.n2,

@@ -143,6 +143,58 @@ GQ4_API gq4_status gq4_gated_matvec(int M, int K, int N, int group_size,
                             const float *zeros_up,
                             float *out, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * One-lane call sequences (decode of a whole layer stack in one launch).
+ *
+ * The pages run a decode step as a list of dispatches over the same kernels
+ * (the gerbil executor's decode entries: per layer the quad QKV matvec, the
+ * output projection, the SiLU-gated gate/up with its norm prologue and the
+ * down projection).  gq4_run_sequence runs such a list of one-lane (M = 1)
+ * calls, in order, with the semantics of issuing them one by one: call i+1
+ * may read what calls 0..i wrote.  It is one persistent launch: while the
+ * lanes of call i finish, the weights of call i+1 are already streaming in.
+ * ------------------------------------------------------------------------ */
+typedef enum gq4_op {
+    GQ4_OP_MATVEC = 0,   /* gq4_matvec:       out[0] = C                        */
+    GQ4_OP_QUAD = 1,     /* gq4_quad_matvec:  out[0..3], split points n0..n2    */
+    GQ4_OP_NORM = 2,     /* gq4_norm_matvec:  out[0] = C, norm required          */
+    GQ4_OP_GATED = 3     /* gq4_gated_matvec: out[0], gate = [0], up = [1], norm optional */
+} gq4_op;
+
+typedef struct gq4_call {
+    int op;                    /* gq4_op */
+    int K, N, group_size;
+    int n0, n1, n2;            /* GQ4_OP_QUAD only */
+    const float *A;            /* [K] */
+    const uint32_t *Bq[2];     /* [1], scales[1], zeros[1]: GQ4_OP_GATED's up matrix */
+    const float *scales[2];
+    const float *zeros[2];
+    float *out[4];
+    int has_norm;              /* GQ4_OP_NORM: must be 1; GQ4_OP_GATED: optional */
+    gq4_norm norm;
+} gq4_call;
+
+/* Bytes of device workspace gq4_run_sequence needs (a grid barrier). */
+GQ4_API size_t gq4_sequence_workspace_bytes(void);
+
+/* Run n_calls one-lane calls in order on `stream`.  Each call is validated
+ * as its single entry point would validate it (M = 1); outputs of one call
+ * must not overlap that call's inputs, but later calls may read them.
+ * `workspace` is device memory of at least gq4_sequence_workspace_bytes(),
+ * 16-byte aligned, that no call touches, zero-filled by the caller before
+ * its first use; a completed launch leaves it ready for the next sequence on
+ * the same stream (its arrival counter back at zero).
+ * Sequences in flight at the same time (other streams) need distinct
+ * workspaces.  After a call fails with a device error (gq4_device_error bit
+ * 2) the workspace must be zero-filled again.  The launch is cooperative
+ * (one CTA per SM, all resident).  Long sequences run as several launches
+ * of up to 128 calls each.  A sequence the persistent kernel cannot take
+ * (scale or zero rows not 16-byte aligned, shapes whose ring entries do not
+ * fit, no room for one CTA per SM) runs as individual launches instead,
+ * with the same results. */
+GQ4_API gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace,
+                                    cudaStream_t stream);
+
 /* Integer unpack test kernel: q[n*K + k] = q(n,k) as u8 [N][K].
  * Uses the same in-register extraction as the matvec kernels.
  * Requires K % 32 == 0. */
@@ -159,9 +211,10 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
 /* The library's sticky device-side error bits on the current device.  Bit 0
  * is set when the one-lane kernel gave up waiting for one of its own bulk
  * copies, bit 1 when the tensor-core kernel gave up waiting for a copy, an
- * MMA or a peer CTA of its cluster (every wait inside the kernels is bounded
- * in time, so a broken copy cannot hang the GPU; the outputs of that call are
- * then invalid).  Copies the word to
+ * MMA or a peer CTA of its cluster, bit 2 when a call sequence gave up
+ * waiting for a copy or for the other CTAs at a call boundary (every wait
+ * inside the kernels is bounded in time, so a broken copy cannot hang the
+ * GPU; the outputs of that call are then invalid).  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);

@@ -9,6 +9,7 @@
 // size are whole multiples of the 32-code vec4u load.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "gq4.h"
 #include "gq4_internal.h"
@@ -156,12 +157,11 @@ gq4::Call base_call(int M, int K, int N, int gs, const float *A)
     return c;
 }
 
-}  // namespace
+// Validation and the internal call of each entry point (shared with the
+// call sequences).
 
-extern "C" {
-
-gq4_status gq4_matvec(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
-                      const float *scales, const float *zeros, float *C, cudaStream_t stream)
+gq4_status build_matvec(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
+                        const float *scales, const float *zeros, float *C, gq4::Call &call)
 {
     GQ4_TRY(check_shape(M, K, N, group_size));
     RangeSet rs;
@@ -171,19 +171,18 @@ gq4_status gq4_matvec(int M, int K, int N, int group_size, const float *A, const
     GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
     if (!rs.disjoint()) return GQ4_ERR_ALIAS;
 
-    gq4::Call call = base_call(M, K, N, group_size, A);
+    call = base_call(M, K, N, group_size, A);
     call.Bq[0] = Bq;
     call.scales[0] = scales;
     call.zeros[0] = zeros;
     call.epi = gq4::kEpiStore;
     call.out[0] = C;
-    return run(call, stream);
+    return GQ4_OK;
 }
 
-gq4_status gq4_quad_matvec(int M, int K, int N, int group_size, int n0, int n1, int n2,
-                           const float *A, const uint32_t *Bq, const float *scales,
-                           const float *zeros, float *out0, float *out1, float *out2,
-                           float *out3, cudaStream_t stream)
+gq4_status build_quad(int M, int K, int N, int group_size, int n0, int n1, int n2, const float *A,
+                      const uint32_t *Bq, const float *scales, const float *zeros, float *const outs[4],
+                      gq4::Call &call)
 {
     GQ4_TRY(check_shape(M, K, N, group_size));
     if (!(0 <= n0 && n0 <= n1 && n1 <= n2 && n2 <= N)) return GQ4_ERR_INVALID_ARG;
@@ -192,11 +191,10 @@ gq4_status gq4_quad_matvec(int M, int K, int N, int group_size, int n0, int n1, 
     GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
     const int start[4] = {0, n0, n1, n2};
     const int len[4] = {n0, n1 - n0, n2 - n1, N - n2};
-    float *const outs[4] = {out0, out1, out2, out3};
     for (int i = 0; i < 4; ++i) GQ4_TRY(check_output(outs[i], (size_t)M * (size_t)len[i], rs));
     if (!rs.disjoint()) return GQ4_ERR_ALIAS;
 
-    gq4::Call call = base_call(M, K, N, group_size, A);
+    call = base_call(M, K, N, group_size, A);
     call.Bq[0] = Bq;
     call.scales[0] = scales;
     call.zeros[0] = zeros;
@@ -206,12 +204,12 @@ gq4_status gq4_quad_matvec(int M, int K, int N, int group_size, int n0, int n1, 
         call.seg_start[i] = start[i];
         call.seg_len[i] = len[i];
     }
-    return run(call, stream);
+    return GQ4_OK;
 }
 
-gq4_status gq4_norm_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
-                           const float *A, const uint32_t *Bq, const float *scales,
-                           const float *zeros, float *C, cudaStream_t stream)
+gq4_status build_norm(int M, int K, int N, int group_size, const gq4_norm *norm, const float *A,
+                      const uint32_t *Bq, const float *scales, const float *zeros, float *C,
+                      gq4::Call &call)
 {
     GQ4_TRY(check_shape(M, K, N, group_size));
     if (!norm) return GQ4_ERR_INVALID_ARG;
@@ -223,21 +221,20 @@ gq4_status gq4_norm_matvec(int M, int K, int N, int group_size, const gq4_norm *
     GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
     if (!rs.disjoint()) return GQ4_ERR_ALIAS;
 
-    gq4::Call call = base_call(M, K, N, group_size, A);
+    call = base_call(M, K, N, group_size, A);
     call.norm = norm;
     call.Bq[0] = Bq;
     call.scales[0] = scales;
     call.zeros[0] = zeros;
     call.epi = gq4::kEpiStore;
     call.out[0] = C;
-    return run(call, stream);
+    return GQ4_OK;
 }
 
-gq4_status gq4_gated_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
-                            const float *A, const uint32_t *Bq_gate, const float *scales_gate,
-                            const float *zeros_gate, const uint32_t *Bq_up,
-                            const float *scales_up, const float *zeros_up, float *out,
-                            cudaStream_t stream)
+gq4_status build_gated(int M, int K, int N, int group_size, const gq4_norm *norm, const float *A,
+                       const uint32_t *Bq_gate, const float *scales_gate, const float *zeros_gate,
+                       const uint32_t *Bq_up, const float *scales_up, const float *zeros_up,
+                       float *out, gq4::Call &call)
 {
     GQ4_TRY(check_shape(M, K, N, group_size));
     RangeSet rs;
@@ -249,7 +246,7 @@ gq4_status gq4_gated_matvec(int M, int K, int N, int group_size, const gq4_norm 
     GQ4_TRY(check_output(out, (size_t)M * (size_t)N, rs));
     if (!rs.disjoint()) return GQ4_ERR_ALIAS;
 
-    gq4::Call call = base_call(M, K, N, group_size, A);
+    call = base_call(M, K, N, group_size, A);
     call.norm = norm;
     call.nmat = 2;
     call.Bq[0] = Bq_gate;
@@ -260,7 +257,119 @@ gq4_status gq4_gated_matvec(int M, int K, int N, int group_size, const gq4_norm 
     call.zeros[1] = zeros_up;
     call.epi = gq4::kEpiGated;
     call.out[0] = out;
+    return GQ4_OK;
+}
+
+// One call of a sequence (M = 1).
+gq4_status build_seq_call(const gq4_call &c, gq4::Call &call)
+{
+    switch (c.op) {
+    case GQ4_OP_MATVEC:
+        return build_matvec(1, c.K, c.N, c.group_size, c.A, c.Bq[0], c.scales[0], c.zeros[0], c.out[0],
+                            call);
+    case GQ4_OP_QUAD:
+        return build_quad(1, c.K, c.N, c.group_size, c.n0, c.n1, c.n2, c.A, c.Bq[0], c.scales[0],
+                          c.zeros[0], c.out, call);
+    case GQ4_OP_NORM:
+        if (!c.has_norm) return GQ4_ERR_INVALID_ARG;
+        return build_norm(1, c.K, c.N, c.group_size, &c.norm, c.A, c.Bq[0], c.scales[0], c.zeros[0],
+                          c.out[0], call);
+    case GQ4_OP_GATED:
+        return build_gated(1, c.K, c.N, c.group_size, c.has_norm ? &c.norm : nullptr, c.A, c.Bq[0],
+                           c.scales[0], c.zeros[0], c.Bq[1], c.scales[1], c.zeros[1], c.out[0], call);
+    default:
+        return GQ4_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+gq4_status gq4_matvec(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
+                      const float *scales, const float *zeros, float *C, cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_matvec(M, K, N, group_size, A, Bq, scales, zeros, C, call));
     return run(call, stream);
+}
+
+gq4_status gq4_quad_matvec(int M, int K, int N, int group_size, int n0, int n1, int n2,
+                           const float *A, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *out0, float *out1, float *out2,
+                           float *out3, cudaStream_t stream)
+{
+    float *const outs[4] = {out0, out1, out2, out3};
+    gq4::Call call;
+    GQ4_TRY(build_quad(M, K, N, group_size, n0, n1, n2, A, Bq, scales, zeros, outs, call));
+    return run(call, stream);
+}
+
+gq4_status gq4_norm_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
+                           const float *A, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *C, cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_norm(M, K, N, group_size, norm, A, Bq, scales, zeros, C, call));
+    return run(call, stream);
+}
+
+gq4_status gq4_gated_matvec(int M, int K, int N, int group_size, const gq4_norm *norm,
+                            const float *A, const uint32_t *Bq_gate, const float *scales_gate,
+                            const float *zeros_gate, const uint32_t *Bq_up,
+                            const float *scales_up, const float *zeros_up, float *out,
+                            cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_gated(M, K, N, group_size, norm, A, Bq_gate, scales_gate, zeros_gate, Bq_up,
+                        scales_up, zeros_up, out, call));
+    return run(call, stream);
+}
+
+size_t gq4_sequence_workspace_bytes(void)
+{
+    return gq4::kSeqWorkspaceBytes;
+}
+
+gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace, cudaStream_t stream)
+{
+    if (n_calls < 0 || (n_calls > 0 && !calls)) return GQ4_ERR_INVALID_ARG;
+    if (n_calls == 0) return GQ4_OK;
+    if (!workspace) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return GQ4_ERR_MISALIGNED;
+    std::vector<gq4::Call> built((size_t)n_calls);
+    bool persistent = true;
+    for (int i = 0; i < n_calls; ++i) {
+        GQ4_TRY(build_seq_call(calls[i], built[(size_t)i]));
+        const gq4::Call &c = built[(size_t)i];
+        // the workspace is the launch's own scratch: no call may touch it
+        RangeSet rs;
+        rs.input(c.A, (size_t)c.K * sizeof(float));
+        for (int m = 0; m < c.nmat; ++m) {
+            rs.input(c.Bq[m], (size_t)c.N * (size_t)c.K / 2);
+            rs.input(c.scales[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
+            rs.input(c.zeros[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
+        }
+        for (int j = 0; j < 4; ++j) rs.input(c.out[j], (size_t)c.seg_len[j] * sizeof(float));
+        if (c.norm) {
+            rs.input(c.norm->A_b, (size_t)c.K * sizeof(float));
+            rs.input(c.norm->W_norm, (size_t)c.K * sizeof(float));
+            rs.input(c.norm->residual_out, (size_t)c.K * sizeof(float));
+            rs.input(c.norm->norm_out, (size_t)c.K * sizeof(float));
+        }
+        rs.output(workspace, gq4::kSeqWorkspaceBytes);
+        if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+        // the persistent kernel copies scale/zero rows in bulk (16-byte bases)
+        for (int m = 0; m < c.nmat; ++m)
+            if (!aligned(c.scales[m], 16) || !aligned(c.zeros[m], 16)) persistent = false;
+    }
+    if (persistent && gq4::sequence_plannable(built.data(), n_calls)) {
+        return gq4::launch_sequence(built.data(), n_calls, workspace, stream) == cudaSuccess ? GQ4_OK
+                                                                                            : GQ4_ERR_CUDA;
+    }
+    // otherwise the calls run one by one (same semantics, stream order)
+    for (int i = 0; i < n_calls; ++i) GQ4_TRY(run(built[(size_t)i], stream));
+    return GQ4_OK;
 }
 
 gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream)
@@ -291,10 +400,11 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
 gq4_status gq4_device_error(unsigned int *bits, int clear)
 {
     if (!bits) return GQ4_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     if (gq4::read_device_error(&a, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_tc_device_error(&b, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    *bits = a | b;
+    if (gq4::read_seq_device_error(&c, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b | c;
     return GQ4_OK;
 }
 

@@ -42,6 +42,14 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream);
 bool tc_path_supported(const Call &call);
 cudaError_t launch_tc(const Call &call, cudaStream_t stream);
 
+// One persistent launch for a sequence of one-lane calls (gq4_run_sequence):
+// whether the calls fit its ring, and the launch (up to 128 calls per
+// launch).  The workspace holds the grid barrier's counter and generation.
+constexpr size_t kSeqWorkspaceBytes = 128;
+bool sequence_plannable(const Call *calls, int n);
+cudaError_t launch_sequence(const Call *calls, int n, void *workspace, cudaStream_t stream);
+cudaError_t read_seq_device_error(unsigned int *bits, bool clear);
+
 // The sticky device-side error words (read, optionally clear): the one-lane
 // streaming path's and the tensor-core path's.
 cudaError_t read_device_error(unsigned int *bits, bool clear);

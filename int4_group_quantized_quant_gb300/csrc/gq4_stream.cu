@@ -81,11 +81,6 @@ struct StreamParams {
     int seg_len[4];
 };
 
-__device__ __forceinline__ int chunk_group(int gc, unsigned long long magic)
-{
-    return (int)(((unsigned long long)gc * magic) >> 40);
-}
-
 __device__ __forceinline__ void named_barrier(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -94,41 +89,6 @@ __device__ __forceinline__ void named_barrier(int id, int threads)
 __device__ __forceinline__ void record_error(unsigned int bits)
 {
     atomicOr(&g_device_error, bits);
-}
-
-// Per (column, group) zero-point constants.  The integer part of the zero
-// is folded into the magic offset, exactly: with zi = round(clamp(z, 0, 15)),
-//   f - (2^23 + 16^p zi) = 16^p (q - zi)          (an exact small integer),
-// and the fractional part dz = zi - z multiplies the chunk's activation sum:
-//   sum_k a_k (q_k - z) = sum_k a_k (q_k - zi) + dz * sum_k a_k.
-// When the zero is an integer in 0..15 (as for codes equal to their zero),
-// dz is exactly 0 and so is the correction.
-struct ZeroFold {
-    f32x2 nc01, nc23;  // -(2^23 + 16^p zi) for p = 0, 1 and p = 2, 3
-    float dz;
-};
-
-__device__ __forceinline__ ZeroFold fold_zero(float z)
-{
-    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
-    const float rz = zc + kMagic;  // 2^23 + round(zc)
-    const uint32_t rb = __float_as_uint(rz);
-    const uint32_t zi = rb - kMagicBits;
-    const uint32_t nb = rb | 0x80000000u;  // bits of -(2^23 + zi)
-    ZeroFold f;
-    f.nc01 = pack2(__uint_as_float(nb), __uint_as_float(nb + zi * 15u));
-    f.nc23 = pack2(__uint_as_float(nb + zi * 255u), __uint_as_float(nb + zi * 4095u));
-    f.dz = (rz - kMagic) - z;
-    return f;
-}
-
-// Shared-memory slot of activation float4 j (0..7) of chunk t: chunk groups
-// of R chunks are XOR-swizzled so that 32 lanes reading 32 consecutive
-// groups hit distinct banks.
-template <int R>
-__device__ __forceinline__ int act_index(int t, int j)
-{
-    return t * 8 + (j ^ ((t / R) & 7));
 }
 
 // R: consecutive 32-code chunks per chunk group (R = 2 only when a scale

@@ -46,6 +46,16 @@ class Norm(ctypes.Structure):
 
 _NormP = ctypes.POINTER(Norm)
 
+OP_MATVEC, OP_QUAD, OP_NORM, OP_GATED = 0, 1, 2, 3
+
+
+class Call(ctypes.Structure):
+    """``gq4_call``: one one-lane call of a sequence (``gq4_run_sequence``)."""
+    _fields_ = [("op", _i), ("K", _i), ("N", _i), ("group_size", _i),
+                ("n0", _i), ("n1", _i), ("n2", _i),
+                ("A", _vp), ("Bq", _vp * 2), ("scales", _vp * 2), ("zeros", _vp * 2),
+                ("out", _vp * 4), ("has_norm", _i), ("norm", Norm)]
+
 _SIGS = {
     "gq4_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_quad_matvec": [_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -53,6 +63,7 @@ _SIGS = {
     "gq4_norm_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_gated_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                          _vp],
+    "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_unpack": [_i, _i, _vp, _vp, _vp],
     "gq4_dequant": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
 }
@@ -66,8 +77,11 @@ lib.gq4_version.restype = _i
 lib.gq4_version.argtypes = []
 lib.gq4_device_error.restype = _i
 lib.gq4_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _i]
+lib.gq4_sequence_workspace_bytes.restype = ctypes.c_size_t
+lib.gq4_sequence_workspace_bytes.argtypes = []
 
-EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version", "gq4_device_error"]
+EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version", "gq4_device_error",
+                          "gq4_sequence_workspace_bytes"]
 
 
 class GQ4Error(RuntimeError):
@@ -199,6 +213,101 @@ def gated_matvec(A, Bq_gate, scales_gate, zeros_gate, Bq_up, scales_up, zeros_up
                                 _ptr(Bq_up), _ptr(scales_up), _ptr(zeros_up), _ptr(out),
                                 _stream(stream)), "gq4_gated_matvec")
     return out
+
+
+# ---------------------------------------------------------------------------
+# Call sequences (one lane)
+# ---------------------------------------------------------------------------
+
+class SeqCall:
+    """One call of a sequence: the C descriptor plus the tensors it points to
+    (kept alive while the descriptor is in use)."""
+
+    def __init__(self, desc: Call, tensors):
+        self.desc = desc
+        self.tensors = tensors
+
+
+def _one_lane(A):
+    M, K = _lanes(A)
+    if M != 1:
+        raise ValueError("sequence calls take one lane (A of shape [1, K])")
+    return K
+
+
+def _seq_norm(desc, K, W_norm, eps, A_b, residual_out, norm_out):
+    desc.has_norm = 1
+    desc.norm = _norm_struct(1, K, W_norm, eps, A_b, residual_out, norm_out)
+
+
+def seq_matvec(A, Bq, scales, zeros, group_size, C):
+    """Sequence entry of gq4_matvec (C [1, N] must be given)."""
+    K = _one_lane(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    _need(C, "C", _F32, (1, N))
+    d = Call(op=OP_MATVEC, K=K, N=N, group_size=group_size, A=_ptr(A))
+    d.Bq[0], d.scales[0], d.zeros[0], d.out[0] = _ptr(Bq), _ptr(scales), _ptr(zeros), _ptr(C)
+    return SeqCall(d, (A, Bq, scales, zeros, C))
+
+
+def seq_quad(A, Bq, scales, zeros, group_size, n0, n1, n2, outs):
+    """Sequence entry of gq4_quad_matvec (outs: four [1, len] tensors or None for empty ones)."""
+    K = _one_lane(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    lens = [n0, n1 - n0, n2 - n1, N - n2]
+    d = Call(op=OP_QUAD, K=K, N=N, group_size=group_size, n0=n0, n1=n1, n2=n2, A=_ptr(A))
+    d.Bq[0], d.scales[0], d.zeros[0] = _ptr(Bq), _ptr(scales), _ptr(zeros)
+    for i, (o, n) in enumerate(zip(outs, lens)):
+        if o is not None:
+            _need(o, f"out{i}", _F32, (1, n))
+        d.out[i] = _ptr(o)
+    return SeqCall(d, (A, Bq, scales, zeros, *outs))
+
+
+def seq_norm(A, Bq, scales, zeros, group_size, W_norm, C, eps=1e-6, A_b=None,
+             residual_out=None, norm_out=None):
+    """Sequence entry of gq4_norm_matvec."""
+    K = _one_lane(A)
+    N = _weights(Bq, scales, zeros, K, group_size)
+    _need(C, "C", _F32, (1, N))
+    d = Call(op=OP_NORM, K=K, N=N, group_size=group_size, A=_ptr(A))
+    d.Bq[0], d.scales[0], d.zeros[0], d.out[0] = _ptr(Bq), _ptr(scales), _ptr(zeros), _ptr(C)
+    _seq_norm(d, K, W_norm, eps, A_b, residual_out, norm_out)
+    return SeqCall(d, (A, Bq, scales, zeros, C, W_norm, A_b, residual_out, norm_out))
+
+
+def seq_gated(A, Bq_gate, scales_gate, zeros_gate, Bq_up, scales_up, zeros_up, group_size, out,
+              W_norm=None, eps=1e-6, A_b=None, residual_out=None, norm_out=None):
+    """Sequence entry of gq4_gated_matvec."""
+    K = _one_lane(A)
+    N = _weights(Bq_gate, scales_gate, zeros_gate, K, group_size, "_gate")
+    if _weights(Bq_up, scales_up, zeros_up, K, group_size, "_up") != N:
+        raise ValueError("gate and up must have the same N")
+    _need(out, "out", _F32, (1, N))
+    d = Call(op=OP_GATED, K=K, N=N, group_size=group_size, A=_ptr(A))
+    d.Bq[0], d.scales[0], d.zeros[0] = _ptr(Bq_gate), _ptr(scales_gate), _ptr(zeros_gate)
+    d.Bq[1], d.scales[1], d.zeros[1] = _ptr(Bq_up), _ptr(scales_up), _ptr(zeros_up)
+    d.out[0] = _ptr(out)
+    if W_norm is not None:
+        _seq_norm(d, K, W_norm, eps, A_b, residual_out, norm_out)
+    elif A_b is not None or residual_out is not None or norm_out is not None:
+        raise ValueError("A_b / residual_out / norm_out need W_norm")
+    return SeqCall(d, (A, Bq_gate, scales_gate, zeros_gate, Bq_up, scales_up, zeros_up, out,
+                       W_norm, A_b, residual_out, norm_out))
+
+
+def sequence_workspace(device=None):
+    """A zero-filled workspace for run_sequence (reusable on one stream)."""
+    n = int(lib.gq4_sequence_workspace_bytes())
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def run_sequence(calls, workspace, stream=None):
+    """Run the calls in order as one persistent launch (gq4_run_sequence)."""
+    _need(workspace, "workspace", (torch.uint8,), (int(lib.gq4_sequence_workspace_bytes()),))
+    arr = (Call * max(len(calls), 1))(*[c.desc for c in calls])
+    _check(lib.gq4_run_sequence(arr, len(calls), _ptr(workspace), _stream(stream)),
+           "gq4_run_sequence")
 
 
 def unpack(Bq, K, q=None, stream=None):

@@ -186,3 +186,77 @@ def test_binding_refuses_cpu_tensors(gq4):
     s = torch.zeros(4, 2)
     with pytest.raises(ValueError, match="CUDA"):
         gq4.matvec(A, Bq, s, s, 32)
+
+
+# ---------------------------------------------------------------------------
+# Call sequences: struct layout and validation on the host
+# ---------------------------------------------------------------------------
+
+def test_call_struct_layout_matches_header(gq4, tmp_path):
+    """The binding's gq4_call / gq4_norm mirror the C layout field by field."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "layout.c"
+    src.write_text(r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "gq4.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(gq4_call), offsetof(gq4_call, A),
+         offsetof(gq4_call, Bq), offsetof(gq4_call, scales), offsetof(gq4_call, zeros),
+         offsetof(gq4_call, out), offsetof(gq4_call, has_norm), offsetof(gq4_call, norm),
+         sizeof(gq4_norm), offsetof(gq4_norm, residual_out));
+  return 0;
+}
+""")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    C, N = gq4.Call, gq4.Norm
+    want = [ctypes.sizeof(C), C.A.offset, C.Bq.offset, C.scales.offset, C.zeros.offset,
+            C.out.offset, C.has_norm.offset, C.norm.offset, ctypes.sizeof(N), N.residual_out.offset]
+    assert got == want
+
+
+def _seq_call(gq4, op, K=256, N=64, gs=32, base=0x7f0000000000):
+    d = gq4.Call(op=op, K=K, N=N, group_size=gs, A=base)
+    d.Bq[0], d.scales[0], d.zeros[0] = base + 0x100000, base + 0x200000, base + 0x300000
+    d.Bq[1], d.scales[1], d.zeros[1] = base + 0x400000, base + 0x500000, base + 0x600000
+    d.out[0] = base + 0x700000
+    return d
+
+
+def _run_seq(gq4, descs, ws=0x7e0000000000):
+    arr = (gq4.Call * max(len(descs), 1))(*descs)
+    return gq4.lib.gq4_run_sequence(arr, len(descs), ws, None)
+
+
+@no_gpu_only
+def test_sequence_validation(gq4):
+    # no calls: nothing to do
+    assert gq4.lib.gq4_run_sequence(None, 0, None, None) == gq4.OK
+    assert gq4.lib.gq4_run_sequence(None, 1, 0x7e0000000000, None) == gq4.ERR_INVALID_ARG
+    good = _seq_call(gq4, gq4.OP_MATVEC)
+    assert _run_seq(gq4, [good], ws=0) == gq4.ERR_INVALID_ARG              # no workspace
+    assert _run_seq(gq4, [good], ws=0x7e0000000004) == gq4.ERR_MISALIGNED  # workspace alignment
+    bad_op = _seq_call(gq4, 7)
+    assert _run_seq(gq4, [good, bad_op]) == gq4.ERR_INVALID_ARG
+    bad_shape = _seq_call(gq4, gq4.OP_MATVEC, K=100)
+    assert _run_seq(gq4, [bad_shape]) == gq4.ERR_INVALID_ARG
+    no_norm = _seq_call(gq4, gq4.OP_NORM)                                  # norm op needs has_norm
+    assert _run_seq(gq4, [no_norm]) == gq4.ERR_INVALID_ARG
+    quad = _seq_call(gq4, gq4.OP_QUAD)
+    quad.n0, quad.n1, quad.n2 = 40, 30, 64                                 # non-monotone split
+    assert _run_seq(gq4, [quad]) == gq4.ERR_INVALID_ARG
+    # the workspace may not overlap any call's buffers
+    assert _run_seq(gq4, [good], ws=good.out[0]) == gq4.ERR_ALIAS
+    # within a call, outputs may not overlap inputs
+    alias = _seq_call(gq4, gq4.OP_MATVEC)
+    alias.out[0] = alias.A
+    assert _run_seq(gq4, [alias]) == gq4.ERR_ALIAS
