@@ -189,4 +189,104 @@ __device__ __forceinline__ int act_index(int t, int j)
     return t * 8 + (j ^ ((t / R) & 7));
 }
 
+// ---------------------------------------------------------------------------
+// One-lane path: fp16 code pairs.  A LOP3 places two codes of a word as the
+// low mantissa bits of the two halves of an fp16 pair whose exponent is that
+// of 1024 (bits 0x6400 per half):
+//
+//     halves = 0x64006400 | (x & (0x000F000F << 4p))  =>  1024 + 16^p q, p in {0, 1}
+//
+// (exact: 16^p q <= 240 stays inside the 10-bit mantissa).  With t = w >> 8
+// the four masks give the pairs (0,4) (1,5) (2,6) (3,7) of a word, codes
+// 0, 2, 4, 6 at p = 0 and 1, 3, 5, 7 at p = 1: five ALU operations per word
+// instead of nine.  One mixed-precision add (PTX `add.rn.f32.f16`, sm_100
+// and later) then widens a half to f32 and adds -(1024 + 16^p zi) in one
+// rounding, which is exact: the result 16^p (q - zi) is a small integer.
+// The activation that multiplies the code is pre-scaled by 16^-p, so the
+// packed FMA forms a * (q - zi) exactly before its single rounding, the same
+// arithmetic as the f32 magic form above with half the logic operations.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kHalfMagicBits = 0x64006400u;
+
+// Per (column, group) zero-point constants of the fp16 form: the integer
+// part zi = round(clamp(z, 0, 15)) goes into the widening adds, the
+// fractional part dz = zi - z multiplies the chunk group's activation sum
+// (sum_k a_k (q_k - z) = sum_k a_k (q_k - zi) + dz * sum_k a_k).  An integer
+// zero point in 0..15 gives dz = 0 exactly.
+struct HalfZero {
+    float nz0;  // -(1024 + zi)       (codes at p = 0)
+    float nz1;  // -(1024 + 16 zi)    (codes at p = 1)
+    float dz;
+};
+
+__device__ __forceinline__ HalfZero half_zero(float z)
+{
+    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
+    const float zi = __fsub_rn(__fadd_rn(zc, kMagic), kMagic);  // round to nearest integer
+    HalfZero h;
+    h.nz0 = -1024.0f - zi;
+    h.nz1 = fmaf(-16.0f, zi, -1024.0f);
+    h.dz = zi - z;
+    return h;
+}
+
+// f32(low / high half of x, as fp16) + c, one rounding.
+__device__ __forceinline__ float widen_add_lo(uint32_t x, float c)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, l, %2;\n\t}"
+        : "=f"(r) : "r"(x), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float widen_add_hi(uint32_t x, float c)
+{
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, h, %2;\n\t}"
+        : "=f"(r) : "r"(x), "f"(c));
+    return r;
+}
+
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t masked_magic_bits(uint32_t x, uint32_t magic)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(MASK), "r"(magic));
+    return d;
+}
+
+// acc += the eight products of one word with its activations.  `lo` holds
+// the activations of codes (0, 4, 1, 5) and `hi` those of (2, 6, 3, 7), the
+// ones of codes 1, 3, 5, 7 pre-scaled by 1/16 (see pair_activations).
+// `magic` is kHalfMagicBits, passed in from a kernel parameter.
+__device__ __forceinline__ f32x2 word_dot(uint32_t w, ulonglong2 lo, ulonglong2 hi, const HalfZero &z,
+                                          uint32_t magic, f32x2 acc)
+{
+    const uint32_t t = w >> 8;
+    const uint32_t h04 = masked_magic_bits<0x000F000Fu>(w, magic);
+    const uint32_t h15 = masked_magic_bits<0x00F000F0u>(w, magic);
+    const uint32_t h26 = masked_magic_bits<0x000F000Fu>(t, magic);
+    const uint32_t h37 = masked_magic_bits<0x00F000F0u>(t, magic);
+    acc = fma2(lo.x, pack2(widen_add_lo(h04, z.nz0), widen_add_hi(h04, z.nz0)), acc);
+    acc = fma2(lo.y, pack2(widen_add_lo(h15, z.nz1), widen_add_hi(h15, z.nz1)), acc);
+    acc = fma2(hi.x, pack2(widen_add_lo(h26, z.nz0), widen_add_hi(h26, z.nz0)), acc);
+    acc = fma2(hi.y, pack2(widen_add_lo(h37, z.nz1), widen_add_hi(h37, z.nz1)), acc);
+    return acc;
+}
+
+// The eight activations a0..a7 of one word (x0 = a0..a3, x1 = a4..a7) in
+// the order word_dot reads them, pre-scaled: (a0, a4, a1/16, a5/16) and
+// (a2, a6, a3/16, a7/16).
+__device__ __forceinline__ void pair_activations(float4 x0, float4 x1, float4 &lo, float4 &hi)
+{
+    lo = make_float4(x0.x, x1.x, x0.y * 0.0625f, x1.y * 0.0625f);
+    hi = make_float4(x0.z, x1.z, x0.w * 0.0625f, x1.w * 0.0625f);
+}
+
+// Sum of the unscaled activations held by one paired float4.
+__device__ __forceinline__ float paired_sum(float4 v)
+{
+    return (v.x + v.y) + 16.0f * (v.z + v.w);
+}
+
 }  // namespace gq4

@@ -21,12 +21,12 @@
 //     atomic counter in a caller-provided workspace; waits bounded in time)
 //     before staging call i+1's activations, which may be call i's outputs.  Activations are read through L2 (ld.global.cg),
 //     never from a possibly stale L1 line.
-//   * Within a call the arithmetic is the one-lane streaming kernel's: the
-//     activations staged once per CTA, pre-scaled by 16^-p and swizzled; warp
-//     slots of four columns (or two gate and two up columns); in-register
-//     magic-number unpack with the zero's integer part folded into the magic
-//     and its fractional part applied through chunk-group activation sums;
-//     one xor reduce-scatter per slot.
+//   * Within a call the arithmetic is the one-lane streaming kernel's
+//     (gq4_onelane.cuh): the activations staged once per CTA, paired,
+//     pre-scaled and swizzled; warp slots of four columns (or two gate and
+//     two up columns); fp16-pair unpack with the zero's integer part taken
+//     out in one exact widening add and its fractional part applied through
+//     chunk-group activation sums; one xor reduce-scatter per slot.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -36,6 +36,7 @@
 
 #include "gq4_device.cuh"
 #include "gq4_internal.h"
+#include "gq4_onelane.cuh"
 #include "gq4_tma.cuh"
 
 namespace gq4 {
@@ -96,7 +97,7 @@ struct SeqParams {
     int S;                    // ring depth
     uint32_t stage_bytes;
     uint32_t off_act, off_asum, off_norm, off_bar;
-    uint32_t magic_bits;      // kMagicBits, read from the parameter bank
+    uint32_t magic_bits;      // kHalfMagicBits, read from the parameter bank
     unsigned int *bar_count;  // grid barrier: arrivals so far in this launch
     unsigned int *bar_exit;   // CTAs that have finished this launch
     SeqCall calls[kMaxCalls];
@@ -204,107 +205,9 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
     const int n_slots = (ncols + CPS - 1) / CPS;
 
     // ---- prologue: activations (through L2: earlier calls may have written
-    // them), batched loads ----
-    const int K4 = c.K >> 2;
-    constexpr int kB = 6;
-    const float4 *A4 = reinterpret_cast<const float4 *>(c.A);
-    const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if constexpr (NORM) {
-        const float4 *B4 = reinterpret_cast<const float4 *>(c.A_b);
-        float part = 0.0f;
-        const bool write_res = blockIdx.x == 0 && c.residual_out;
-        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
-            float4 x[kB], b[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                x[u] = v < K4 ? __ldcg(A4 + v) : z4;
-                b[u] = (v < K4 && B4) ? __ldcg(B4 + v) : z4;
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                x[u].x += b[u].x; x[u].y += b[u].y; x[u].z += b[u].z; x[u].w += b[u].w;
-                if (write_res) reinterpret_cast<float4 *>(c.residual_out)[v] = x[u];
-                part = fmaf(x[u].x, x[u].x, part);
-                part = fmaf(x[u].y, x[u].y, part);
-                part = fmaf(x[u].z, x[u].z, part);
-                part = fmaf(x[u].w, x[u].w, part);
-                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) s_norm[warp] = part;
-        named_barrier_sync(1, kCT);
-        float sum = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) sum += s_norm[w];
-        const float inv = 1.0f / sqrtf(sum / (float)c.K + c.eps);
-        const bool write_norm = blockIdx.x == 0 && c.norm_out;
-        const float4 *W4 = reinterpret_cast<const float4 *>(c.W_norm);
-        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
-            float4 g[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                g[u] = v < K4 ? __ldcg(W4 + v) : z4;
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                float4 x = s_act[act_index<R>(v >> 3, v & 7)];
-                x.x = (x.x * inv) * g[u].x; x.y = (x.y * inv) * g[u].y;
-                x.z = (x.z * inv) * g[u].z; x.w = (x.w * inv) * g[u].w;
-                if (write_norm) reinterpret_cast<float4 *>(c.norm_out)[v] = x;
-                x.x *= code_prescale(0);
-                x.y *= code_prescale(1);
-                x.z *= code_prescale(2);
-                x.w *= code_prescale(3);
-                s_act[act_index<R>(v >> 3, v & 7)] = x;
-            }
-        }
-    } else {
-        for (int v0 = ctid; v0 < K4; v0 += 2 * kB * kCT) {
-            float4 x[2 * kB];
-#pragma unroll
-            for (int u = 0; u < 2 * kB; ++u) {
-                const int v = v0 + u * kCT;
-                x[u] = v < K4 ? __ldcg(A4 + v) : z4;
-            }
-#pragma unroll
-            for (int u = 0; u < 2 * kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                x[u].x *= code_prescale(0);
-                x[u].y *= code_prescale(1);
-                x[u].z *= code_prescale(2);
-                x[u].w *= code_prescale(3);
-                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
-            }
-        }
-    }
-    named_barrier_sync(1, kCT);
-    // activation sum of each chunk group (unscaled, fixed order)
-    for (int jg = ctid; jg < c.KP; jg += kCT) {
-        float a = 0.0f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int t = jg * R + r;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = s_act[act_index<R>(t, j)];
-                a += x.x * (1.0f / code_prescale(0));
-                a += x.y * (1.0f / code_prescale(1));
-                a += x.z * (1.0f / code_prescale(2));
-                a += x.w * (1.0f / code_prescale(3));
-            }
-        }
-        s_asum[jg] = a;
-    }
-    named_barrier_sync(1, kCT);
+    // them) ----
+    stage_activations<R, NORM, kCT, LoadL2>(c.K, c.KP, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
+                                            c.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm, ctid, 1);
     if (first_call && ctid == 0) mbar_arrive(sh.ready);
 
     // ---- warp slots ----
@@ -344,12 +247,10 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
             return reinterpret_cast<const uint4 *>(sl + mat * c.mat_w) + (size_t)(sc0 + lc) * c.KC;
         };
         // One chunk group (R chunks) of all kSPW streams.
-        auto chunk_group_dot = [&](int jg, const uint4 (&wq)[kSPW][R]) {
-            const int t0 = jg * R;
-            const int grp = chunk_group(t0, c.group_magic);
-            const float asum = s_asum[jg];
+        auto group_dot = [&](int jg, const uint4 (&wq)[kSPW][R]) {
+            const int grp = chunk_group(jg * R, c.group_magic);
             float sc[kSPW];
-            ZeroFold zf[kSPW];
+            HalfZero hz[kSPW];
 #pragma unroll
             for (int q = 0; q < kSPW; ++q) {
                 const int mat = NMAT == 2 ? (q / CPS) : 0;
@@ -357,45 +258,9 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
                 lc = lc < nc ? lc : 0;
                 const int si = (sc0 + lc) * c.G + grp;
                 sc[q] = srow[mat][si];
-                zf[q] = fold_zero(zrow[mat][si]);
+                hz[q] = half_zero(zrow[mat][si]);
             }
-            // two independent accumulators per stream (words 0-1 and 2-3)
-            f32x2 in0[kSPW], in1[kSPW];
-#pragma unroll
-            for (int q = 0; q < kSPW; ++q) {
-                in0[q] = pack2(0.0f, 0.0f);
-                in1[q] = pack2(0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                // the chunk's 32 activations, loaded before any use
-                ulonglong2 av[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    av[j] = reinterpret_cast<const ulonglong2 *>(s_act)[act_index<R>(t0 + r, j)];
-#pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-                    const ulonglong2 lo = av[2 * wd];
-                    const ulonglong2 hi = av[2 * wd + 1];
-#pragma unroll
-                    for (int q = 0; q < kSPW; ++q) {
-                        const uint32_t word = wd == 0 ? wq[q][r].x : wd == 1 ? wq[q][r].y
-                                            : wd == 2 ? wq[q][r].z : wq[q][r].w;
-                        const CodePairs cp = extract_word(word, magic);
-                        f32x2 a = wd < 2 ? in0[q] : in1[q];
-                        a = fma2(lo.x, add2(cp.p01, zf[q].nc01), a);
-                        a = fma2(lo.y, add2(cp.p23, zf[q].nc23), a);
-                        a = fma2(hi.x, add2(cp.p45, zf[q].nc01), a);
-                        a = fma2(hi.y, add2(cp.p67, zf[q].nc23), a);
-                        if (wd < 2) in0[q] = a; else in1[q] = a;
-                    }
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < kSPW; ++q) {
-                const float2 v = unpack2(add2(in0[q], in1[q]));
-                acc[q] = fmaf(sc[q], fmaf(zf[q].dz, asum, v.x + v.y), acc[q]);
-            }
+            chunk_group_dot<kSPW, R>(s_act, jg, s_asum[jg], wq, sc, hz, magic, acc);
         };
 
         if (!failed) {
@@ -407,7 +272,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
 #pragma unroll
                     for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + r];
                 }
-                chunk_group_dot(jg, wq);
+                group_dot(jg, wq);
             }
         }
         // this warp's slot of the ring entry has been read; the last of the
@@ -717,7 +582,7 @@ bool plan_sequence(const Call *calls, int n, SeqParams &prm, size_t &smem)
     prm.off_asum = prm.off_act + act;
     prm.off_norm = prm.off_asum + asum;
     prm.off_bar = prm.off_norm + 128u;
-    prm.magic_bits = kMagicBits;
+    prm.magic_bits = kHalfMagicBits;
     smem = prm.off_bar + bars;
     return true;
 }

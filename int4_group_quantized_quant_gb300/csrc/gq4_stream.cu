@@ -22,14 +22,16 @@
 //     slot (lane l owns 32-code chunk groups l, l+32, ...) and reduces it
 //     once with an xor reduce-scatter.  No cross-warp reduction, no group
 //     barriers in the steady state.
-//   * Activations are staged once per CTA in shared memory, pre-scaled by
-//     16^-p (see gq4_device.cuh) and XOR-swizzled so that a warp's 128-bit
-//     loads are conflict-free; every activation load serves all SPW streams.
-//     The RMSNorm prologue (x = A + A_b, inverse RMS, gain) is applied while
-//     staging, together with each chunk group's activation sum.
-//   * The integer part of each zero point is folded into the magic offset
-//     (exact), the fractional part is applied once per chunk group through
-//     the activation sum (see fold_zero).
+//   * Activations are staged once per CTA in shared memory, paired and
+//     pre-scaled for the fp16-pair unpack and XOR-swizzled so that a warp's
+//     128-bit loads are conflict-free (gq4_onelane.cuh); every activation
+//     load serves all SPW streams.  The RMSNorm prologue (x = A + A_b,
+//     inverse RMS, gain) is applied while staging, together with each chunk
+//     group's activation sum.
+//   * Codes are unpacked two per logic operation as fp16 pairs and widened
+//     with the integer part of the zero point subtracted in one exact add;
+//     the fractional part is applied once per chunk group through the
+//     activation sum (see gq4_device.cuh).
 //   * Every mbarrier wait is bounded in time; on expiry the kernel records
 //     an error in a device word (gq4_device_error) and leaves.
 #include <atomic>
@@ -37,6 +39,7 @@
 
 #include "gq4_device.cuh"
 #include "gq4_internal.h"
+#include "gq4_onelane.cuh"
 #include "gq4_tma.cuh"
 
 namespace gq4 {
@@ -66,7 +69,7 @@ struct StreamParams {
     uint32_t off_s[2], off_z[2];    // scale/zero rows of the CTA's range
     uint32_t off_act, off_asum, off_norm, off_bar;
     unsigned long long group_magic;
-    uint32_t magic_bits;  // kMagicBits, read from the parameter bank
+    uint32_t magic_bits;  // kHalfMagicBits, read from the parameter bank
     const float *A;
     const float *A_b;
     const float *W_norm;
@@ -214,113 +217,9 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // Consumer warps: prologue (activations into shared memory).
     // =====================================================================
     constexpr int kCT = kConsumerWarps * 32;
-    const int K4 = p.K >> 2;
-    // Activation loads are read-only (__ldg) and issued in batches of kB per
-    // thread before any use, so their latency is paid once per batch rather
-    // than once per element (the side-output stores in between would
-    // otherwise keep the compiler from hoisting them).
-    constexpr int kB = 6;
-    const float4 *A4 = reinterpret_cast<const float4 *>(p.A);
-    if constexpr (NORM) {
-        // One global pass: x = A + A_b (to shared memory, unscaled), its
-        // square sum; the gain is read in the second pass.
-        const float4 *B4 = reinterpret_cast<const float4 *>(p.A_b);
-        float part = 0.0f;
-        const bool write_res = blockIdx.x == 0 && p.residual_out;
-        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
-            float4 x[kB], b[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                x[u] = v < K4 ? __ldg(A4 + v) : z4;
-                b[u] = (v < K4 && B4) ? __ldg(B4 + v) : z4;
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                x[u].x += b[u].x; x[u].y += b[u].y; x[u].z += b[u].z; x[u].w += b[u].w;
-                if (write_res) reinterpret_cast<float4 *>(p.residual_out)[v] = x[u];
-                part = fmaf(x[u].x, x[u].x, part);
-                part = fmaf(x[u].y, x[u].y, part);
-                part = fmaf(x[u].z, x[u].z, part);
-                part = fmaf(x[u].w, x[u].w, part);
-                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) s_norm[warp] = part;
-        named_barrier(1, kCT);
-        float sum = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) sum += s_norm[w];
-        const float inv = 1.0f / sqrtf(sum / (float)p.K + p.eps);
-        const bool write_norm = blockIdx.x == 0 && p.norm_out;
-        const float4 *W4 = reinterpret_cast<const float4 *>(p.W_norm);
-        for (int v0 = ctid; v0 < K4; v0 += kB * kCT) {
-            float4 g[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                g[u] = v < K4 ? __ldg(W4 + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                float4 x = s_act[act_index<R>(v >> 3, v & 7)];
-                x.x = (x.x * inv) * g[u].x; x.y = (x.y * inv) * g[u].y;
-                x.z = (x.z * inv) * g[u].z; x.w = (x.w * inv) * g[u].w;
-                if (write_norm) reinterpret_cast<float4 *>(p.norm_out)[v] = x;
-                // pre-scale by 16^-p (exact): both halves of a word sit at p = 0..3
-                x.x *= code_prescale(0);
-                x.y *= code_prescale(1);
-                x.z *= code_prescale(2);
-                x.w *= code_prescale(3);
-                s_act[act_index<R>(v >> 3, v & 7)] = x;
-            }
-        }
-    } else {
-        for (int v0 = ctid; v0 < K4; v0 += 2 * kB * kCT) {
-            float4 x[2 * kB];
-#pragma unroll
-            for (int u = 0; u < 2 * kB; ++u) {
-                const int v = v0 + u * kCT;
-                x[u] = v < K4 ? __ldg(A4 + v) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int u = 0; u < 2 * kB; ++u) {
-                const int v = v0 + u * kCT;
-                if (v >= K4) continue;
-                x[u].x *= code_prescale(0);
-                x[u].y *= code_prescale(1);
-                x[u].z *= code_prescale(2);
-                x[u].w *= code_prescale(3);
-                s_act[act_index<R>(v >> 3, v & 7)] = x[u];
-            }
-        }
-    }
-    named_barrier(1, kCT);
-    // activation sum of each chunk group (unscaled, fixed order)
-    for (int jg = ctid; jg < p.KP; jg += kCT) {
-        float a = 0.0f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int t = jg * R + r;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = s_act[act_index<R>(t, j)];
-                a += x.x * (1.0f / code_prescale(0));
-                a += x.y * (1.0f / code_prescale(1));
-                a += x.z * (1.0f / code_prescale(2));
-                a += x.w * (1.0f / code_prescale(3));
-            }
-        }
-        s_asum[jg] = a;
-    }
-    named_barrier(1, kCT);
+    stage_activations<R, NORM, kCT, LoadReadOnly>(p.K, p.KP, p.A, p.A_b, p.W_norm, p.eps, p.residual_out,
+                                                  p.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm,
+                                                  ctid, 1);
     if (ctid == 0) mbar_arrive(ready);
 
     // =====================================================================
@@ -365,12 +264,10 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
             return reinterpret_cast<const uint4 *>(sl + p.off_w[mat]) + (size_t)(sub * CPS + lc) * p.KC;
         };
         // One chunk group (R chunks) of all SPW streams.
-        auto chunk_group_dot = [&](int jg, const uint4 (&wq)[SPW][R]) {
-            const int t0 = jg * R;
-            const int grp = chunk_group(t0, p.group_magic);
-            const float asum = s_asum[jg];
+        auto group_dot = [&](int jg, const uint4 (&wq)[SPW][R]) {
+            const int grp = chunk_group(jg * R, p.group_magic);
             float sc[SPW];
-            ZeroFold zf[SPW];
+            HalfZero hz[SPW];
 #pragma unroll
             for (int q = 0; q < SPW; ++q) {
                 const int mat = NMAT == 2 ? (q / CPS) : 0;
@@ -378,48 +275,9 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
                 lc = lc < nc ? lc : 0;
                 const int si = (lc0 + lc) * p.G + grp;
                 sc[q] = srow[mat][si];
-                zf[q] = fold_zero(zrow[mat][si]);
+                hz[q] = half_zero(zrow[mat][si]);
             }
-            // two independent accumulators per stream (words 0-1 and 2-3)
-            f32x2 in0[SPW], in1[SPW];
-#pragma unroll
-            for (int q = 0; q < SPW; ++q) {
-                in0[q] = pack2(0.0f, 0.0f);
-                in1[q] = pack2(0.0f, 0.0f);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                // the chunk's 32 activations, loaded before any use
-                ulonglong2 av[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    av[j] = reinterpret_cast<const ulonglong2 *>(s_act)[act_index<R>(t0 + r, j)];
-#pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-                    const ulonglong2 lo = av[2 * wd];
-                    const ulonglong2 hi = av[2 * wd + 1];
-#pragma unroll
-                    for (int q = 0; q < SPW; ++q) {
-                        const uint32_t word = wd == 0 ? wq[q][r].x : wd == 1 ? wq[q][r].y
-                                            : wd == 2 ? wq[q][r].z : wq[q][r].w;
-                        const CodePairs c = extract_word(word, magic);
-                        f32x2 a = wd < 2 ? in0[q] : in1[q];
-                        a = fma2(lo.x, add2(c.p01, zf[q].nc01), a);
-                        a = fma2(lo.y, add2(c.p23, zf[q].nc23), a);
-                        a = fma2(hi.x, add2(c.p45, zf[q].nc01), a);
-                        a = fma2(hi.y, add2(c.p67, zf[q].nc23), a);
-                        if (wd < 2) in0[q] = a; else in1[q] = a;
-                    }
-                }
-            }
-            f32x2 inner[SPW];
-#pragma unroll
-            for (int q = 0; q < SPW; ++q) inner[q] = add2(in0[q], in1[q]);
-#pragma unroll
-            for (int q = 0; q < SPW; ++q) {
-                const float2 v = unpack2(inner[q]);
-                acc[q] = fmaf(sc[q], fmaf(zf[q].dz, asum, v.x + v.y), acc[q]);
-            }
+            chunk_group_dot<SPW, R>(s_act, jg, s_asum[jg], wq, sc, hz, magic, acc);
         };
 
         if constexpr (NS > 0) {
@@ -443,7 +301,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
 #pragma unroll
                 for (int st = 0; st < NS; ++st) {
                     const int jg = lane + 32 * st;
-                    if (jg < p.KP) chunk_group_dot(jg, wreg[st]);
+                    if (jg < p.KP) group_dot(jg, wreg[st]);
                 }
             }
         } else {
@@ -456,7 +314,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
 #pragma unroll
                         for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + r];
                     }
-                    chunk_group_dot(jg, wq);
+                    group_dot(jg, wq);
                 }
             }
             // this warp's part of the stage has been read: release it
@@ -685,7 +543,7 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream)
     if (sms <= 0 || !plan_stream(call, prm, R, spw, ns, smem, sms)) return cudaErrorInvalidValue;
     const unsigned long long cpgrp = (unsigned long long)(call.gs / 32);
     prm.group_magic = ((1ull << 40) + cpgrp - 1) / cpgrp;
-    prm.magic_bits = kMagicBits;
+    prm.magic_bits = kHalfMagicBits;
     prm.A = call.A;
     if (call.norm) {
         prm.A_b = call.norm->A_b;
