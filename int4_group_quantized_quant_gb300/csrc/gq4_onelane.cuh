@@ -6,7 +6,8 @@
 // (a2, a6, a3/16, a7/16), chunk groups XOR-swizzled by act_index so that the
 // 32 lanes of a warp, reading 32 consecutive chunk groups, hit distinct
 // banks.  Each chunk group also keeps the sum of its unscaled activations,
-// which carries the fractional part of the zero points.
+// which carries the fractional part of the zero points.  Activations are
+// 16-byte aligned f32 vectors, read as float4.
 //
 // Operation (gerbil moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4 main loop and
 // WGSL_NORM_MATVEC_INT4 prologue): C[n] = sum_k a[k] * (q(n,k) - z) * s with,
@@ -40,124 +41,133 @@ __device__ __forceinline__ int act_slot(int u, int half)
     return act_index<R>(u >> 2, 2 * (u & 3) + half);
 }
 
-// Stages one call's activations (K a multiple of 32) and the chunk groups'
-// activation sums.  NT consumer threads (ctid < NT) take part; named barrier
-// `bar_id` synchronises them.  NORM: x = A + A_b (A_b may be null), then
-// a = x / sqrt(mean(x^2) + eps) * W_norm; when `side_outputs`, x is written to
-// residual_out and a to norm_out (either may be null).  Loads are issued in
-// batches of several words per thread before any use, so their latency is
-// paid once per batch.  s_norm holds NT/32 floats.
-template <int R, bool NORM, int NT, class Ld>
-__device__ __forceinline__ void stage_activations(int K, int KP, const float *A, const float *A_b,
+// Pairs the float4 x of an even lane with its odd neighbour's (one packed
+// word: a0..a3 and a4..a7) for word_dot, stores it, and stores the sum of
+// each chunk group (8R consecutive float4 = 8R consecutive lanes).  All
+// lanes of the warp take part; v is this lane's float4 index (v >= K4: out
+// of range, x zero, nothing stored).
+template <int R>
+__device__ __forceinline__ void pair_and_store(float4 x, int v, int K4, int lane, float4 *s_act,
+                                               float *s_asum)
+{
+    constexpr int kGL = 8 * R;
+    const bool odd = (lane & 1) != 0;
+    // the even lane keeps (a0, a4, a1, a5), the odd one (a2, a6, a3, a7)
+    const float r1 = __shfl_xor_sync(0xffffffffu, odd ? x.x : x.z, 1);
+    const float r2 = __shfl_xor_sync(0xffffffffu, odd ? x.y : x.w, 1);
+    const float4 pr = odd ? make_float4(r1, x.z, r2 * 0.0625f, x.w * 0.0625f)
+                          : make_float4(x.x, r1, x.y * 0.0625f, r2 * 0.0625f);
+    float a = (x.x + x.y) + (x.z + x.w);
+#pragma unroll
+    for (int off = 1; off < kGL; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (v < K4) {
+        s_act[act_slot<R>(v >> 1, v & 1)] = pr;
+        if ((lane & (kGL - 1)) == 0) s_asum[v / kGL] = a;
+    }
+}
+
+// Stages one call's activations (K a multiple of 32; K/32 even when R = 2)
+// and the chunk groups' activation sums.  NT consumer threads (ctid < NT)
+// take part; named barrier `bar_id` synchronises them.  NORM: x = A + A_b
+// (A_b may be null), then a = x / sqrt(mean(x^2) + eps) * W_norm; when
+// `side_outputs`, x is written to residual_out and a to norm_out (either may
+// be null).  s_norm holds NT/32 floats.
+//
+// Consecutive lanes own consecutive float4 of the vector (coalesced loads),
+// up to NV per thread per batch, all issued before any use: for K <= 4*NV*NT
+// the whole prologue pays one round trip to L2 (the norm gain included).
+// Longer vectors take several batches; with NORM, x then waits in shared
+// memory for the inverse RMS.
+template <int R, bool NORM, int NT, int NV, class Ld>
+__device__ __forceinline__ void stage_activations(int K, const float *A, const float *A_b,
                                                   const float *W_norm, float eps, float *residual_out,
                                                   float *norm_out, bool side_outputs, float4 *s_act,
                                                   float *s_asum, float *s_norm, int ctid, int bar_id)
 {
-    constexpr int kB = NORM ? 3 : 6;  // words per thread per batch
     constexpr int kWarps = NT / 32;
-    const int Kw = K >> 3;  // packed words per column
+    constexpr int kBatch = NV * NT;
+    const int K4 = K >> 2;
+    const int lane = ctid & 31;
     const float4 *A4 = reinterpret_cast<const float4 *>(A);
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if constexpr (NORM) {
         const float4 *B4 = reinterpret_cast<const float4 *>(A_b);
-        float part = 0.0f;
+        const float4 *W4 = reinterpret_cast<const float4 *>(W_norm);
+        const bool one_batch = K4 <= kBatch;
         float4 *res4 = side_outputs ? reinterpret_cast<float4 *>(residual_out) : nullptr;
-        for (int u0 = ctid; u0 < Kw; u0 += kB * NT) {
-            float4 x[kB][2], b[kB][2];
+        float4 x[NV], g[NV];
+        float part = 0.0f;
+        for (int b0 = 0; b0 < K4; b0 += kBatch) {
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    x[i][h] = u < Kw ? Ld::ld(A4 + 2 * u + h) : z4;
-                    b[i][h] = (u < Kw && B4) ? Ld::ld(B4 + 2 * u + h) : z4;
-                }
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                x[i] = v < K4 ? Ld::ld(A4 + v) : z4;
+                const float4 b = (v < K4 && B4) ? Ld::ld(B4 + v) : z4;
+                if (b0 == 0) g[i] = v < K4 ? Ld::ld(W4 + v) : z4;
+                x[i].x += b.x; x[i].y += b.y; x[i].z += b.z; x[i].w += b.w;
             }
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-                if (u >= Kw) continue;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float4 &v = x[i][h];
-                    v.x += b[i][h].x; v.y += b[i][h].y; v.z += b[i][h].z; v.w += b[i][h].w;
-                    if (res4) res4[2 * u + h] = v;
-                    part = fmaf(v.x, v.x, part);
-                    part = fmaf(v.y, v.y, part);
-                    part = fmaf(v.z, v.z, part);
-                    part = fmaf(v.w, v.w, part);
-                    s_act[act_slot<R>(u, h)] = v;  // natural order, unscaled for now
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                if (v - lane >= K4) break;  // warp-uniform: the rest of the batch is past the end
+                if (v < K4) {
+                    if (res4) res4[v] = x[i];
+                    // several batches: x waits in shared memory (natural order)
+                    if (!one_batch) s_act[act_slot<R>(v >> 1, v & 1)] = x[i];
                 }
+                part = fmaf(x[i].x, x[i].x, part);
+                part = fmaf(x[i].y, x[i].y, part);
+                part = fmaf(x[i].z, x[i].z, part);
+                part = fmaf(x[i].w, x[i].w, part);
             }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if ((ctid & 31) == 0) s_norm[ctid >> 5] = part;
+        if (lane == 0) s_norm[ctid >> 5] = part;
         onelane_bar(bar_id, NT);
         float sum = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) sum += s_norm[w];
         const float inv = 1.0f / sqrtf(sum / (float)K + eps);
         float4 *nrm4 = side_outputs ? reinterpret_cast<float4 *>(norm_out) : nullptr;
-        const float4 *W4 = reinterpret_cast<const float4 *>(W_norm);
-        for (int u0 = ctid; u0 < Kw; u0 += kB * NT) {
-            float4 g[kB][2];
+        for (int b0 = 0; b0 < K4; b0 += kBatch) {
+            if (!one_batch) {
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) g[i][h] = u < Kw ? Ld::ld(W4 + 2 * u + h) : z4;
+                for (int i = 0; i < NV; ++i) {
+                    const int v = b0 + ctid + i * NT;
+                    x[i] = v < K4 ? s_act[act_slot<R>(v >> 1, v & 1)] : z4;
+                    if (b0 > 0) g[i] = v < K4 ? Ld::ld(W4 + v) : z4;
+                }
+                // every lane has read its own slots before any pair is written
+                __syncwarp();
             }
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-                if (u >= Kw) continue;
-                float4 a[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const float4 v = s_act[act_slot<R>(u, h)];
-                    a[h].x = (v.x * inv) * g[i][h].x;
-                    a[h].y = (v.y * inv) * g[i][h].y;
-                    a[h].z = (v.z * inv) * g[i][h].z;
-                    a[h].w = (v.w * inv) * g[i][h].w;
-                    if (nrm4) nrm4[2 * u + h] = a[h];
-                }
-                float4 lo, hi;
-                pair_activations(a[0], a[1], lo, hi);
-                s_act[act_slot<R>(u, 0)] = lo;
-                s_act[act_slot<R>(u, 1)] = hi;
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                if (v - lane >= K4) break;  // warp-uniform: the rest of the batch is past the end
+                x[i].x = (x[i].x * inv) * g[i].x;
+                x[i].y = (x[i].y * inv) * g[i].y;
+                x[i].z = (x[i].z * inv) * g[i].z;
+                x[i].w = (x[i].w * inv) * g[i].w;
+                if (nrm4 && v < K4) nrm4[v] = x[i];
+                pair_and_store<R>(x[i], v, K4, lane, s_act, s_asum);
             }
         }
     } else {
-        for (int u0 = ctid; u0 < Kw; u0 += kB * NT) {
-            float4 x[kB][2];
+        for (int b0 = 0; b0 < K4; b0 += kBatch) {
+            float4 x[NV];
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) x[i][h] = u < Kw ? Ld::ld(A4 + 2 * u + h) : z4;
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                x[i] = v < K4 ? Ld::ld(A4 + v) : z4;
             }
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
-                const int u = u0 + i * NT;
-                if (u >= Kw) continue;
-                float4 lo, hi;
-                pair_activations(x[i][0], x[i][1], lo, hi);
-                s_act[act_slot<R>(u, 0)] = lo;
-                s_act[act_slot<R>(u, 1)] = hi;
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                if (v - lane >= K4) break;  // warp-uniform: the rest of the batch is past the end
+                pair_and_store<R>(x[i], v, K4, lane, s_act, s_asum);
             }
         }
-    }
-    onelane_bar(bar_id, NT);
-    // activation sum of each chunk group (unscaled, fixed order)
-    for (int jg = ctid; jg < KP; jg += NT) {
-        float a = 0.0f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a += paired_sum(s_act[act_index<R>(jg * R + r, j)]);
-        }
-        s_asum[jg] = a;
     }
     onelane_bar(bar_id, NT);
 }

@@ -47,6 +47,7 @@ __device__ unsigned int g_seq_error = 0;
 namespace {
 
 constexpr int kConsumerWarps = 8;
+constexpr int kActBatch = 2;  // activation float4 per consumer thread per prologue batch (register budget: the kernel holds every call variant)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kCT = kConsumerWarps * 32;
 constexpr int kSPW = 4;          // weight streams per warp slot
@@ -206,8 +207,9 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
 
     // ---- prologue: activations (through L2: earlier calls may have written
     // them) ----
-    stage_activations<R, NORM, kCT, LoadL2>(c.K, c.KP, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
-                                            c.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm, ctid, 1);
+    stage_activations<R, NORM, kCT, kActBatch, LoadL2>(c.K, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
+                                                       c.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm,
+                                                       ctid, 1);
     if (first_call && ctid == 0) mbar_arrive(sh.ready);
 
     // ---- warp slots ----

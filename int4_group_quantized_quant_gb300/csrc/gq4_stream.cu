@@ -50,6 +50,7 @@ __device__ unsigned int g_device_error = 0;
 namespace {
 
 constexpr int kConsumerWarps = 8;
+constexpr int kActBatch = 12;  // activation float4 per consumer thread per prologue batch
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 32;
 constexpr uint32_t kSmemLimit = 220u * 1024u;
@@ -87,6 +88,11 @@ struct StreamParams {
 __device__ __forceinline__ void named_barrier(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void record_error(unsigned int bits)
@@ -135,22 +141,25 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     const int n_stages = (ncols + stage_cols - 1) / stage_cols;
     const int n_slots = (ncols + CPS - 1) / CPS;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < p.S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], p.wps);
-            s_seq[s] = -1;
-        }
-        mbar_init(ready, 1);
-        mbar_init(srows, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-
     // =====================================================================
-    // Producer warp.
+    // Producer warp.  Its lane 0 initialises the mbarriers and starts
+    // streaming at once; the consumers stage their activations meanwhile and
+    // meet it at named barrier 2 only before their first mbarrier operation,
+    // so neither waits for the other at the start.
     // =====================================================================
     if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            for (int s = 0; s < p.S; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], p.wps);
+                s_seq[s] = -1;
+            }
+            mbar_init(ready, 1);
+            mbar_init(srows, 1);
+            mbar_fence_init();
+        }
+        __syncwarp();
+        named_barrier_arrive(2, kThreads);
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
@@ -217,9 +226,10 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // Consumer warps: prologue (activations into shared memory).
     // =====================================================================
     constexpr int kCT = kConsumerWarps * 32;
-    stage_activations<R, NORM, kCT, LoadReadOnly>(p.K, p.KP, p.A, p.A_b, p.W_norm, p.eps, p.residual_out,
-                                                  p.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm,
-                                                  ctid, 1);
+    stage_activations<R, NORM, kCT, kActBatch, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, p.eps,
+                                                             p.residual_out, p.norm_out, blockIdx.x == 0,
+                                                             s_act, s_asum, s_norm, ctid, 1);
+    named_barrier(2, kThreads);  // the producer has initialised the mbarriers
     if (ctid == 0) mbar_arrive(ready);
 
     // =====================================================================
