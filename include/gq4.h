@@ -195,6 +195,22 @@ GQ4_API size_t gq4_sequence_workspace_bytes(void);
 GQ4_API gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace,
                                     cudaStream_t stream);
 
+/* Allocation-free form of gq4_run_sequence, for callers that cannot
+ * allocate device memory.  The pages have no counterpart to it: it changes
+ * only where the launch's scratch lives.  Same calls, validation, semantics
+ * and results as gq4_run_sequence; the grid barrier's counters
+ * (gq4_sequence_workspace_bytes() bytes) live in a fixed 256-byte array of
+ * this library on the current device instead of a caller workspace.  A
+ * sequence whose scratch would exceed that array is rejected with
+ * GQ4_ERR_INVALID_ARG before anything is enqueued.  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine; the array's
+ * address is looked up once per device.  The counters must start at zero:
+ * every call enqueues a cudaMemsetAsync of them on `stream` before its
+ * launch.  All such calls on one device share the array, so calls that
+ * overlap on the GPU (other streams, other host threads) race: the caller
+ * must order them. */
+GQ4_API gq4_status gq4_run_sequence_static(const gq4_call *calls, int n_calls, cudaStream_t stream);
+
 /* Integer unpack test kernel: q[n*K + k] = q(n,k) as u8 [N][K].
  * Uses the same in-register extraction as the matvec kernels.
  * Requires K % 32 == 0. */

@@ -372,6 +372,20 @@ gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace,
     return GQ4_OK;
 }
 
+gq4_status gq4_run_sequence_static(const gq4_call *calls, int n_calls, cudaStream_t stream)
+{
+    if (n_calls < 0 || (n_calls > 0 && !calls)) return GQ4_ERR_INVALID_ARG;
+    if (n_calls == 0) return GQ4_OK;
+    // the launch's scratch must fit the static array
+    const size_t need = gq4::kSeqWorkspaceBytes;
+    if (need > gq4::seq_static_scratch_bytes()) return GQ4_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    if (gq4::seq_static_scratch(&scratch) != cudaSuccess) return GQ4_ERR_CUDA;
+    // what must start at zero: the barrier counters
+    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return GQ4_ERR_CUDA;
+    return gq4_run_sequence(calls, n_calls, scratch, stream);
+}
+
 gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream)
 {
     if (K <= 0 || N <= 0 || K % 32 != 0 || K > kMaxK) return GQ4_ERR_INVALID_ARG;

@@ -49,6 +49,8 @@ constexpr size_t kSeqWorkspaceBytes = 128;
 bool sequence_plannable(const Call *calls, int n);
 cudaError_t launch_sequence(const Call *calls, int n, void *workspace, cudaStream_t stream);
 cudaError_t read_seq_device_error(unsigned int *bits, bool clear);
+size_t seq_static_scratch_bytes();
+cudaError_t seq_static_scratch(void **ptr);
 
 // The sticky device-side error words (read, optionally clear): the one-lane
 // streaming path's and the tensor-core path's.

@@ -649,6 +649,38 @@ cudaError_t launch_sequence(const Call *calls, int n, void *workspace, cudaStrea
     return cudaGetLastError();
 }
 
+// Scratch of the allocation-free sequence entry point: the grid barrier's
+// counters in a fixed device array of this library instead of a caller
+// buffer (zero when the module loads; a completed launch leaves it zero).
+constexpr size_t kSeqStaticScratchBytes = 256;
+static_assert(kSeqWorkspaceBytes <= kSeqStaticScratchBytes, "sequence scratch exceeds its static array");
+__device__ __align__(256) unsigned char g_seq_static_scratch[kSeqStaticScratchBytes];
+
+size_t seq_static_scratch_bytes()
+{
+    return kSeqStaticScratchBytes;
+}
+
+cudaError_t seq_static_scratch(void **ptr)
+{
+    // Looked up once per device, with that device current (the caller's).
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_seq_static_scratch);
+        if (err != cudaSuccess) return err;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+
 cudaError_t read_seq_device_error(unsigned int *bits, bool clear)
 {
     cudaError_t err = cudaMemcpyFromSymbol(bits, g_seq_error, sizeof(unsigned int));

@@ -64,6 +64,7 @@ _SIGS = {
     "gq4_gated_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                          _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
+    "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
     "gq4_unpack": [_i, _i, _vp, _vp, _vp],
     "gq4_dequant": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
 }
@@ -308,6 +309,12 @@ def run_sequence(calls, workspace, stream=None):
     arr = (Call * max(len(calls), 1))(*[c.desc for c in calls])
     _check(lib.gq4_run_sequence(arr, len(calls), _ptr(workspace), _stream(stream)),
            "gq4_run_sequence")
+
+
+def run_sequence_static(calls, stream=None):
+    """Run the calls in order with the library's fixed scratch (gq4_run_sequence_static)."""
+    arr = (Call * max(len(calls), 1))(*[c.desc for c in calls])
+    _check(lib.gq4_run_sequence_static(arr, len(calls), _stream(stream)), "gq4_run_sequence_static")
 
 
 def unpack(Bq, K, q=None, stream=None):
