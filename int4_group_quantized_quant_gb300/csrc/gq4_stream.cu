@@ -90,6 +90,17 @@ __device__ __forceinline__ void named_barrier(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Programmatic dependent launch (PTX griddepcontrol, sm_90 and later).
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier_arrive(int id, int threads)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -226,6 +237,10 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // Consumer warps: prologue (activations into shared memory).
     // =====================================================================
     constexpr int kCT = kConsumerWarps * 32;
+    // The activations may be the previous kernel's outputs: wait for that
+    // grid to complete (its writes visible).  The producer does not wait: the
+    // weights do not depend on it, so they stream in meanwhile.
+    grid_dependency_wait();
     stage_activations<R, NORM, kCT, kActBatch, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, p.eps,
                                                              p.residual_out, p.norm_out, blockIdx.x == 0,
                                                              s_act, s_asum, s_norm, ctid, 1);
@@ -249,6 +264,13 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     }
 
     for (int i = warp; i < n_slots; i += kConsumerWarps) {
+        // A warp starting its last slot lets the next kernel in the stream be
+        // scheduled (once every CTA has done so or left): its CTAs then take
+        // SMs as this grid's CTAs leave and start streaming their weights; it
+        // reads this grid's outputs only after its own dependency wait.
+        // Signalling at the start would let a third kernel queue for SMs
+        // ahead of the second's.
+        if (i + kConsumerWarps >= n_slots && lane == 0) grid_dependents_launch();
         const int stage = i / p.wps;
         const int sub = i - stage * p.wps;
         const int ring = stage % p.S;
@@ -424,14 +446,32 @@ cudaError_t launch_stream_variant(const StreamParams &prm, size_t smem, cudaStre
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)(kSmemLimit + 4096u));
         if (err != cudaSuccess) return err;
+        // every variant takes the same (largest) shared-memory carveout, so
+        // an SM never has to drain to change it between consecutive calls
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < kMaxDevices) smem_ready[dev].store(1, std::memory_order_release);
     }
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return err;
     int grid = sms;
     if (grid > prm.n_units) grid = prm.n_units;
-    kern<<<grid, kThreads, smem, stream>>>(prm);
-    return cudaGetLastError();
+    // Launched with programmatic stream serialization: this kernel's CTAs may
+    // start while the previous kernel in the stream finishes (its producer
+    // then streams weights early); its consumers wait for that kernel's
+    // completion before reading activations (griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 template <int NMAT, bool NORM, int EPI>
