@@ -482,7 +482,9 @@ bool plan_stream(const Call &call, StreamParams &prm, int &R, int &spw, size_t &
     const uint32_t fixed = act_bytes + asum_bytes + 2u * call.nmat * rows_bytes + 128u +
                            (2 * kMaxStages + 2) * 8u + kMaxStages * 4u;
     const int spw_first = long_cols ? 2 : 4, spw_last = 2;
-    const uint32_t stage_cap = (long_cols ? 12u : 48u) * 1024u;
+    // stage size cap (gate/up pairs: 24 KB, measured 16.1 -> 15.4 us on
+    // 4096 -> 2 x 11008 against 48 KB; 12 KB is slower again)
+    const uint32_t stage_cap = (long_cols ? 12u : call.nmat == 2 ? 24u : 48u) * 1024u;
     for (spw = spw_first; spw >= spw_last; spw /= 2) {
         const int cps = call.nmat == 2 ? spw / 2 : spw;
         // warp slots per stage: aim at ~32-48 KB per bulk copy round (long
