@@ -51,11 +51,11 @@
  *   - Outputs must not overlap each other or any input (GQ4_ERR_ALIAS).
  *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
  *     Stream order holds for activations, norm inputs and outputs.  One
- *     exception for weights: a one-lane (M = 1) call is launched with
- *     programmatic dependent launch, so it may start reading its Bq, scales
- *     and zeros while the one-lane call just before it on the same stream is
- *     still running.  The weights of a one-lane call must therefore not be
- *     written by the one-lane call immediately preceding it on the stream.
+ *     exception for weights: calls with M = 1 or 16 <= M <= 32 are launched
+ *     with programmatic dependent launch, so such a call may start reading
+ *     its Bq, scales and zeros while the call just before it on the same
+ *     stream (if it is one of these) is still running.  The weights of a call
+ *     must therefore not be written by the call immediately preceding it.
  *   - Results are deterministic: the same inputs give the same bits.
  *   - Arithmetic: with M = 1 or 2 <= M <= 15 lanes every product and sum is
  *     f32 (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot

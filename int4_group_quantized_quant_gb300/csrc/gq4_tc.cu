@@ -366,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         // chunk c of lane m by cluster (m * n_chunks + c) mod n_clusters
         auto writer = [&](int mm, int c) { return (mm * n_chunks + c) % p.n_clusters == cid; };
         bool ok = true;
+        // the activations may be the previous kernel's outputs
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if constexpr (NORM) {
             // One pass over A and A_b: x = A + A_b to bf16 in place (and x
             // itself to residual_out), its square sum; then the staged x is
@@ -520,6 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         const int srow = r >> p.logP;
         int slot = 0, phase = 0, tl = 0, sir = 0;
         for (int i = 0; ok && i < n_stages_total; ++i) {
+            // The last stage lets the next kernel in the stream be scheduled
+            // (once every CTA has done so or left); earlier, a third kernel
+            // could queue for SMs ahead of the second.
+            if (i == n_stages_total - 1 && threadIdx.x == 0)
+                asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             // warp-uniform outcome: the collective tensor-memory stores below
             // need every lane
             if (!__all_sync(0xffffffffu, tc_wait(&sh.full[slot], phase, abort, false))) {
@@ -1095,7 +1102,7 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
     }
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)(pl.n_clusters * pl.ks));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = pl.smem;
@@ -1104,8 +1111,14 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
     attr[0].val.clusterDim.x = pl.ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic stream serialization: the CTAs may start while the
+    // previous kernel in the stream finishes (the producer streams weights at
+    // once); the dequant warps wait for that kernel's completion
+    // (griddepcontrol.wait) before reading activations.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if ((err = cudaLaunchKernelEx(&cfg, kern, prm)) != cudaSuccess) return err;
     return cudaGetLastError();
 }
