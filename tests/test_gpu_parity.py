@@ -46,6 +46,7 @@ MATVEC_CASES = [
     (1, 11008, 37, 128),     # 86 groups per column (8-byte aligned scale rows)
     (1, 12800, 19, 256),     # two K tiles of staged activations at M=1
     (7, 4096, 23, 64),       # several K tiles at M>4
+    (1, 65536, 9, 128),      # K past the one-lane kernel's shared-memory plan (general kernel)
 ]
 
 
@@ -104,6 +105,7 @@ NORM_CASES = [
     (4, 4096, 50, 128, True),                  # stack hidden size at M=4 (largest K tile)
     (2, 11008, 30, 128, True),                 # ffn size at M=2 (largest K tile)
     (32, 512, 20, 32, True),
+    (1, 12800, 40, 256, True),                 # one lane, K past one prologue batch
 ]
 
 
