@@ -118,41 +118,15 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
         zp[s] = p.zeros[mat] + (size_t)c * p.G;
     }
 
-    // ---- RMSNorm prologue: inverse RMS of x = A + A_b per lane ----
-    if constexpr (NORM) {
-        const int K4 = p.K >> 2;
+    // RMSNorm: the inverse RMS is a per-lane scalar, so it is taken out of
+    // the dot product: the staged activations are x * W_norm (x = A + A_b),
+    // the square sum of x is accumulated while staging (each CTA stages all
+    // of K), and the finished sums are scaled by 1/sqrt(sum/K + eps).  Each
+    // lane's elements go to threads in a fixed order independent of MB, so a
+    // lane's result does not depend on the lane count.
+    float sq[MB];
 #pragma unroll
-        for (int m = 0; m < MB; ++m) {
-            float part = 0.0f;
-            if (m < nb) {
-                const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)(m0 + m) * p.K);
-                const float4 *b4 = p.A_b ? reinterpret_cast<const float4 *>(p.A_b + (size_t)(m0 + m) * p.K)
-                                         : nullptr;
-                for (int v = tid; v < K4; v += kThreads) {
-                    float4 x = a4[v];
-                    if (b4) {
-                        const float4 b = b4[v];
-                        x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
-                    }
-                    part = fmaf(x.x, x.x, part);
-                    part = fmaf(x.y, x.y, part);
-                    part = fmaf(x.z, x.z, part);
-                    part = fmaf(x.w, x.w, part);
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-            if (lane == 0) s_part[warp][m] = part;
-        }
-        __syncthreads();
-        if (tid < MB) {
-            float sum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) sum += s_part[w][tid];
-            s_inv[tid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
-        }
-        // made visible by the barrier at the top of the tile loop
-    }
+    for (int m = 0; m < MB; ++m) sq[m] = 0.0f;
 
     float acc[MB][kStreams];
 #pragma unroll
@@ -165,36 +139,37 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
     for (int t = 0; t < p.n_ktiles; ++t) {
         const int kc0 = t * p.kct;
         const int kcn = min(p.kct, p.KC - kc0);
-        __syncthreads();  // previous tile consumed (and s_inv visible)
+        __syncthreads();  // previous tile consumed
 
         // ---- stage activations of this K tile ----
         const int per_lane = kcn * 8;
-        for (int idx = tid; idx < MB * per_lane; idx += kThreads) {
-            const int m = idx / per_lane;
-            const int r = idx - m * per_lane;
-            const int c = r >> 3;
-            const int j = r & 7;
-            const size_t k = (size_t)(kc0 + c) * 32 + (size_t)j * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (m < nb) {
-                const size_t row = (size_t)(m0 + m) * p.K;
-                v = *reinterpret_cast<const float4 *>(p.A + row + k);
-                if constexpr (NORM) {
-                    if (p.A_b) {
-                        const float4 b = *reinterpret_cast<const float4 *>(p.A_b + row + k);
-                        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            for (int r = tid; r < per_lane; r += kThreads) {
+                const int c = r >> 3;
+                const int j = r & 7;
+                const size_t k = (size_t)(kc0 + c) * 32 + (size_t)j * 4;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (m < nb) {
+                    const size_t row = (size_t)(m0 + m) * p.K;
+                    v = *reinterpret_cast<const float4 *>(p.A + row + k);
+                    if constexpr (NORM) {
+                        if (p.A_b) {
+                            const float4 b = *reinterpret_cast<const float4 *>(p.A_b + row + k);
+                            v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+                        }
+                        if (write_norm_outputs && p.residual_out)
+                            *reinterpret_cast<float4 *>(p.residual_out + row + k) = v;
+                        sq[m] = fmaf(v.x, v.x, sq[m]);
+                        sq[m] = fmaf(v.y, v.y, sq[m]);
+                        sq[m] = fmaf(v.z, v.z, sq[m]);
+                        sq[m] = fmaf(v.w, v.w, sq[m]);
+                        const float4 g = *reinterpret_cast<const float4 *>(p.W_norm + k);
+                        v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
                     }
-                    if (write_norm_outputs && p.residual_out)
-                        *reinterpret_cast<float4 *>(p.residual_out + row + k) = v;
-                    const float inv = s_inv[m];
-                    const float4 g = *reinterpret_cast<const float4 *>(p.W_norm + k);
-                    v.x = (v.x * inv) * g.x; v.y = (v.y * inv) * g.y;
-                    v.z = (v.z * inv) * g.z; v.w = (v.w * inv) * g.w;
-                    if (write_norm_outputs && p.norm_out)
-                        *reinterpret_cast<float4 *>(p.norm_out + row + k) = v;
                 }
+                s_act[((size_t)m * p.kct + c) * 8 + (j ^ (c & 7))] = prescale(v);
             }
-            s_act[((size_t)m * p.kct + c) * 8 + (j ^ (c & 7))] = prescale(v);
         }
         __syncthreads();
 
@@ -278,6 +253,47 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
                 wq[s] = nwq[s];
                 sc[s] = nsc[s];
                 zr[s] = nzr[s];
+            }
+        }
+    }
+
+    if constexpr (NORM) {
+        // inverse RMS per lane: fixed xor tree within each warp, warps in order
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sq[m] += __shfl_xor_sync(0xffffffffu, sq[m], off);
+            if (lane == 0) s_part[warp][m] = sq[m];
+        }
+        __syncthreads();
+        if (tid < MB) {
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sum += s_part[w][tid];
+            s_inv[tid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < MB; ++m)
+#pragma unroll
+            for (int s = 0; s < kStreams; ++s) acc[m][s] *= s_inv[m];
+        // norm_out = (x * inv) * W_norm, written once (column tile 0)
+        if (write_norm_outputs && p.norm_out) {
+            const int K4 = p.K >> 2;
+            for (int m = 0; m < nb; ++m) {
+                const size_t row = (size_t)(m0 + m) * p.K;
+                const float inv = s_inv[m];
+                for (int v4 = tid; v4 < K4; v4 += kThreads) {
+                    float4 x = reinterpret_cast<const float4 *>(p.A + row)[v4];
+                    if (p.A_b) {
+                        const float4 b = reinterpret_cast<const float4 *>(p.A_b + row)[v4];
+                        x.x += b.x; x.y += b.y; x.z += b.z; x.w += b.w;
+                    }
+                    const float4 g = reinterpret_cast<const float4 *>(p.W_norm)[v4];
+                    x.x = (x.x * inv) * g.x; x.y = (x.y * inv) * g.y;
+                    x.z = (x.z * inv) * g.z; x.w = (x.w * inv) * g.w;
+                    reinterpret_cast<float4 *>(p.norm_out + row)[v4] = x;
+                }
             }
         }
     }
