@@ -26,6 +26,7 @@
 //   * Partial sums are reduced across the warp with a fixed xor butterfly,
 //     so results are deterministic and independent of where a column sits in
 //     a tile (quad == plain, lane == solo, bit for bit).
+#include <atomic>
 #include <cstdint>
 
 #include "gq4_device.cuh"
@@ -40,6 +41,9 @@ constexpr int kStreams = 2;                 // weight streams per warp
 // Activation tile, bytes: dynamic shared memory plus the kernel's static
 // arrays must stay within the 48 KB a launch gets without opting in.
 constexpr int kSmemBudget = 47 * 1024;
+// A whole-K activation tile may take up to this much (opt-in above 48 KB):
+// two CTAs still fit on an SM.
+constexpr size_t kSmemSingleMax = 100 * 1024;
 
 struct Fp32Params {
     int M, K, N, gs;
@@ -47,6 +51,7 @@ struct Fp32Params {
     int G;            // groups per column (K / gs)
     int kct;          // chunks per staged K tile
     int n_ktiles;
+    int col_tiles;    // tiles of columns; a CTA takes blockIdx.y, + gridDim.y, ...
     unsigned long long group_magic;  // ceil(2^40 / (gs / 32))
     uint32_t magic_bits;             // kMagicBits, read from the parameter bank
     const float *A;
@@ -99,7 +104,24 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
     const int lane = tid & 31;
     const int m0 = blockIdx.x * MB;
     const int nb = min(MB, p.M - m0);
-    const int col_base = (blockIdx.y * kWarps + warp) * CW;
+    // RMSNorm: the inverse RMS is a per-lane scalar, so it is taken out of
+    // the dot product: the staged activations are x * W_norm (x = A + A_b),
+    // the square sum of x is accumulated while staging (each CTA stages all
+    // of K), and the finished sums are scaled by 1/sqrt(sum/K + eps).  Each
+    // lane's elements go to threads in a fixed order independent of MB, so a
+    // lane's result does not depend on the lane count.
+    float sq[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) sq[m] = 0.0f;
+    const bool write_norm_outputs = NORM && blockIdx.y == 0;
+
+    // Column tiles blockIdx.y, + gridDim.y, ...  With a single K tile the
+    // activations are staged once and serve every column tile of the CTA
+    // (the grid is then sized to the resident CTAs); otherwise each CTA
+    // takes one column tile and stages K tile by tile.
+    for (int tile = blockIdx.y; tile < p.col_tiles; tile += gridDim.y) {
+    const bool first_tile = tile == (int)blockIdx.y;
+    const int col_base = (tile * kWarps + warp) * CW;
 
     // ---- the warp's two weight streams ----
     const uint4 *wp[kStreams];
@@ -118,29 +140,17 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
         zp[s] = p.zeros[mat] + (size_t)c * p.G;
     }
 
-    // RMSNorm: the inverse RMS is a per-lane scalar, so it is taken out of
-    // the dot product: the staged activations are x * W_norm (x = A + A_b),
-    // the square sum of x is accumulated while staging (each CTA stages all
-    // of K), and the finished sums are scaled by 1/sqrt(sum/K + eps).  Each
-    // lane's elements go to threads in a fixed order independent of MB, so a
-    // lane's result does not depend on the lane count.
-    float sq[MB];
-#pragma unroll
-    for (int m = 0; m < MB; ++m) sq[m] = 0.0f;
-
     float acc[MB][kStreams];
 #pragma unroll
     for (int m = 0; m < MB; ++m)
 #pragma unroll
         for (int s = 0; s < kStreams; ++s) acc[m][s] = 0.0f;
 
-    const bool write_norm_outputs = NORM && blockIdx.y == 0;
-
     for (int t = 0; t < p.n_ktiles; ++t) {
         const int kc0 = t * p.kct;
         const int kcn = min(p.kct, p.KC - kc0);
+        if (first_tile || p.n_ktiles > 1) {
         __syncthreads();  // previous tile consumed
-
         // ---- stage activations of this K tile ----
         const int per_lane = kcn * 8;
 #pragma unroll
@@ -172,6 +182,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
             }
         }
         __syncthreads();
+        }
 
         // ---- main loop: lane owns chunks lane, lane + 32, ... ----
         int c = lane;
@@ -258,7 +269,8 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
     }
 
     if constexpr (NORM) {
-        // inverse RMS per lane: fixed xor tree within each warp, warps in order
+        // inverse RMS per lane (once): fixed xor tree within each warp, warps in order
+        if (first_tile) {
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
 #pragma unroll
@@ -273,12 +285,13 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
             s_inv[tid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
         }
         __syncthreads();
+        }
 #pragma unroll
         for (int m = 0; m < MB; ++m)
 #pragma unroll
             for (int s = 0; s < kStreams; ++s) acc[m][s] *= s_inv[m];
         // norm_out = (x * inv) * W_norm, written once (column tile 0)
-        if (write_norm_outputs && p.norm_out) {
+        if (write_norm_outputs && first_tile && p.norm_out) {
             const int K4 = p.K >> 2;
             for (int m = 0; m < nb; ++m) {
                 const size_t row = (size_t)(m0 + m) * p.K;
@@ -307,7 +320,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
             for (int off = 16; off > 0; off >>= 1)
                 acc[m][s] += __shfl_xor_sync(0xffffffffu, acc[m][s], off);
 
-    if (lane != 0) return;
+    if (lane == 0) {
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
         if (m >= nb) break;
@@ -329,18 +342,46 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
             }
         }
     }
+    }  // lane 0
+    }  // column tiles
 }
 
 template <int MB, int NMAT, bool NORM, int EPI>
-cudaError_t launch_variant(const Fp32Params &prm, cudaStream_t stream)
+cudaError_t launch_variant(Fp32Params prm, cudaStream_t stream)
 {
+    auto kern = fp32_matvec_kernel<MB, NMAT, NORM, EPI>;
     const int lane_blocks = (prm.M + MB - 1) / MB;
     const int cols_per_cta = kWarps * (kStreams / NMAT);
-    const int col_tiles = (prm.N + cols_per_cta - 1) / cols_per_cta;
-    if (col_tiles > 65535) return cudaErrorInvalidConfiguration;
+    prm.col_tiles = (prm.N + cols_per_cta - 1) / cols_per_cta;
+    if (prm.col_tiles > 65535) return cudaErrorInvalidConfiguration;
     const size_t smem = (size_t)MB * prm.kct * 8 * sizeof(float4);
-    dim3 grid(lane_blocks, col_tiles);
-    fp32_matvec_kernel<MB, NMAT, NORM, EPI><<<grid, kThreads, smem, stream>>>(prm);
+    int grid_y = prm.col_tiles;
+    cudaError_t err;
+    if (smem > (size_t)kSmemBudget) {
+        // one K tile beyond the default 48 KB: opt in once per device
+        int dev = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+        constexpr int kMaxDevices = 64;
+        static std::atomic<unsigned char> ready[kMaxDevices];
+        if (dev < 0 || dev >= kMaxDevices || !ready[dev].load(std::memory_order_acquire)) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemSingleMax);
+            if (err != cudaSuccess) return err;
+            if (dev >= 0 && dev < kMaxDevices) ready[dev].store(1, std::memory_order_release);
+        }
+    }
+    if (prm.n_ktiles == 1) {
+        // activations staged once per CTA: as many CTAs as are resident
+        int dev = 0, sms = 0, per_sm = 0;
+        if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) != cudaSuccess)
+            return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        const int resident = (sms * per_sm + lane_blocks - 1) / lane_blocks;
+        if (grid_y > resident) grid_y = resident;
+    }
+    dim3 grid(lane_blocks, grid_y);
+    kern<<<grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
@@ -397,10 +438,17 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream)
     }
 
     const int MB = call.M == 1 ? 1 : call.M == 2 ? 2 : call.M <= 4 ? 4 : 8;
-    // K tiles hold a multiple of 32 chunks, so lane l owns chunks l, l+32, ...
-    // in increasing order whatever the tiling (results independent of MB).
-    const int kct_max = kSmemBudget / (MB * 8 * (int)sizeof(float4)) / 32 * 32;
-    prm.kct = prm.KC < kct_max ? prm.KC : kct_max;
+    // All of K in one tile when it fits kSmemSingleMax (the CTAs then stage
+    // once and loop over column tiles); otherwise K tiles of a multiple of 32
+    // chunks within the default 48 KB, so lane l owns chunks l, l+32, ... in
+    // increasing order whatever the tiling (results independent of MB).
+    const size_t whole = (size_t)MB * prm.KC * 8 * sizeof(float4);
+    if (whole <= kSmemSingleMax) {
+        prm.kct = prm.KC;
+    } else {
+        const int kct_max = kSmemBudget / (MB * 8 * (int)sizeof(float4)) / 32 * 32;
+        prm.kct = prm.KC < kct_max ? prm.KC : kct_max;
+    }
     prm.n_ktiles = (prm.KC + prm.kct - 1) / prm.kct;
 
     switch (MB) {
