@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     dequant_f32,
     dequant_f64,
     dot_cols,
+    gated_input_matvec,
     gated_matvec,
     load,
     matvec,

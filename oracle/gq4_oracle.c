@@ -14,6 +14,8 @@
  *   quad        -- concatenated outputs equal the unsplit matvec
  *   norm        -- closed form on constant input, scale invariance, f32 residual
  *   gated       -- all-ones up matrix gives sum(a), zero gate gives 0, composition
+ *   gated input -- sigmoid(0) halves, saturated gates pass or scale the input
+ *                  exactly, silu(0) gives exactly 0
  */
 #include "gq4_oracle.h"
 
@@ -305,4 +307,37 @@ int gq4o_gated_matvec(int M, int K, int N, int gs, const float *A,
     }
     if (a != norm_out) free(a);
     return rc;
+}
+
+/* sigmoid(t) = 1 / (1 + exp(-t)) (the attention SigmoidGate of the
+ * GatedMatVecInt4 fusion doc: "attn_out * sigmoid(gate)"). */
+static double sigmoid(double t)
+{
+    return 1.0 / (1.0 + exp(-t));
+}
+
+int gq4o_gated_input_matvec(int M, int K, int N, int gs, int kind, const float *X,
+                            const float *Gt, const uint32_t *Bq, const float *scales,
+                            const float *zeros, double *C, double *S, double *a_out)
+{
+    if (!shape_ok(M, K, N, gs) || !X || !Gt || !Bq || !scales || !zeros || !C) return -1;
+    if (kind != 0 && kind != 1) return -1;
+    double *a = a_out ? a_out : (double *)malloc(sizeof(double) * (size_t)M * (size_t)K);
+    if (!a) return -1;
+    /* The input vector: kind 0, x * sigmoid(g) (GatedMatVecInt4); kind 1,
+     * silu(g) * x (SwiGLUGatedMatVecInt4: "silu(gate) * up", x = up). */
+    for (size_t i = 0; i < (size_t)M * (size_t)K; ++i) {
+        const double x = (double)X[i], g = (double)Gt[i];
+        a[i] = kind == 0 ? x * sigmoid(g) : silu(g) * x;
+    }
+    for (int m = 0; m < M; ++m) {
+        const double *am = a + (size_t)m * K;
+        for (int n = 0; n < N; ++n) {
+            double sabs = 0.0;
+            C[(size_t)m * N + n] = gq4o_dot(K, gs, am, Bq, scales, zeros, n, &sabs);
+            if (S) S[(size_t)m * N + n] = sabs;
+        }
+    }
+    if (a != a_out) free(a);
+    return 0;
 }

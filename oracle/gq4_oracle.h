@@ -116,6 +116,16 @@ int gq4o_gated_matvec(int M, int K, int N, int gs, const float *A,
                       double *out, double *g, double *u, double *Sg,
                       double *Su, float *residual_out, double *norm_out);
 
+/* Gated-input matvec: the input vector is built from two [M][K] vectors and
+ * then multiplied like gq4o_matvec.  kind 0: a = X * sigmoid(G) (the
+ * attention SigmoidGate fused into o_proj, GatedMatVecInt4 fusion doc);
+ * kind 1: a = silu(G) * X (a standalone SwiGLU "silu(gate) * up" fused into
+ * the consuming projection, SwiGLUGatedMatVecInt4 fusion doc; X = up).
+ * C, S as gq4o_matvec; a_out (optional) receives a [M][K]. */
+int gq4o_gated_input_matvec(int M, int K, int N, int gs, int kind, const float *X,
+                            const float *G, const uint32_t *Bq, const float *scales,
+                            const float *zeros, double *C, double *S, double *a_out);
+
 #ifdef __cplusplus
 }
 #endif

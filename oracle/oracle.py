@@ -64,6 +64,8 @@ def load_library(path: str):
         "gq4o_norm_matvec": (_int, [_int, _int, _int, _int, _f32p, _f32p, _f32p,
                                     ctypes.c_float, _u32p, _f32p, _f32p, _f64p,
                                     _f64p, _f32p, _f64p]),
+        "gq4o_gated_input_matvec": (_int, [_int, _int, _int, _int, _int, _f32p, _f32p,
+                                           _u32p, _f32p, _f32p, _f64p, _f64p, _f64p]),
         "gq4o_gated_matvec": (_int, [_int, _int, _int, _int, _f32p, _f32p, _f32p,
                                      ctypes.c_float, _u32p, _f32p, _f32p, _u32p,
                                      _f32p, _f32p, _f64p, _f64p, _f64p, _f64p,
@@ -237,6 +239,23 @@ class Oracle:
         return out
 
 
+    def gated_input_matvec(self, kind, X, G, Bq, scales, zeros, K, N, gs):
+        """(C, S, a) for the gated input a = X*sigmoid(G) ("sigmoid") or silu(G)*X ("swiglu")."""
+        k = {"sigmoid": 0, "swiglu": 1}[kind]
+        X = _c(X, np.float32).reshape(-1, K)
+        M = X.shape[0]
+        G = _c(G, np.float32).reshape(M, K)
+        Bq, s, z = _c(Bq, np.uint32), _c(scales, np.float32), _c(zeros, np.float32)
+        C = np.empty((M, N), np.float64)
+        S = np.empty((M, N), np.float64)
+        a = np.empty((M, K), np.float64)
+        _check(self.lib.gq4o_gated_input_matvec(M, K, N, gs, k, _ptr(X, _f32p), _ptr(G, _f32p),
+                                              _ptr(Bq, _u32p), _ptr(s, _f32p), _ptr(z, _f32p),
+                                              _ptr(C, _f64p), _ptr(S, _f64p), _ptr(a, _f64p)),
+               "gated_input_matvec")
+        return C, S, a
+
+
 def _default(name):
     def call(*args, **kwargs):
         return getattr(load(), name)(*args, **kwargs)
@@ -256,3 +275,4 @@ quad_matvec = _default("quad_matvec")
 norm = _default("norm")
 norm_matvec = _default("norm_matvec")
 gated_matvec = _default("gated_matvec")
+gated_input_matvec = _default("gated_input_matvec")

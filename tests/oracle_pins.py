@@ -357,9 +357,63 @@ def pin_gated_norm(orc):
     assert np.array_equal(res["g"], g) and np.array_equal(res["u"], u)
 
 
+# ---------------------------------------------------------------------------
+# Gated input (GatedMatVecInt4: x * sigmoid(g); SwiGLUGatedMatVecInt4: silu(g) * x)
+# ---------------------------------------------------------------------------
+
+def _gated_input_problem(seed, M=2, K=256, N=9, gs=64):
+    r = _rng(seed)
+    G = K // gs
+    X = r.standard_normal((M, K)).astype(np.float32)
+    Bq = r.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    s = r.uniform(0.005, 0.02, size=(N, G)).astype(np.float32)
+    z = r.uniform(6, 9, size=(N, G)).astype(np.float32)
+    return X, Bq, s, z, K, N, gs
+
+
+def pin_gated_input_saturation(orc):
+    """sigmoid(0) = 1/2 halves the matvec exactly; a gate of 64 saturates sigmoid to 1
+    (the plain matvec) and silu to 64 (64 times it), exactly in double; silu(0) gives 0."""
+    X, Bq, s, z, K, N, gs = _gated_input_problem(17)
+    C0, S0 = orc.matvec(X, Bq, s, z, K, N, gs)
+    zero = np.zeros_like(X)
+    big = np.full_like(X, 64.0)
+    C, S, a = orc.gated_input_matvec("sigmoid", X, zero, Bq, s, z, K, N, gs)
+    assert np.array_equal(C, 0.5 * C0) and np.array_equal(S, 0.5 * S0)
+    assert np.array_equal(a, 0.5 * X.astype(np.float64))
+    C, S, _ = orc.gated_input_matvec("sigmoid", X, big, Bq, s, z, K, N, gs)
+    assert np.array_equal(C, C0) and np.array_equal(S, S0)
+    C, S, _ = orc.gated_input_matvec("swiglu", X, big, Bq, s, z, K, N, gs)
+    assert np.array_equal(C, 64.0 * C0) and np.array_equal(S, 64.0 * S0)
+    C, S, _ = orc.gated_input_matvec("swiglu", X, zero, Bq, s, z, K, N, gs)
+    assert np.all(C == 0.0) and np.all(S == 0.0)
+
+
+def pin_gated_input_values(orc):
+    """Through a one-hot weight (w = 1 at k = 0), the input element is returned:
+    sigmoid and silu at known points, and the roles of x and g are not swapped."""
+    K, N, gs = 8, 1, 8
+    codes = np.zeros((N, K), np.uint8)
+    codes[0, 0] = 1
+    Bq = orc.pack(codes)
+    s1 = np.ones((1, 1), np.float32)
+    z0 = np.zeros((1, 1), np.float32)
+    for x, g in [(1.0, 0.0), (2.0, 1.0), (-3.0, -1.0), (0.5, 20.0), (4.0, -2.5)]:
+        X = np.zeros((1, K), np.float32)
+        Gt = np.zeros((1, K), np.float32)
+        X[0, 0], Gt[0, 0] = x, g
+        sig = 1.0 / (1.0 + math.exp(-g))
+        C, _, _ = orc.gated_input_matvec("sigmoid", X, Gt, Bq, s1, z0, K, N, gs)
+        assert math.isclose(C[0, 0], x * sig, rel_tol=1e-15), (x, g, C[0, 0])
+        C, _, _ = orc.gated_input_matvec("swiglu", X, Gt, Bq, s1, z0, K, N, gs)
+        assert math.isclose(C[0, 0], g * sig * x, rel_tol=1e-15), (x, g, C[0, 0])
+
+
 ALL_PINS = [
     pin_fixed_words, pin_byte_view, pin_pack_round_trip, pin_one_hot, pin_dequant_f32,
     pin_brute_force_exact, pin_abs_sum, pin_zero_point_exact, pin_lanes_independent,
     pin_quad_routing, pin_norm_constant, pin_norm_scale_invariance, pin_norm_residual,
     pin_gated_closed_forms, pin_silu_values, pin_gated_norm,
+    pin_gated_input_saturation,
+    pin_gated_input_values,
 ]

@@ -39,6 +39,11 @@ MUTANTS = {
     "norm_sqrt_dropped": ("1.0 / sqrt(sum_sq", "1.0 / (sum_sq"),
     "silu_sign": ("t / (1.0 + exp(-t))", "t / (1.0 + exp(t))"),
     "gate_up_swapped": ("out[at] = silu(gv) * uv;", "out[at] = silu(uv) * gv;"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-t));", "return 1.0 / (1.0 + exp(t));"),
+    "gated_input_x_g_swapped": ("a[i] = kind == 0 ? x * sigmoid(g) : silu(g) * x;",
+                                "a[i] = kind == 0 ? g * sigmoid(x) : silu(x) * g;"),
+    "gated_input_kinds_swapped": ("a[i] = kind == 0 ? x * sigmoid(g) : silu(g) * x;",
+                                  "a[i] = kind == 1 ? x * sigmoid(g) : silu(g) * x;"),
     "dequant_f32_double_rounding_skipped": ("volatile float t = (float)gq4o_nibble(Bq, K, n, k) - zeros[g];",
                                             "volatile double t = (double)gq4o_nibble(Bq, K, n, k) - zeros[g];"),
 }
