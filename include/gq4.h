@@ -19,7 +19,13 @@
  *     fuseNormSwiGLUDecodeEntries docs (silu(gate) * up, optional residual +
  *     RMSNorm prologue);
  *   - batched lanes: executor declarations, buildBatchEntries doc (lanes run
- *     the same weights and never interact).
+ *     the same weights and never interact);
+ *   - dual projection: executor declarations, fuseDualMatVecDecodeEntries doc
+ *     (two projections sharing the input and K/N, numerics of two matvecs);
+ *   - gated inputs: executor declarations, fuseGatedOProjDecodeEntries doc
+ *     (attn_out * sigmoid(gate) into o_proj) and
+ *     fuseSwiGLUGatedProjDecodeEntries doc (silu(gate) * up into the
+ *     consuming projection).
  *
  * ---------------------------------------------------------------------------
  * Weight format (one int4 matrix of K inputs and N output columns, group size
@@ -148,6 +154,33 @@ GQ4_API gq4_status gq4_gated_matvec(int M, int K, int N, int group_size,
                             const uint32_t *Bq_up, const float *scales_up,
                             const float *zeros_up,
                             float *out, cudaStream_t stream);
+
+/* Dual projection (DualMatVecInt4): C0 = A . W0 and C1 = A . W1, two K x N
+ * matrices with the same group_size over the same input, in one launch.
+ * Each output equals gq4_matvec of its matrix within the fp32 tolerance; for
+ * M = 1 bit for bit (the same per-column arithmetic).  C0 and C1 are [M][N]
+ * and must not overlap each other or any input. */
+GQ4_API gq4_status gq4_dual_matvec(int M, int K, int N, int group_size, const float *A,
+                                   const uint32_t *Bq0, const float *scales0, const float *zeros0,
+                                   const uint32_t *Bq1, const float *scales1, const float *zeros1,
+                                   float *C0, float *C1, cudaStream_t stream);
+
+/* Sigmoid-gated input (GatedMatVecInt4): C = a . W with
+ * a[m][k] = X[m][k] * sigmoid(G[m][k]), sigmoid(t) = 1 / (1 + exp(-t))
+ * (X = the attention output, G = its gate).  X and G are [M][K], 16-byte
+ * aligned, read only; the gated vector is formed in the kernel (f32). */
+GQ4_API gq4_status gq4_sigmoid_gated_matvec(int M, int K, int N, int group_size, const float *X,
+                                            const float *G, const uint32_t *Bq,
+                                            const float *scales, const float *zeros, float *C,
+                                            cudaStream_t stream);
+
+/* SwiGLU-gated input (SwiGLUGatedMatVecInt4): C = a . W with
+ * a[m][k] = silu(G[m][k]) * X[m][k], silu(t) = t / (1 + exp(-t)) (G = the
+ * gate, X = the up vector).  Layout and rules as gq4_sigmoid_gated_matvec. */
+GQ4_API gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, const float *X,
+                                           const float *G, const uint32_t *Bq,
+                                           const float *scales, const float *zeros, float *C,
+                                           cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * One-lane call sequences (decode of a whole layer stack in one launch).

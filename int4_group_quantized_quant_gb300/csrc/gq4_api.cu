@@ -282,6 +282,59 @@ gq4_status build_seq_call(const gq4_call &c, gq4::Call &call)
     }
 }
 
+gq4_status build_dual(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq0,
+                      const float *scales0, const float *zeros0, const uint32_t *Bq1,
+                      const float *scales1, const float *zeros1, float *C0, float *C1,
+                      gq4::Call &call)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    GQ4_TRY(check_weights(Bq0, scales0, zeros0, K, N, group_size, rs));
+    GQ4_TRY(check_weights(Bq1, scales1, zeros1, K, N, group_size, rs));
+    if (!C0 || !C1) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(C0, (size_t)M * (size_t)N, rs));
+    GQ4_TRY(check_output(C1, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    call = base_call(M, K, N, group_size, A);
+    call.nmat = 2;
+    call.Bq[0] = Bq0;
+    call.scales[0] = scales0;
+    call.zeros[0] = zeros0;
+    call.Bq[1] = Bq1;
+    call.scales[1] = scales1;
+    call.zeros[1] = zeros1;
+    call.epi = gq4::kEpiDual;
+    call.out[0] = C0;
+    call.out[1] = C1;
+    return GQ4_OK;
+}
+
+gq4_status build_gated_input(int M, int K, int N, int group_size, int kind, const float *X,
+                             const float *G, const uint32_t *Bq, const float *scales,
+                             const float *zeros, float *C, gq4::Call &call)
+{
+    GQ4_TRY(check_shape(M, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_activation(X, M, K, rs));
+    GQ4_TRY(check_activation(G, M, K, rs));
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    if (!C) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+
+    call = base_call(M, K, N, group_size, X);
+    call.gate_kind = kind;
+    call.G = G;
+    call.Bq[0] = Bq;
+    call.scales[0] = scales;
+    call.zeros[0] = zeros;
+    call.epi = gq4::kEpiStore;
+    call.out[0] = C;
+    return GQ4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -311,6 +364,35 @@ gq4_status gq4_norm_matvec(int M, int K, int N, int group_size, const gq4_norm *
 {
     gq4::Call call;
     GQ4_TRY(build_norm(M, K, N, group_size, norm, A, Bq, scales, zeros, C, call));
+    return run(call, stream);
+}
+
+gq4_status gq4_dual_matvec(int M, int K, int N, int group_size, const float *A,
+                           const uint32_t *Bq0, const float *scales0, const float *zeros0,
+                           const uint32_t *Bq1, const float *scales1, const float *zeros1,
+                           float *C0, float *C1, cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_dual(M, K, N, group_size, A, Bq0, scales0, zeros0, Bq1, scales1, zeros1, C0, C1,
+                       call));
+    return run(call, stream);
+}
+
+gq4_status gq4_sigmoid_gated_matvec(int M, int K, int N, int group_size, const float *X,
+                                    const float *G, const uint32_t *Bq, const float *scales,
+                                    const float *zeros, float *C, cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_gated_input(M, K, N, group_size, gq4::kGateSigmoid, X, G, Bq, scales, zeros, C, call));
+    return run(call, stream);
+}
+
+gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, const float *X,
+                                   const float *G, const uint32_t *Bq, const float *scales,
+                                   const float *zeros, float *C, cudaStream_t stream)
+{
+    gq4::Call call;
+    GQ4_TRY(build_gated_input(M, K, N, group_size, gq4::kGateSwiglu, X, G, Bq, scales, zeros, C, call));
     return run(call, stream);
 }
 

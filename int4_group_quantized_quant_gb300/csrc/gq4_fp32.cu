@@ -3,8 +3,9 @@
 // gate/up, for 1 <= M <= 32 decode lanes.
 //
 // Operation (gerbil moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4 and
-// WGSL_NORM_MATVEC_INT4): C[m][n] = sum_k a[m][k] * (q(n,k) - z) * s, with
-// the code layout and dequant rule described in gq4.h.
+// WGSL_NORM_MATVEC_INT4; the DualMatVecInt4, GatedMatVecInt4 and
+// SwiGLUGatedMatVecInt4 fusion docs): C[m][n] = sum_k a[m][k] * (q(n,k) - z)
+// * s, with the code layout and dequant rule described in gq4.h.
 //
 // Work decomposition (GB300-first; the WGSL 16 x 16 workgroup is not kept):
 //   * CTA = 8 warps.  grid.x walks lane blocks of MB lanes (fastest, so the
@@ -85,12 +86,23 @@ __device__ __forceinline__ float4 prescale(float4 v)
     return v;
 }
 
+// One element of a gated input: x * sigmoid(g) or silu(g) * x (the same
+// formulas as the one-lane kernel's prologue).
+template <int PRO>
+__device__ __forceinline__ float gate_input(float x, float g)
+{
+    if constexpr (PRO == kProSigmoid)
+        return x / (1.0f + expf(-g));
+    else
+        return g / (1.0f + expf(-g)) * x;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
     return g / (1.0f + expf(-g)) * u;
 }
 
-template <int MB, int NMAT, bool NORM, int EPI>
+template <int MB, int NMAT, int PRO, int EPI>
 __global__ void __launch_bounds__(kThreads)
 fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
 {
@@ -113,6 +125,7 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
     float sq[MB];
 #pragma unroll
     for (int m = 0; m < MB; ++m) sq[m] = 0.0f;
+    constexpr bool NORM = PRO == kProNorm;
     const bool write_norm_outputs = NORM && blockIdx.y == 0;
 
     // Column tiles blockIdx.y, + gridDim.y, ...  With a single K tile the
@@ -176,6 +189,13 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
                         sq[m] = fmaf(v.w, v.w, sq[m]);
                         const float4 g = *reinterpret_cast<const float4 *>(p.W_norm + k);
                         v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
+                    } else if constexpr (PRO != kProNone) {
+                        // the gated input: x * sigmoid(g), or silu(g) * x
+                        const float4 g = *reinterpret_cast<const float4 *>(p.A_b + row + k);
+                        v.x = gate_input<PRO>(v.x, g.x);
+                        v.y = gate_input<PRO>(v.y, g.y);
+                        v.z = gate_input<PRO>(v.z, g.z);
+                        v.w = gate_input<PRO>(v.w, g.w);
                     }
                 }
                 s_act[((size_t)m * p.kct + c) * 8 + (j ^ (c & 7))] = prescale(v);
@@ -327,6 +347,12 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
         const size_t mm = (size_t)(m0 + m);
         if constexpr (EPI == kEpiGated) {
             if (valid[0]) p.out[0][mm * p.N + col[0]] = silu_mul(acc[m][0], acc[m][1]);
+        } else if constexpr (EPI == kEpiDual) {
+            // stream 0: the column of matrix 0, stream 1: the same column of matrix 1
+            if (valid[0]) {
+                p.out[0][mm * p.N + col[0]] = acc[m][0];
+                p.out[1][mm * p.N + col[0]] = acc[m][1];
+            }
         } else {
 #pragma unroll
             for (int s = 0; s < kStreams; ++s) {
@@ -346,10 +372,10 @@ fp32_matvec_kernel(const __grid_constant__ Fp32Params p)
     }  // column tiles
 }
 
-template <int MB, int NMAT, bool NORM, int EPI>
+template <int MB, int NMAT, int PRO, int EPI>
 cudaError_t launch_variant(Fp32Params prm, cudaStream_t stream)
 {
-    auto kern = fp32_matvec_kernel<MB, NMAT, NORM, EPI>;
+    auto kern = fp32_matvec_kernel<MB, NMAT, PRO, EPI>;
     const int lane_blocks = (prm.M + MB - 1) / MB;
     const int cols_per_cta = kWarps * (kStreams / NMAT);
     prm.col_tiles = (prm.N + cols_per_cta - 1) / cols_per_cta;
@@ -388,16 +414,25 @@ cudaError_t launch_variant(Fp32Params prm, cudaStream_t stream)
 template <int MB>
 cudaError_t dispatch_mb(const Call &call, const Fp32Params &prm, cudaStream_t stream)
 {
-    const bool norm = call.norm != nullptr;
+    const int pro = prologue_of(call);
     switch (call.epi) {
     case kEpiStore:
-        return norm ? launch_variant<MB, 1, true, kEpiStore>(prm, stream)
-                    : launch_variant<MB, 1, false, kEpiStore>(prm, stream);
+        switch (pro) {
+        case kProNorm: return launch_variant<MB, 1, kProNorm, kEpiStore>(prm, stream);
+        case kProSigmoid: return launch_variant<MB, 1, kProSigmoid, kEpiStore>(prm, stream);
+        case kProSwiglu: return launch_variant<MB, 1, kProSwiglu, kEpiStore>(prm, stream);
+        default: return launch_variant<MB, 1, kProNone, kEpiStore>(prm, stream);
+        }
     case kEpiQuad:
-        return launch_variant<MB, 1, false, kEpiQuad>(prm, stream);
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_variant<MB, 1, kProNone, kEpiQuad>(prm, stream);
     case kEpiGated:
-        return norm ? launch_variant<MB, 2, true, kEpiGated>(prm, stream)
-                    : launch_variant<MB, 2, false, kEpiGated>(prm, stream);
+        if (pro == kProNorm) return launch_variant<MB, 2, kProNorm, kEpiGated>(prm, stream);
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_variant<MB, 2, kProNone, kEpiGated>(prm, stream);
+    case kEpiDual:
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_variant<MB, 2, kProNone, kEpiDual>(prm, stream);
     default:
         return cudaErrorInvalidValue;
     }
@@ -424,6 +459,8 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream)
         prm.eps = call.norm->eps;
         prm.residual_out = call.norm->residual_out;
         prm.norm_out = call.norm->norm_out;
+    } else if (call.gate_kind != kGateNone) {
+        prm.A_b = call.G;  // the gate vector
     }
     for (int i = 0; i < 2; ++i) {
         const int src = i < call.nmat ? i : 0;

@@ -14,13 +14,32 @@ enum Epilogue : int {
     kEpiStore = 0,  // C[m][col]
     kEpiQuad = 1,   // route col to out0..out3 at the split points
     kEpiGated = 2,  // out[m][col] = silu(gate) * up
+    kEpiDual = 3,   // two matrices, one input: out0[m][col], out1[m][col]
 };
 
-// One validated call, as the launchers see it.
+// How the activation vector is built (kernel template parameter).
+enum Prologue : int {
+    kProNone = 0,     // a = A
+    kProNorm = 1,     // a = RMSNorm(A + A_b) * W_norm
+    kProSigmoid = 2,  // a = A * sigmoid(G)
+    kProSwiglu = 3,   // a = silu(G) * A
+};
+
+// Gated-input kinds of a call (Call::gate_kind).
+enum GateKind : int {
+    kGateNone = 0,
+    kGateSigmoid = 1,
+    kGateSwiglu = 2,
+};
+
+// One validated call, as the launchers see it.  At most one of norm and
+// gate_kind is set.
 struct Call {
     int M, K, N, gs;
     const float *A;
-    const gq4_norm *norm;  // NULL: no prologue
+    const gq4_norm *norm;  // NULL: no norm prologue
+    int gate_kind;         // GateKind: the input is A gated by G
+    const float *G;        // [M][K] gate vector of a gated input
     int nmat;              // 1, or 2 for gate/up
     const uint32_t *Bq[2];
     const float *scales[2];
@@ -30,6 +49,14 @@ struct Call {
     int seg_start[4];
     int seg_len[4];
 };
+
+inline int prologue_of(const Call &c)
+{
+    return c.norm ? kProNorm
+         : c.gate_kind == kGateSigmoid ? kProSigmoid
+         : c.gate_kind == kGateSwiglu ? kProSwiglu
+         : kProNone;
+}
 
 // CUDA-core fp32 path (any M <= GQ4_MAX_LANES).
 cudaError_t launch_fp32(const Call &call, cudaStream_t stream);

@@ -10,13 +10,15 @@
 // 16-byte aligned f32 vectors, read as float4.
 //
 // Operation (gerbil moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4 main loop and
-// WGSL_NORM_MATVEC_INT4 prologue): C[n] = sum_k a[k] * (q(n,k) - z) * s with,
+// WGSL_NORM_MATVEC_INT4 prologue; the GatedMatVecInt4 and SwiGLUGatedMatVecInt4
+// fusion docs for the gated inputs): C[n] = sum_k a[k] * (q(n,k) - z) * s with,
 // for the norm form, a = RMSNorm(A + A_b) * W_norm.
 #pragma once
 
 #include <cstdint>
 
 #include "gq4_device.cuh"
+#include "gq4_internal.h"
 
 namespace gq4 {
 
@@ -66,19 +68,34 @@ __device__ __forceinline__ void pair_and_store(float4 x, int v, int K4, int lane
     }
 }
 
+// One element of a gated input: x * sigmoid(g) (kProSigmoid) or silu(g) * x
+// (kProSwiglu), with sigmoid(g) = 1 / (1 + e^-g) and silu(g) = g sigmoid(g).
+template <int PRO>
+__device__ __forceinline__ float gate_input(float x, float g)
+{
+    if constexpr (PRO == kProSigmoid)
+        return x / (1.0f + expf(-g));
+    else
+        return g / (1.0f + expf(-g)) * x;
+}
+
 // Stages one call's activations (K a multiple of 32; K/32 even when R = 2)
 // and the chunk groups' activation sums.  NT consumer threads (ctid < NT)
-// take part; named barrier `bar_id` synchronises them.  NORM: x = A + A_b
-// (A_b may be null), then a = x / sqrt(mean(x^2) + eps) * W_norm; when
-// `side_outputs`, x is written to residual_out and a to norm_out (either may
-// be null).  s_norm holds NT/32 floats.
+// take part; named barrier `bar_id` synchronises them.  PRO (Prologue):
+//   kProNone     a = A;
+//   kProNorm     x = A + A_b (A_b may be null), a = x / sqrt(mean(x^2) + eps)
+//                * W_norm; when `side_outputs`, x is written to residual_out
+//                and a to norm_out (either may be null);
+//   kProSigmoid  a = A * sigmoid(A_b)   (A_b is the gate vector);
+//   kProSwiglu   a = silu(A_b) * A      (A_b is the gate vector).
+// s_norm holds NT/32 floats.
 //
 // Consecutive lanes own consecutive float4 of the vector (coalesced loads),
 // up to NV per thread per batch, all issued before any use: for K <= 4*NV*NT
 // the whole prologue pays one round trip to L2 (the norm gain included).
-// Longer vectors take several batches; with NORM, x then waits in shared
+// Longer vectors take several batches; with the norm, x then waits in shared
 // memory for the inverse RMS.
-template <int R, bool NORM, int NT, int NV, class Ld>
+template <int R, int PRO, int NT, int NV, class Ld>
 __device__ __forceinline__ void stage_activations(int K, const float *A, const float *A_b,
                                                   const float *W_norm, float eps, float *residual_out,
                                                   float *norm_out, bool side_outputs, float4 *s_act,
@@ -90,7 +107,7 @@ __device__ __forceinline__ void stage_activations(int K, const float *A, const f
     const int lane = ctid & 31;
     const float4 *A4 = reinterpret_cast<const float4 *>(A);
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if constexpr (NORM) {
+    if constexpr (PRO == kProNorm) {
         const float4 *B4 = reinterpret_cast<const float4 *>(A_b);
         const float4 *W4 = reinterpret_cast<const float4 *>(W_norm);
         const bool one_batch = K4 <= kBatch;
@@ -154,12 +171,25 @@ __device__ __forceinline__ void stage_activations(int K, const float *A, const f
             }
         }
     } else {
+        const float4 *G4 = reinterpret_cast<const float4 *>(A_b);
         for (int b0 = 0; b0 < K4; b0 += kBatch) {
             float4 x[NV];
+            float4 g[PRO == kProNone ? 1 : NV];
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 const int v = b0 + ctid + i * NT;
                 x[i] = v < K4 ? Ld::ld(A4 + v) : z4;
+                if constexpr (PRO != kProNone) g[i] = v < K4 ? Ld::ld(G4 + v) : z4;
+            }
+            if constexpr (PRO != kProNone) {
+                // the gated input: x * sigmoid(g), or silu(g) * x
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    x[i].x = gate_input<PRO>(x[i].x, g[i].x);
+                    x[i].y = gate_input<PRO>(x[i].y, g[i].y);
+                    x[i].z = gate_input<PRO>(x[i].z, g[i].z);
+                    x[i].w = gate_input<PRO>(x[i].w, g[i].w);
+                }
             }
 #pragma unroll
             for (int i = 0; i < NV; ++i) {

@@ -207,7 +207,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
 
     // ---- prologue: activations (through L2: earlier calls may have written
     // them) ----
-    stage_activations<R, NORM, kCT, kActBatch, LoadL2>(c.K, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
+    stage_activations<R, NORM ? kProNorm : kProNone, kCT, kActBatch, LoadL2>(c.K, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
                                                        c.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm,
                                                        ctid, 1);
     if (first_call && ctid == 0) mbar_arrive(sh.ready);

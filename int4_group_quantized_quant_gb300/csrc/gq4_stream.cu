@@ -3,7 +3,9 @@
 // prologue and SiLU-gated gate/up.
 //
 // Operation (gerbil moonshine-stt bundle, WGSL_QUAD_MATVEC_INT4 and
-// WGSL_NORM_MATVEC_INT4): C[n] = sum_k a[k] * (q(n,k) - z) * s.
+// WGSL_NORM_MATVEC_INT4; the DualMatVecInt4, GatedMatVecInt4 and
+// SwiGLUGatedMatVecInt4 fusion docs): C[n] = sum_k a[k] * (q(n,k) - z) * s,
+// a built by the call's prologue; two matrices for gate/up or dual.
 //
 // Decomposition.  At M = 1 the path is one streaming pass over the weights,
 // so the kernel is organised around moving bytes:
@@ -114,7 +116,7 @@ __device__ __forceinline__ void record_error(unsigned int bits)
 // R: consecutive 32-code chunks per chunk group (R = 2 only when a scale
 // group holds at least 64 codes, so both chunks share one scale and zero).
 // SPW: weight streams per warp per slot (columns, or gate and up columns).
-template <int NMAT, bool NORM, int EPI, int R, int SPW>
+template <int NMAT, int PRO, int EPI, int R, int SPW>
 __global__ void __launch_bounds__(kThreads, 1)
 stream_matvec_kernel(const __grid_constant__ StreamParams p)
 {
@@ -238,7 +240,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // grid to complete (its writes visible).  The producer does not wait: the
     // weights do not depend on it, so they stream in meanwhile.
     grid_dependency_wait();
-    stage_activations<R, NORM, kCT, kActBatch, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, p.eps,
+    stage_activations<R, PRO, kCT, kActBatch, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, p.eps,
                                                              p.residual_out, p.norm_out, blockIdx.x == 0,
                                                              s_act, s_asum, s_norm, ctid, 1);
     named_barrier(2, kThreads);  // the producer has initialised the mbarriers
@@ -369,6 +371,13 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
                     p.out[0][c0 + lc] = gv / (1.0f + expf(-gv)) * u;
                 }
             }
+        } else if constexpr (EPI == kEpiDual) {
+            // streams 0 .. CPS-1 are columns of matrix 0, CPS .. 2*CPS-1 of matrix 1
+            if ((lane % kLaneStride) == 0) {
+                const int mat = q_of_lane / CPS;
+                const int lc = q_of_lane - mat * CPS;
+                if (lc < nc) p.out[mat][c0 + lc] = total;
+            }
         } else {
             if ((lane % kLaneStride) == 0) {
                 const int lc = q_of_lane;
@@ -402,10 +411,10 @@ uint32_t round_up(uint32_t x, uint32_t a)
     return (x + a - 1) / a * a;
 }
 
-template <int NMAT, bool NORM, int EPI, int R, int SPW>
+template <int NMAT, int PRO, int EPI, int R, int SPW>
 cudaError_t launch_stream_variant(const StreamParams &prm, size_t smem, cudaStream_t stream)
 {
-    auto kern = stream_matvec_kernel<NMAT, NORM, EPI, R, SPW>;
+    auto kern = stream_matvec_kernel<NMAT, PRO, EPI, R, SPW>;
     int dev = 0, sms = 0;
     cudaError_t err;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -445,14 +454,14 @@ cudaError_t launch_stream_variant(const StreamParams &prm, size_t smem, cudaStre
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <int NMAT, bool NORM, int EPI>
+template <int NMAT, int PRO, int EPI>
 cudaError_t launch_stream_rs(const StreamParams &prm, int R, int spw, size_t smem, cudaStream_t stream)
 {
     if (R == 2)
-        return spw == 4 ? launch_stream_variant<NMAT, NORM, EPI, 2, 4>(prm, smem, stream)
-                        : launch_stream_variant<NMAT, NORM, EPI, 2, 2>(prm, smem, stream);
-    return spw == 4 ? launch_stream_variant<NMAT, NORM, EPI, 1, 4>(prm, smem, stream)
-                    : launch_stream_variant<NMAT, NORM, EPI, 1, 2>(prm, smem, stream);
+        return spw == 4 ? launch_stream_variant<NMAT, PRO, EPI, 2, 4>(prm, smem, stream)
+                        : launch_stream_variant<NMAT, PRO, EPI, 2, 2>(prm, smem, stream);
+    return spw == 4 ? launch_stream_variant<NMAT, PRO, EPI, 1, 4>(prm, smem, stream)
+                    : launch_stream_variant<NMAT, PRO, EPI, 1, 2>(prm, smem, stream);
 }
 
 // Ring geometry for a call; false when the call does not fit this path.
@@ -562,6 +571,8 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream)
         prm.eps = call.norm->eps;
         prm.residual_out = call.norm->residual_out;
         prm.norm_out = call.norm->norm_out;
+    } else if (call.gate_kind != kGateNone) {
+        prm.A_b = call.G;  // the gate vector
     }
     for (int m = 0; m < 2; ++m) {
         const int src = m < call.nmat ? m : 0;
@@ -574,16 +585,25 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream)
         prm.seg_start[i] = call.seg_start[i];
         prm.seg_len[i] = call.seg_len[i];
     }
-    const bool norm = call.norm != nullptr;
+    const int pro = prologue_of(call);
     switch (call.epi) {
     case kEpiStore:
-        return norm ? launch_stream_rs<1, true, kEpiStore>(prm, R, spw, smem, stream)
-                    : launch_stream_rs<1, false, kEpiStore>(prm, R, spw, smem, stream);
+        switch (pro) {
+        case kProNorm: return launch_stream_rs<1, kProNorm, kEpiStore>(prm, R, spw, smem, stream);
+        case kProSigmoid: return launch_stream_rs<1, kProSigmoid, kEpiStore>(prm, R, spw, smem, stream);
+        case kProSwiglu: return launch_stream_rs<1, kProSwiglu, kEpiStore>(prm, R, spw, smem, stream);
+        default: return launch_stream_rs<1, kProNone, kEpiStore>(prm, R, spw, smem, stream);
+        }
     case kEpiQuad:
-        return launch_stream_rs<1, false, kEpiQuad>(prm, R, spw, smem, stream);
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_stream_rs<1, kProNone, kEpiQuad>(prm, R, spw, smem, stream);
     case kEpiGated:
-        return norm ? launch_stream_rs<2, true, kEpiGated>(prm, R, spw, smem, stream)
-                    : launch_stream_rs<2, false, kEpiGated>(prm, R, spw, smem, stream);
+        if (pro == kProNorm) return launch_stream_rs<2, kProNorm, kEpiGated>(prm, R, spw, smem, stream);
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_stream_rs<2, kProNone, kEpiGated>(prm, R, spw, smem, stream);
+    case kEpiDual:
+        if (pro != kProNone) return cudaErrorInvalidValue;
+        return launch_stream_rs<2, kProNone, kEpiDual>(prm, R, spw, smem, stream);
     default:
         return cudaErrorInvalidValue;
     }

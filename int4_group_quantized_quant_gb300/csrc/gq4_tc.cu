@@ -1146,6 +1146,8 @@ cudaError_t dispatch_tc(const Call &call, cudaStream_t stream)
 bool tc_path_supported(const Call &call)
 {
     if (call.M < 16 || call.M > 32) return false;
+    // gated inputs and the dual projection run on the CUDA-core kernels
+    if (call.gate_kind != kGateNone || call.epi == kEpiDual) return false;
     // scales and zeros are read by tensor-map copies of whole super-rows of
     // P = 4 / gcd(G, 4) rows (16-byte aligned bases, at least one super-row)
     const int P = 4 / gcd_int(call.K / call.gs, 4);

@@ -63,6 +63,9 @@ _SIGS = {
     "gq4_norm_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_gated_matvec": [_i, _i, _i, _i, _NormP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                          _vp],
+    "gq4_dual_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_sigmoid_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_swiglu_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
     "gq4_unpack": [_i, _i, _vp, _vp, _vp],
@@ -214,6 +217,49 @@ def gated_matvec(A, Bq_gate, scales_gate, zeros_gate, Bq_up, scales_up, zeros_up
                                 _ptr(Bq_up), _ptr(scales_up), _ptr(zeros_up), _ptr(out),
                                 _stream(stream)), "gq4_gated_matvec")
     return out
+
+
+def dual_matvec(A, Bq0, scales0, zeros0, Bq1, scales1, zeros1, group_size, C0=None, C1=None,
+                stream=None):
+    """(C0, C1) = (A . W0, A . W1): two projections sharing the input (gq4_dual_matvec)."""
+    M, K = _lanes(A)
+    N = _weights(Bq0, scales0, zeros0, K, group_size, "0")
+    if _weights(Bq1, scales1, zeros1, K, group_size, "1") != N:
+        raise ValueError("both matrices must have the same N")
+    if C0 is None:
+        C0 = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if C1 is None:
+        C1 = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _need(C0, "C0", _F32, (M, N))
+    _need(C1, "C1", _F32, (M, N))
+    _check(lib.gq4_dual_matvec(M, K, N, group_size, _ptr(A), _ptr(Bq0), _ptr(scales0),
+                               _ptr(zeros0), _ptr(Bq1), _ptr(scales1), _ptr(zeros1), _ptr(C0),
+                               _ptr(C1), _stream(stream)), "gq4_dual_matvec")
+    return C0, C1
+
+
+def _gated_input(fn, name, X, G, Bq, scales, zeros, group_size, C, stream):
+    M, K = _lanes(X)
+    _need(G, "G", _F32, (M, K))
+    N = _weights(Bq, scales, zeros, K, group_size)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _need(C, "C", _F32, (M, N))
+    _check(fn(M, K, N, group_size, _ptr(X), _ptr(G), _ptr(Bq), _ptr(scales), _ptr(zeros), _ptr(C),
+              _stream(stream)), name)
+    return C
+
+
+def sigmoid_gated_matvec(X, G, Bq, scales, zeros, group_size, C=None, stream=None):
+    """C = (X * sigmoid(G)) . W (gq4_sigmoid_gated_matvec)."""
+    return _gated_input(lib.gq4_sigmoid_gated_matvec, "gq4_sigmoid_gated_matvec", X, G, Bq, scales,
+                        zeros, group_size, C, stream)
+
+
+def swiglu_gated_matvec(X, G, Bq, scales, zeros, group_size, C=None, stream=None):
+    """C = (silu(G) * X) . W (gq4_swiglu_gated_matvec)."""
+    return _gated_input(lib.gq4_swiglu_gated_matvec, "gq4_swiglu_gated_matvec", X, G, Bq, scales,
+                        zeros, group_size, C, stream)
 
 
 # ---------------------------------------------------------------------------

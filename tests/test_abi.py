@@ -171,6 +171,27 @@ def test_gated_checks(gq4):
 
 
 @no_gpu_only
+def test_dual_and_gated_input_checks(gq4):
+    lib = gq4.lib
+    M, K, N, gs = 1, 1024, 64, 32
+    w0 = [addr(1), addr(2), addr(3)]
+    w1 = [addr(11), addr(12), addr(13)]
+    # the two outputs overlapping each other, or an output over the second matrix
+    assert lib.gq4_dual_matvec(M, K, N, gs, addr(0), *w0, *w1, addr(20), addr(20, 64), None) \
+        == gq4.ERR_ALIAS
+    assert lib.gq4_dual_matvec(M, K, N, gs, addr(0), *w0, *w1, addr(20), addr(12, 16), None) \
+        == gq4.ERR_ALIAS
+    assert lib.gq4_dual_matvec(M, K, N, gs, addr(0), *w0, *w1, addr(20), None, None) \
+        == gq4.ERR_INVALID_ARG
+    for fn in (lib.gq4_sigmoid_gated_matvec, lib.gq4_swiglu_gated_matvec):
+        # gate vector missing, misaligned, or overlapped by the output
+        assert fn(M, K, N, gs, addr(0), None, *w0, addr(20), None) == gq4.ERR_INVALID_ARG
+        assert fn(M, K, N, gs, addr(0), addr(5, 4), *w0, addr(20), None) == gq4.ERR_MISALIGNED
+        assert fn(M, K, N, gs, addr(0), addr(5), *w0, addr(5, 16), None) == gq4.ERR_ALIAS
+        assert fn(0, K, N, gs, addr(0), addr(5), *w0, addr(20), None) == gq4.ERR_INVALID_ARG
+
+
+@no_gpu_only
 def test_unpack_dequant_checks(gq4):
     lib = gq4.lib
     assert lib.gq4_unpack(100, 4, addr(0), addr(1), None) == gq4.ERR_INVALID_ARG   # K % 32
