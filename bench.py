@@ -560,6 +560,97 @@ def run_profile_case(args):
                       "launch_rounds": args.steps}))
 
 
+def run_extras(args):
+    """Time the dual projection and the gated-input matvecs (one lane, 7B-sized
+    4096 x 4096 matrices), each in a CUDA graph over rotating weight sets
+    larger than 4x L2, against the plain matvec; one JSON line per op."""
+    import torch
+    from int4_group_quantized_quant_gb300 import build as b
+    b.build()
+    from int4_group_quantized_quant_gb300 import gq4
+    from int4_group_quantized_quant_gb300 import inputs as I
+    torch.cuda.set_device(0)
+    K = N = 4096
+    gs = GS
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    mat_bytes = K * N // 2 + 8 * N * (K // gs)
+    R = max(8, -(-4 * l2 // mat_bytes))
+    mats = []
+    for r in range(R):
+        w = I.quant_weights(K, N, gs, 1600, r)
+        mats.append(tuple(torch.from_numpy(a).cuda() for a in (w.Bq, w.scales, w.zeros)))
+    X = torch.from_numpy(I.activations(1, K, 1600, 0)).cuda()
+    G = torch.from_numpy(I.activations(1, K, 1600, 1)).cuda()
+    C0 = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    C1 = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    peak, peak_src = hbm_peak()
+
+    def time_graph(body):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                body(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body(torch.cuda.current_stream())
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / args.steps
+
+    def dual(s):
+        for r in range(0, R - 1, 2):
+            gq4.dual_matvec(X, *mats[r], *mats[r + 1], gs, C0=C0, C1=C1, stream=s)
+
+    def two_matvecs(s):
+        for r in range(0, R - 1, 2):
+            gq4.matvec(X, *mats[r], gs, C=C0, stream=s)
+            gq4.matvec(X, *mats[r + 1], gs, C=C1, stream=s)
+
+    def plain(s):
+        for r in range(R):
+            gq4.matvec(X, *mats[r], gs, C=C0, stream=s)
+
+    def sigmoid(s):
+        for r in range(R):
+            gq4.sigmoid_gated_matvec(X, G, *mats[r], gs, C=C0, stream=s)
+
+    def swiglu(s):
+        for r in range(R):
+            gq4.swiglu_gated_matvec(X, G, *mats[r], gs, C=C0, stream=s)
+
+    pairs = R // 2
+    t_dual = time_graph(dual) / pairs
+    t_two = time_graph(two_matvecs) / pairs
+    t_plain = time_graph(plain) / R
+    t_sig = time_graph(sigmoid) / R
+    t_swi = time_graph(swiglu) / R
+    rows = [
+        ("dual 4096 -> 2 x 4096", t_dual, 2 * mat_bytes + 4 * K + 8 * N,
+         {"two_matvecs_us": round(t_two, 3)}),
+        ("sigmoid-gated input 4096 -> 4096", t_sig, mat_bytes + 8 * K + 4 * N,
+         {"plain_matvec_us": round(t_plain, 3)}),
+        ("swiglu-gated input 4096 -> 4096", t_swi, mat_bytes + 8 * K + 4 * N,
+         {"plain_matvec_us": round(t_plain, 3)}),
+    ]
+    for name, us, nbytes, extra in rows:
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"extra": name, "lanes": 1, "group_size": gs, "us_per_call": round(us, 3),
+                          "bytes_per_call": nbytes, "GB/s": round(gbs, 1),
+                          "frac_of_hbm_peak": round(gbs / peak, 4), "peak": peak,
+                          "peak_source": peak_src, "weight_sets": R,
+                          "timing": "CUDA graph over rotating weight sets > 4x L2, CUDA events",
+                          **extra}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,11 +664,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["gated", "down", "quad", "step"], default=None,
                     help="run a small launch sequence of one kernel for ncu (no timing)")
+    ap.add_argument("--extras", action="store_true",
+                    help="time the dual and gated-input matvecs (one JSON line each)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.profile is None:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     rank, world, local_rank = dist_env()
-    if args.profile:
+    if args.extras:
+        run_extras(args)
+    elif args.profile:
         run_profile_case(args)
     elif args.impl == "reference":
         run_reference(args, rank, world)

@@ -70,13 +70,15 @@ __device__ __forceinline__ void pair_and_store(float4 x, int v, int K4, int lane
 
 // One element of a gated input: x * sigmoid(g) (kProSigmoid) or silu(g) * x
 // (kProSwiglu), with sigmoid(g) = 1 / (1 + e^-g) and silu(g) = g sigmoid(g).
+// The fast exponential and divide intrinsics: a few ulp, far inside the
+// matvec's tolerance; a saturated gate (e^-g = inf) gives exactly 0.
 template <int PRO>
 __device__ __forceinline__ float gate_input(float x, float g)
 {
     if constexpr (PRO == kProSigmoid)
-        return x / (1.0f + expf(-g));
+        return __fdividef(x, 1.0f + __expf(-g));
     else
-        return g / (1.0f + expf(-g)) * x;
+        return __fdividef(g, 1.0f + __expf(-g)) * x;
 }
 
 // Stages one call's activations (K a multiple of 32; K/32 even when R = 2)
@@ -181,20 +183,17 @@ __device__ __forceinline__ void stage_activations(int K, const float *A, const f
                 x[i] = v < K4 ? Ld::ld(A4 + v) : z4;
                 if constexpr (PRO != kProNone) g[i] = v < K4 ? Ld::ld(G4 + v) : z4;
             }
-            if constexpr (PRO != kProNone) {
-                // the gated input: x * sigmoid(g), or silu(g) * x
 #pragma unroll
-                for (int i = 0; i < NV; ++i) {
+            for (int i = 0; i < NV; ++i) {
+                const int v = b0 + ctid + i * NT;
+                if (v - lane >= K4) break;  // warp-uniform: the rest of the batch is past the end
+                if constexpr (PRO != kProNone) {
+                    // the gated input: x * sigmoid(g), or silu(g) * x
                     x[i].x = gate_input<PRO>(x[i].x, g[i].x);
                     x[i].y = gate_input<PRO>(x[i].y, g[i].y);
                     x[i].z = gate_input<PRO>(x[i].z, g[i].z);
                     x[i].w = gate_input<PRO>(x[i].w, g[i].w);
                 }
-            }
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int v = b0 + ctid + i * NT;
-                if (v - lane >= K4) break;  // warp-uniform: the rest of the batch is past the end
                 pair_and_store<R>(x[i], v, K4, lane, s_act, s_asum);
             }
         }

@@ -90,3 +90,19 @@ def test_saturated_gate(gq4, M):
     C = host(gq4.swiglu_gated_matvec(dev(X), dev(G), *wdev(w), gs))
     check_close("silu(64)", C, 64.0 * ref, tol_fp32(64.0 * S))
     assert gq4.device_error() == 0
+
+
+@pytest.mark.parametrize("kind", ["sigmoid", "swiglu"])
+@pytest.mark.parametrize("M", [1, 4])
+def test_wide_gate(gq4, kind, M):
+    """Gates spread over +-100: e^-g overflows (the gate is exactly 0) or
+    vanishes (sigmoid 1, silu g) for many of them; against the oracle."""
+    K, N, gs = 4096, 257, 128
+    w = I.quant_weights(K, N, gs, 1503, M)
+    X = I.activations(M, K, 1503, M, 0)
+    G = (40.0 * I.activations(M, K, 1503, M, 1)).clip(-100.0, 100.0).astype(np.float32)
+    fn = gq4.sigmoid_gated_matvec if kind == "sigmoid" else gq4.swiglu_gated_matvec
+    C = host(fn(dev(X), dev(G), *wdev(w), gs))
+    ref, S, _ = oracle.gated_input_matvec(kind, X, G, w.Bq, w.scales, w.zeros, K, N, gs)
+    check_close(f"wide {kind} M={M}", C, ref, tol_fp32(S))
+    assert gq4.device_error() == 0
