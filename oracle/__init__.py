@@ -12,14 +12,17 @@ from .oracle import (  # noqa: F401
     dequant_f32,
     dequant_f64,
     dot_cols,
+    from_mlx,
     gated_input_matvec,
     gated_matvec,
     load,
     matvec,
+    mlx_dequant_f64,
     nibble,
     norm,
     norm_matvec,
     pack,
     quad_matvec,
+    quantize,
     unpack,
 )

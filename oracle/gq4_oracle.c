@@ -16,12 +16,25 @@
  *   gated       -- all-ones up matrix gives sum(a), zero gate gives 0, composition
  *   gated input -- sigmoid(0) halves, saturated gates pass or scale the input
  *                  exactly, silu(0) gives exactly 0
+ *   quantize    -- values on a 16-level grid come back exactly; every code is
+ *                  the nearest level (brute force over the 16); error within
+ *                  half a step; both ends of every group are used
+ *   MLX         -- a worked word with scale 1/2 and bias -4; conversion agrees
+ *                  with the page's dequant within rounding; degenerate groups
+ *                  reproduce the bias exactly
  */
 #include "gq4_oracle.h"
 
+#include <float.h>
 #include <math.h>
 #include <stddef.h>
 #include <stdlib.h>
+
+/* The quantizer decides integer codes in binary32: float expressions must be
+ * evaluated in float, one rounding per operation. */
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the oracle needs FLT_EVAL_METHOD == 0"
+#endif
 
 static int shape_ok(int M, int K, int N, int gs)
 {
@@ -339,5 +352,102 @@ int gq4o_gated_input_matvec(int M, int K, int N, int gs, int kind, const float *
         }
     }
     if (a != a_out) free(a);
+    return 0;
+}
+
+/* ---- Quantizer and MLX conversion --------------------------------------- */
+
+int gq4o_quantize(int K, int N, int gs, const float *W, uint32_t *Bq,
+                  float *scales, float *zeros, int *bad_groups)
+{
+    if (!shape_ok(1, K, N, gs) || !W || !Bq || !scales || !zeros) return -1;
+    const int G = K / gs;
+    int bad_count = 0;
+    for (size_t i = 0; i < (size_t)N * (size_t)(K / 8); ++i) Bq[i] = 0u;
+    for (int n = 0; n < N; ++n) {
+        for (int g = 0; g < G; ++g) {
+            const float *v = W + (size_t)n * K + (size_t)g * gs;
+            const size_t gi = (size_t)n * G + g;
+            int bad = 0;
+            for (int i = 0; i < gs; ++i)
+                if (!isfinite(v[i])) bad = 1;
+            volatile float lo = 0.0f, hi = 0.0f, d = 0.0f;
+            if (!bad) {
+                lo = v[0];
+                hi = v[0];
+                for (int i = 1; i < gs; ++i) {
+                    if (v[i] < lo) lo = v[i];
+                    if (v[i] > hi) hi = v[i];
+                }
+                lo = lo + 0.0f;  /* -0 becomes +0 */
+                hi = hi + 0.0f;
+                d = hi - lo;
+                if (!isfinite(d)) bad = 1;
+            }
+            if (bad) {
+                /* codes stay 0 */
+                scales[gi] = NAN;
+                zeros[gi] = NAN;
+                ++bad_count;
+                continue;
+            }
+            volatile float s = d / 15.0f;
+            if (s < FLT_MIN) s = 1.0f;
+            volatile float r = 1.0f / s;
+            volatile float z = -lo / s;
+            for (int i = 0; i < gs; ++i) {
+                volatile float diff = v[i] - lo;
+                volatile float t = diff * r;
+                float qf = rintf(t);
+                if (qf < 0.0f) qf = 0.0f;
+                if (qf > 15.0f) qf = 15.0f;
+                const int k = g * gs + i;
+                Bq[(size_t)n * (K / 8) + k / 8] |= (uint32_t)qf << (4 * (k % 8));
+            }
+            scales[gi] = s;
+            zeros[gi] = z;
+        }
+    }
+    if (bad_groups) *bad_groups = bad_count;
+    return 0;
+}
+
+int gq4o_mlx_dequant_f64(int K, int N, int gs, const uint32_t *packed,
+                         const float *mlx_scales, const float *mlx_biases,
+                         double *W)
+{
+    if (!shape_ok(1, K, N, gs) || !packed || !mlx_scales || !mlx_biases || !W) return -1;
+    for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < K; ++k) {
+            const size_t g = group_index(K, gs, n, k);
+            const double q = (double)gq4o_nibble(packed, K, n, k);
+            W[(size_t)n * K + k] = (double)mlx_scales[g] * q + (double)mlx_biases[g];
+        }
+    }
+    return 0;
+}
+
+int gq4o_from_mlx(int K, int N, int gs, const uint32_t *packed,
+                  const float *mlx_scales, const float *mlx_biases,
+                  uint32_t *Bq, float *scales, float *zeros)
+{
+    if (!shape_ok(1, K, N, gs) || !packed || !mlx_scales || !mlx_biases) return -1;
+    if (!Bq || !scales || !zeros) return -1;
+    const int G = K / gs;
+    for (size_t i = 0; i < (size_t)N * (size_t)(K / 8); ++i) Bq[i] = packed[i];
+    for (size_t gi = 0; gi < (size_t)N * (size_t)G; ++gi) {
+        const float s = mlx_scales[gi], b = mlx_biases[gi];
+        volatile float z = -b / s;
+        if (s == 0.0f || (isinf(z) && isfinite(b))) {
+            /* w = b for every code: codes 1, scale b, zero 0 */
+            const size_t w0 = gi * (size_t)(gs / 8);
+            for (int j = 0; j < gs / 8; ++j) Bq[w0 + j] = 0x11111111u;
+            scales[gi] = b;
+            zeros[gi] = 0.0f;
+        } else {
+            scales[gi] = s;
+            zeros[gi] = z;
+        }
+    }
     return 0;
 }

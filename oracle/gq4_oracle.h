@@ -126,6 +126,45 @@ int gq4o_gated_input_matvec(int M, int K, int N, int gs, int kind, const float *
                             const float *G, const uint32_t *Bq, const float *scales,
                             const float *zeros, double *C, double *S, double *a_out);
 
+/* ---- The step before the path: producing the format ----------------------
+ *
+ * Group-wise int4 quantizer (the backbone's weight-only INT4 of the gpu
+ * bundle's loader, quantizeInt4 / quantizeBackboneInt4, whose body the pages
+ * do not show).  Reading: per group of gs consecutive inputs of a column, a
+ * min/max asymmetric affine map onto the 16 codes with a float zero point,
+ * every step one binary32 operation (the precision in which the codes are
+ * decided):
+ *   lo = min v, hi = max v             (+0.0 added: no negative zero)
+ *   s  = fl(fl(hi - lo) / 15)          s < FLT_MIN (a range below 15 normal
+ *                                      steps, e.g. a constant group): s = 1
+ *   z  = fl(-lo / s)
+ *   q  = clamp(rint(fl(fl(v - lo) * fl(1 / s))), 0, 15)   (ties to even)
+ * so that (q - z) * s is the nearest of the 16 levels lo + j*s.  A group with
+ * a non-finite value, or whose range hi - lo overflows, gets codes 0 and a
+ * NaN scale and zero.  W is f32 [N][K] (column n's K weights contiguous:
+ * W[n][k] multiplies input k for output n).  *bad_groups (nullable) receives
+ * the number of such groups. */
+int gq4o_quantize(int K, int N, int gs, const float *W, uint32_t *Bq,
+                  float *scales, float *zeros, int *bad_groups);
+
+/* MLX affine int4 (gpu bundle 1.0.0, dequantizeMLXProjection): the same
+ * words (8 codes per u32, low nibble first, rows = output columns, groups of
+ * gs along the row) with w = scale * q + bias.  Dequantized in double:
+ * W[n][k] = (double)scale * q + (double)bias.  W is [N][K]. */
+int gq4o_mlx_dequant_f64(int K, int N, int gs, const uint32_t *packed,
+                         const float *mlx_scales, const float *mlx_biases,
+                         double *W);
+
+/* MLX (scale, bias) to this format's (scale, zero): zero = fl(-bias / scale)
+ * in binary32, codes unchanged, so (q - zero) * scale = scale * q + bias.
+ * A group that has no such zero (scale 0, or -bias/scale overflowing while
+ * bias is finite; then w = bias for every code, to within bias's own
+ * rounding) is rewritten exactly: all its codes 1, scale = bias, zero = 0.
+ * Bq may be packed (in place). */
+int gq4o_from_mlx(int K, int N, int gs, const uint32_t *packed,
+                  const float *mlx_scales, const float *mlx_biases,
+                  uint32_t *Bq, float *scales, float *zeros);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,10 @@ def load_library(path: str):
                                     _f64p, _f32p, _f64p]),
         "gq4o_gated_input_matvec": (_int, [_int, _int, _int, _int, _int, _f32p, _f32p,
                                            _u32p, _f32p, _f32p, _f64p, _f64p, _f64p]),
+        "gq4o_quantize": (_int, [_int, _int, _int, _f32p, _u32p, _f32p, _f32p, _i32p]),
+        "gq4o_mlx_dequant_f64": (_int, [_int, _int, _int, _u32p, _f32p, _f32p, _f64p]),
+        "gq4o_from_mlx": (_int, [_int, _int, _int, _u32p, _f32p, _f32p, _u32p, _f32p,
+                                 _f32p]),
         "gq4o_gated_matvec": (_int, [_int, _int, _int, _int, _f32p, _f32p, _f32p,
                                      ctypes.c_float, _u32p, _f32p, _f32p, _u32p,
                                      _f32p, _f32p, _f64p, _f64p, _f64p, _f64p,
@@ -255,6 +259,39 @@ class Oracle:
                "gated_input_matvec")
         return C, S, a
 
+    def quantize(self, W, gs):
+        """(Bq [N, K/8], scales [N, G], zeros [N, G], bad_groups) for W f32 [N, K]."""
+        W = _c(W, np.float32)
+        N, K = W.shape
+        Bq = np.empty((N, K // 8), np.uint32)
+        s = np.empty((N, K // gs), np.float32)
+        z = np.empty((N, K // gs), np.float32)
+        bad = ctypes.c_int(0)
+        _check(self.lib.gq4o_quantize(K, N, gs, _ptr(W, _f32p), _ptr(Bq, _u32p), _ptr(s, _f32p),
+                                      _ptr(z, _f32p), ctypes.byref(bad)), "quantize")
+        return Bq, s, z, bad.value
+
+    def mlx_dequant_f64(self, packed, mlx_scales, mlx_biases, K, N, gs):
+        """W [N, K] (double) = scale * q + bias of an MLX affine int4 matrix."""
+        packed = _c(packed, np.uint32)
+        ms, mb = _c(mlx_scales, np.float32), _c(mlx_biases, np.float32)
+        W = np.empty((N, K), np.float64)
+        _check(self.lib.gq4o_mlx_dequant_f64(K, N, gs, _ptr(packed, _u32p), _ptr(ms, _f32p),
+                                             _ptr(mb, _f32p), _ptr(W, _f64p)), "mlx_dequant_f64")
+        return W
+
+    def from_mlx(self, packed, mlx_scales, mlx_biases, K, N, gs):
+        """(Bq, scales, zeros) of this format for an MLX affine int4 matrix."""
+        packed = _c(packed, np.uint32)
+        ms, mb = _c(mlx_scales, np.float32), _c(mlx_biases, np.float32)
+        Bq = np.empty((N, K // 8), np.uint32)
+        s = np.empty((N, K // gs), np.float32)
+        z = np.empty((N, K // gs), np.float32)
+        _check(self.lib.gq4o_from_mlx(K, N, gs, _ptr(packed, _u32p), _ptr(ms, _f32p),
+                                      _ptr(mb, _f32p), _ptr(Bq, _u32p), _ptr(s, _f32p),
+                                      _ptr(z, _f32p)), "from_mlx")
+        return Bq, s, z
+
 
 def _default(name):
     def call(*args, **kwargs):
@@ -276,3 +313,6 @@ norm = _default("norm")
 norm_matvec = _default("norm_matvec")
 gated_matvec = _default("gated_matvec")
 gated_input_matvec = _default("gated_input_matvec")
+quantize = _default("quantize")
+mlx_dequant_f64 = _default("mlx_dequant_f64")
+from_mlx = _default("from_mlx")

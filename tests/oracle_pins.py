@@ -409,6 +409,166 @@ def pin_gated_input_values(orc):
         assert math.isclose(C[0, 0], g * sig * x, rel_tol=1e-15), (x, g, C[0, 0])
 
 
+# ---------------------------------------------------------------------------
+# Quantizer and MLX conversion
+# ---------------------------------------------------------------------------
+
+_U = 2.0 ** -24  # unit roundoff of binary32
+
+
+def _group_view(x, gs):
+    N, K = x.shape
+    return x.reshape(N, K // gs, gs)
+
+
+def pin_quantize_grid(orc):
+    """Values on a 16-level grid lo + j*s (power-of-two s, lo a multiple of s,
+    both ends in every group) come back exactly: codes j, scale s, zero -lo/s,
+    and the dequantized values.  A group size of 96 (12 words) included."""
+    r = _rng(30)
+    N, K, gs = 5, 384, 96
+    G = K // gs
+    codes = r.integers(0, 16, size=(N, K)).astype(np.uint8)
+    for g in range(G):
+        codes[:, g * gs + 3] = 0
+        codes[:, g * gs + 50] = 15
+    s = 2.0 ** r.integers(-8, 3, size=(N, G))
+    j = r.integers(-20, 6, size=(N, G))
+    W = (j * s)[:, :, None] + _group_view(codes, gs) * s[:, :, None]
+    W = W.reshape(N, K).astype(np.float32)
+    Bq, sc, z, bad = orc.quantize(W, gs)
+    assert bad == 0
+    assert np.array_equal(byte_view_codes(Bq, K, N), codes)
+    assert np.array_equal(sc, s.astype(np.float32))
+    assert np.array_equal(z, (-j).astype(np.float32))
+    assert np.array_equal(orc.dequant_f64(Bq, sc, z, K, N, gs), W.astype(np.float64))
+
+
+def pin_quantize_nearest(orc):
+    """Random groups: every code is the nearest of its group's 16 levels
+    (q - z) * s (brute force over the 16, in double), the error is at most
+    half a step, codes 0 and 15 both occur, and the levels of codes 0 and 15
+    are the group's min and max to within rounding."""
+    r = _rng(31)
+    N, K, gs = 7, 512, 128
+    W = (r.normal(0.0, 0.02, size=(N, K)) + r.normal(0.0, 0.01, size=(N, 1))).astype(np.float32)
+    Bq, s, z, bad = orc.quantize(W, gs)
+    assert bad == 0
+    codes = byte_view_codes(Bq, K, N).astype(np.int64)
+    sd = np.repeat(s.astype(np.float64), gs, axis=1)
+    zd = np.repeat(z.astype(np.float64), gs, axis=1)
+    levels = (np.arange(16)[None, None, :] - zd[:, :, None]) * sd[:, :, None]
+    err = np.abs(W.astype(np.float64)[:, :, None] - levels)
+    mine = np.take_along_axis(err, codes[:, :, None], axis=2)[:, :, 0]
+    assert np.all(mine <= err.min(axis=2) + 1e-5 * sd)
+    assert np.all(mine <= 0.5 * sd * (1.0 + 1e-5))
+    cg = _group_view(codes, gs)
+    assert np.all(cg.min(axis=2) == 0) and np.all(cg.max(axis=2) == 15)
+    Wg = _group_view(W.astype(np.float64), gs)
+    lo, hi = Wg.min(axis=2), Wg.max(axis=2)
+    s64, z64 = s.astype(np.float64), z.astype(np.float64)
+    tol = 4 * _U * (np.abs(lo) + np.abs(hi))
+    assert np.all(np.abs((0.0 - z64) * s64 - lo) <= tol)
+    assert np.all(np.abs((15.0 - z64) * s64 - hi) <= tol)
+
+
+def pin_quantize_special_groups(orc):
+    """A constant group dequantizes to exactly its value (scale 1), an all-zero
+    group to 0; a subnormal range falls back to scale 1 with the minimum
+    reproduced; a group holding NaN or inf, or whose range overflows, is
+    counted and gets codes 0 and a NaN scale and zero, without touching the
+    other group of its column."""
+    K, gs, N = 64, 32, 6
+    r = _rng(33)
+    W = r.normal(0.0, 1.0, size=(N, K)).astype(np.float32)
+    W[0] = 3.25
+    W[1] = 0.0
+    W[2, 5] = np.nan
+    W[3, 40] = np.inf
+    W[4, :32] = np.where(np.arange(32) % 2 == 0, 3e38, -3e38).astype(np.float32)
+    W[5, :32] = np.where(np.arange(32) % 3 == 0, 1e-40, 2e-40).astype(np.float32)
+    Bq, s, z, bad = orc.quantize(W, gs)
+    assert bad == 3
+    codes = byte_view_codes(Bq, K, N)
+    D = orc.dequant_f64(Bq, s, z, K, N, gs)
+    assert np.all(D[0] == 3.25) and np.all(s[0] == 1.0)
+    assert np.all(D[1] == 0.0)
+    for n, g in ((2, 0), (3, 1), (4, 0)):
+        assert math.isnan(s[n, g]) and math.isnan(z[n, g])
+        assert np.all(codes[n, g * gs:(g + 1) * gs] == 0)
+        other = 1 - g
+        seg = slice(other * gs, (other + 1) * gs)
+        assert np.isfinite(s[n, other])
+        assert np.all(np.abs(D[n, seg] - W[n, seg]) <= 0.5 * s[n, other] * (1 + 1e-5)
+                      + 4 * _U * np.abs(W[n, seg]).max())
+    assert s[5, 0] == 1.0 and D[5, 0] == np.float64(np.float32(1e-40))
+
+
+def pin_mlx_worked_example(orc):
+    """MLX words 0x76543210 and 0xFEDCBA98 (codes 0..7 and 8..15) with scale 1/2
+    and bias -4 give w = q/2 - 4 = -4, -3.5, ..., 3.5, through the page's
+    formula and through the conversion (zero 8) and this format's dequant."""
+    K, N, gs = 32, 1, 32
+    packed = np.array([[0x76543210, 0xFEDCBA98, 0x76543210, 0xFEDCBA98]], np.uint32)
+    ms = np.array([[0.5]], np.float32)
+    mb = np.array([[-4.0]], np.float32)
+    expect = np.array([q / 2.0 - 4.0 for q in list(range(16)) * 2])
+    assert np.array_equal(orc.mlx_dequant_f64(packed, ms, mb, K, N, gs)[0], expect)
+    Bq, s, z = orc.from_mlx(packed, ms, mb, K, N, gs)
+    assert np.array_equal(Bq, packed) and s[0, 0] == 0.5 and z[0, 0] == 8.0
+    assert np.array_equal(orc.dequant_f64(Bq, s, z, K, N, gs)[0], expect)
+
+
+def _mlx_problem(seed, N=6, K=256, gs=64):
+    r = _rng(seed)
+    G = K // gs
+    packed = r.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    ms = (r.uniform(1e-3, 1e-2, size=(N, G)) * r.choice([-1.0, 1.0], size=(N, G)))
+    mb = -np.abs(ms) * r.uniform(0.0, 15.0, size=(N, G)) + r.normal(0.0, 1e-3, size=(N, G))
+    return packed, ms.astype(np.float32), mb.astype(np.float32), K, N, gs
+
+
+def pin_mlx_conversion(orc):
+    """Random MLX matrices: codes and scales pass through, and this format's
+    dequant of the conversion equals the page's scale * q + bias to within the
+    one rounding of the zero, |error| <= 2^-24 |bias| (in double both sides
+    are otherwise exact)."""
+    packed, ms, mb, K, N, gs = _mlx_problem(34)
+    Bq, s, z = orc.from_mlx(packed, ms, mb, K, N, gs)
+    assert np.array_equal(Bq, packed) and np.array_equal(s, ms)
+    D = orc.dequant_f64(Bq, s, z, K, N, gs)
+    R = orc.mlx_dequant_f64(packed, ms, mb, K, N, gs)
+    bias = np.repeat(mb.astype(np.float64), gs, axis=1)
+    assert np.all(np.abs(D - R) <= _U * np.abs(bias) * (1.0 + 1e-12))
+
+
+def pin_mlx_degenerate(orc):
+    """A zero scale (w = bias for every code) and a scale so small that
+    -bias/scale overflows are rewritten to codes 1, scale = bias, zero 0, so
+    this format's dequant gives the bias exactly (the page's value for the
+    overflow group rounds to the bias in binary32); other groups' words pass
+    through unchanged."""
+    packed, ms, mb, K, N, gs = _mlx_problem(35)
+    ms[1, 2] = 0.0
+    ms[3, 0] = -0.0
+    mb[3, 0] = 0.0
+    ms[4, 1] = 1e-38
+    mb[4, 1] = 3e38
+    Bq, s, z = orc.from_mlx(packed, ms, mb, K, N, gs)
+    D = orc.dequant_f64(Bq, s, z, K, N, gs)
+    R = orc.mlx_dequant_f64(packed, ms, mb, K, N, gs)
+    wpg = gs // 8
+    for n, g in ((1, 2), (3, 0), (4, 1)):
+        seg = slice(g * gs, (g + 1) * gs)
+        assert np.all(D[n, seg] == np.float64(mb[n, g]))
+        assert np.all(R[n, seg].astype(np.float32) == mb[n, g])
+        assert np.all(Bq[n, g * wpg:(g + 1) * wpg] == 0x11111111)
+    keep = np.ones_like(packed, dtype=bool)
+    for n, g in ((1, 2), (3, 0), (4, 1)):
+        keep[n, g * wpg:(g + 1) * wpg] = False
+    assert np.array_equal(Bq[keep], packed[keep])
+
+
 ALL_PINS = [
     pin_fixed_words, pin_byte_view, pin_pack_round_trip, pin_one_hot, pin_dequant_f32,
     pin_brute_force_exact, pin_abs_sum, pin_zero_point_exact, pin_lanes_independent,
@@ -416,4 +576,6 @@ ALL_PINS = [
     pin_gated_closed_forms, pin_silu_values, pin_gated_norm,
     pin_gated_input_saturation,
     pin_gated_input_values,
+    pin_quantize_grid, pin_quantize_nearest, pin_quantize_special_groups,
+    pin_mlx_worked_example, pin_mlx_conversion, pin_mlx_degenerate,
 ]

@@ -44,6 +44,13 @@ MUTANTS = {
                                 "a[i] = kind == 0 ? g * sigmoid(x) : silu(x) * g;"),
     "gated_input_kinds_swapped": ("a[i] = kind == 0 ? x * sigmoid(g) : silu(g) * x;",
                                   "a[i] = kind == 1 ? x * sigmoid(g) : silu(g) * x;"),
+    "quantize_16_steps": ("volatile float s = d / 15.0f;", "volatile float s = d / 16.0f;"),
+    "quantize_zero_sign": ("volatile float z = -lo / s;", "volatile float z = lo / s;"),
+    "quantize_floor": ("float qf = rintf(t);", "float qf = floorf(t);"),
+    "quantize_min_not_tracked": ("if (v[i] < lo) lo = v[i];", "if (v[i] < lo) hi = hi;"),
+    "quantize_nonfinite_unchecked": ("if (!isfinite(v[i])) bad = 1;", "if (!isfinite(v[i])) bad = 0;"),
+    "mlx_bias_sign": ("volatile float z = -b / s;", "volatile float z = b / s;"),
+    "mlx_degenerate_codes_zero": ("Bq[w0 + j] = 0x11111111u;", "Bq[w0 + j] = 0x00000000u;"),
     "dequant_f32_double_rounding_skipped": ("volatile float t = (float)gq4o_nibble(Bq, K, n, k) - zeros[g];",
                                             "volatile double t = (double)gq4o_nibble(Bq, K, n, k) - zeros[g];"),
 }
