@@ -627,7 +627,33 @@ def run_extras(args):
         for r in range(R):
             gq4.swiglu_gated_matvec(X, G, *mats[r], gs, C=C0, stream=s)
 
+    # producing the format: the quantizer over the 4096 -> 11008 gate/up
+    # projection (f32 weights, 180 MB each, two rotating copies) and the MLX
+    # converter over rotating MLX matrices of the same shape
+    Kq, Nq = 4096, 11008
+    Gq = Kq // gs
+    Wf = [torch.from_numpy(I.float_weights(Nq, Kq, 1600, r)).cuda() for r in range(2)]
+    qout = [gq4.quantize(Wf[r], gs) for r in range(2)]
+    mlx_set = Kq * Nq // 2 + 8 * Nq * Gq
+    Rm = max(8, -(-4 * l2 // (2 * mlx_set)))
+    mlx_in, mlx_out = [], []
+    for r in range(Rm):
+        m = I.mlx_weights(Kq, Nq, gs, 1600, r)
+        mlx_in.append(tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a)
+                            .cuda() for a in (m.packed, m.scales, m.biases)))
+        mlx_out.append(gq4.from_mlx(*mlx_in[r], gs))
+
+    def quantize(s):
+        for r in range(2):
+            gq4.quantize(Wf[r], gs, *qout[r], stream=s)
+
+    def convert(s):
+        for r in range(Rm):
+            gq4.from_mlx(*mlx_in[r], gs, *mlx_out[r], stream=s)
+
     pairs = R // 2
+    t_quant = time_graph(quantize) / 2
+    t_mlx = time_graph(convert) / Rm
     t_dual = time_graph(dual) / pairs
     t_two = time_graph(two_matvecs) / pairs
     t_plain = time_graph(plain) / R
@@ -640,6 +666,10 @@ def run_extras(args):
          {"plain_matvec_us": round(t_plain, 3)}),
         ("swiglu-gated input 4096 -> 4096", t_swi, mat_bytes + 8 * K + 4 * N,
          {"plain_matvec_us": round(t_plain, 3)}),
+        ("quantize f32 4096 -> 11008 (gs %d)" % gs, t_quant,
+         Kq * Nq * 4 + Kq * Nq // 2 + 8 * Nq * Gq, {"weight_sets": 2}),
+        ("MLX convert 4096 -> 11008 (gs %d)" % gs, t_mlx, 2 * mlx_set,
+         {"weight_sets": Rm}),
     ]
     for name, us, nbytes, extra in rows:
         gbs = nbytes / (us * 1e-6) / 1e9

@@ -25,7 +25,11 @@
  *   - gated inputs: executor declarations, fuseGatedOProjDecodeEntries doc
  *     (attn_out * sigmoid(gate) into o_proj) and
  *     fuseSwiGLUGatedProjDecodeEntries doc (silu(gate) * up into the
- *     consuming projection).
+ *     consuming projection);
+ *   - producing the format: the gpu bundle's loader (the backbone's linears
+ *     quantized weight-only, group-wise to INT4 by quantizeInt4 /
+ *     quantizeBackboneInt4, body not shown) and the gpu bundle 1.0.0
+ *     dequantizeMLXProjection (MLX affine int4, w = scale * q + bias).
  *
  * ---------------------------------------------------------------------------
  * Weight format (one int4 matrix of K inputs and N output columns, group size
@@ -183,6 +187,45 @@ GQ4_API gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, 
                                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Producing the format (the step before the matvec).
+ * ------------------------------------------------------------------------ */
+
+/* Group-wise int4 quantizer.  W is f32 [N][K], column n's K weights
+ * contiguous (W[n][k] multiplies input k for output n: one row of a
+ * PyTorch or MLX Linear weight), 16-byte aligned.  Writes Bq, scales and
+ * zeros in the format above (Bq 16-byte aligned, scales and zeros 4-byte),
+ * none overlapping W or each other.  Per group of group_size consecutive
+ * inputs of a column, a min/max asymmetric map onto the 16 codes with a
+ * float zero point, every step one binary32 operation, ties to even:
+ *   lo, hi = min, max of the group (+0.0 added: no negative zero)
+ *   scale  = fl(fl(hi - lo) / 15); 1 when that is below FLT_MIN (a constant
+ *            group, or a range under 15 normal steps)
+ *   zero   = fl(-lo / scale)
+ *   q      = clamp(rint(fl(fl(v - lo) * fl(1 / scale))), 0, 15)
+ * The dequantized (q - zero) * scale is the nearest of the group's 16
+ * levels, within half a step of v.  A group holding a NaN or an infinity,
+ * or whose range hi - lo overflows, gets codes 0 and a NaN scale and zero
+ * and sets device error bit 3.  Shape rules as above (no M). */
+GQ4_API gq4_status gq4_quantize(int K, int N, int group_size, const float *W, uint32_t *Bq,
+                                float *scales, float *zeros, cudaStream_t stream);
+
+/* MLX affine int4 to this format.  packed is the MLX weight, u32 [N][K/8]
+ * (rows = output columns, 8 codes per word, low nibble first: the same words
+ * as Bq); mlx_scales and mlx_biases are f32 [N][K/group_size], and the MLX
+ * weight is w = scale * q + bias.  Writes Bq, scales, zeros with
+ * zero = fl(-bias / scale) and codes and scale copied, so that
+ * (q - zero) * scale = scale * q + bias up to the one rounding of zero
+ * (|error| <= 2^-24 |bias|).  A group without such a zero (scale 0, or
+ * -bias / scale overflowing with a finite bias, where w rounds to bias for
+ * every code) is written as codes 1, scale = bias, zero 0: exactly w = bias.
+ * Non-finite scales or biases propagate.  Bq may be packed itself (in place:
+ * only rewritten groups are stored); otherwise no output may overlap an
+ * input or another output.  packed and Bq 16-byte aligned, the rest 4-byte. */
+GQ4_API gq4_status gq4_from_mlx(int K, int N, int group_size, const uint32_t *packed,
+                                const float *mlx_scales, const float *mlx_biases, uint32_t *Bq,
+                                float *scales, float *zeros, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * One-lane call sequences (decode of a whole layer stack in one launch).
  *
  * The pages run a decode step as a list of dispatches over the same kernels
@@ -269,7 +312,8 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
  * MMA or a peer CTA of its cluster, bit 2 when a call sequence gave up
  * waiting for a copy or for the other CTAs at a call boundary (every wait
  * inside the kernels is bounded in time, so a broken copy cannot hang the
- * GPU; the outputs of that call are then invalid).  Copies the word to
+ * GPU; the outputs of that call are then invalid), bit 3 when gq4_quantize
+ * met a group with a non-finite value or range.  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);

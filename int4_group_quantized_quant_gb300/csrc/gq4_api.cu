@@ -493,14 +493,60 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
                : GQ4_ERR_CUDA;
 }
 
+gq4_status gq4_quantize(int K, int N, int group_size, const float *W, uint32_t *Bq,
+                        float *scales, float *zeros, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(1, K, N, group_size));
+    if (!W || !Bq || !scales || !zeros) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(Bq, 16) || !aligned(scales, 4) || !aligned(zeros, 4))
+        return GQ4_ERR_MISALIGNED;
+    const size_t n = (size_t)N, groups = n * (size_t)(K / group_size);
+    RangeSet rs;
+    rs.input(W, n * (size_t)K * sizeof(float));
+    rs.output(Bq, n * (size_t)K / 2);
+    rs.output(scales, groups * sizeof(float));
+    rs.output(zeros, groups * sizeof(float));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    return gq4::launch_quantize(K, N, group_size, W, Bq, scales, zeros, stream) == cudaSuccess
+               ? GQ4_OK
+               : GQ4_ERR_CUDA;
+}
+
+gq4_status gq4_from_mlx(int K, int N, int group_size, const uint32_t *packed,
+                        const float *mlx_scales, const float *mlx_biases, uint32_t *Bq,
+                        float *scales, float *zeros, cudaStream_t stream)
+{
+    GQ4_TRY(check_shape(1, K, N, group_size));
+    if (!packed || !mlx_scales || !mlx_biases || !Bq || !scales || !zeros)
+        return GQ4_ERR_INVALID_ARG;
+    if (!aligned(packed, 16) || !aligned(Bq, 16) || !aligned(mlx_scales, 4) ||
+        !aligned(mlx_biases, 4) || !aligned(scales, 4) || !aligned(zeros, 4))
+        return GQ4_ERR_MISALIGNED;
+    const size_t n = (size_t)N, groups = n * (size_t)(K / group_size);
+    RangeSet rs;
+    // in place: Bq is packed itself (each word is read and written by one thread)
+    if (packed != Bq) rs.input(packed, n * (size_t)K / 2);
+    rs.input(mlx_scales, groups * sizeof(float));
+    rs.input(mlx_biases, groups * sizeof(float));
+    rs.output(Bq, n * (size_t)K / 2);
+    rs.output(scales, groups * sizeof(float));
+    rs.output(zeros, groups * sizeof(float));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    return gq4::launch_from_mlx(K, N, group_size, packed, mlx_scales, mlx_biases, Bq, scales,
+                                zeros, stream) == cudaSuccess
+               ? GQ4_OK
+               : GQ4_ERR_CUDA;
+}
+
 gq4_status gq4_device_error(unsigned int *bits, int clear)
 {
     if (!bits) return GQ4_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     if (gq4::read_device_error(&a, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_tc_device_error(&b, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_seq_device_error(&c, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    *bits = a | b | c;
+    if (gq4::read_quant_device_error(&d, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b | c | d;
     return GQ4_OK;
 }
 

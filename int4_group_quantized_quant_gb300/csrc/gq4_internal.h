@@ -84,6 +84,14 @@ cudaError_t seq_static_scratch(void **ptr);
 cudaError_t read_device_error(unsigned int *bits, bool clear);
 cudaError_t read_tc_device_error(unsigned int *bits, bool clear);
 
+// Producing the format: the group-wise quantizer and the MLX converter.
+cudaError_t launch_quantize(int K, int N, int gs, const float *W, uint32_t *Bq, float *scales,
+                            float *zeros, cudaStream_t stream);
+cudaError_t launch_from_mlx(int K, int N, int gs, const uint32_t *packed, const float *mlx_scales,
+                            const float *mlx_biases, uint32_t *Bq, float *scales, float *zeros,
+                            cudaStream_t stream);
+cudaError_t read_quant_device_error(unsigned int *bits, bool clear);
+
 // Test kernels.
 cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream);
 cudaError_t launch_dequant(int K, int N, int gs, const uint32_t *Bq, const float *scales,

@@ -68,6 +68,8 @@ _SIGS = {
     "gq4_swiglu_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
+    "gq4_quantize": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
+    "gq4_from_mlx": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_unpack": [_i, _i, _vp, _vp, _vp],
     "gq4_dequant": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
 }
@@ -263,6 +265,58 @@ def swiglu_gated_matvec(X, G, Bq, scales, zeros, group_size, C=None, stream=None
 
 
 # ---------------------------------------------------------------------------
+# Producing the format
+# ---------------------------------------------------------------------------
+
+def _format_outputs(N, K, group_size, device, Bq, scales, zeros):
+    G = K // group_size
+    if Bq is None:
+        Bq = torch.empty((N, K // 8), dtype=torch.int32, device=device)
+    if scales is None:
+        scales = torch.empty((N, G), dtype=torch.float32, device=device)
+    if zeros is None:
+        zeros = torch.empty((N, G), dtype=torch.float32, device=device)
+    _need(Bq, "Bq", _WORDS, (N, K // 8))
+    _need(scales, "scales", _F32, (N, G))
+    _need(zeros, "zeros", _F32, (N, G))
+    return Bq, scales, zeros
+
+
+def quantize(W, group_size, Bq=None, scales=None, zeros=None, stream=None):
+    """(Bq, scales, zeros) of W f32 [N, K] (gq4_quantize: min/max asymmetric per group)."""
+    _need(W, "W", _F32)
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    if K % 8 != 0 or group_size <= 0:
+        raise ValueError("K must be a multiple of 8 and group_size positive")
+    Bq, scales, zeros = _format_outputs(N, K, group_size, W.device, Bq, scales, zeros)
+    _check(lib.gq4_quantize(K, N, group_size, _ptr(W), _ptr(Bq), _ptr(scales), _ptr(zeros),
+                            _stream(stream)), "gq4_quantize")
+    return Bq, scales, zeros
+
+
+def from_mlx(packed, mlx_scales, mlx_biases, group_size, Bq=None, scales=None, zeros=None,
+             stream=None):
+    """(Bq, scales, zeros) of an MLX affine int4 matrix (gq4_from_mlx); pass Bq=packed to
+    convert the words in place."""
+    _need(packed, "packed", _WORDS)
+    if packed.dim() != 2:
+        raise ValueError("packed must be [N, K/8]")
+    N, K = packed.shape[0], packed.shape[1] * 8
+    if group_size <= 0 or K % group_size != 0:
+        raise ValueError("K must be a multiple of group_size")
+    G = K // group_size
+    _need(mlx_scales, "mlx_scales", _F32, (N, G))
+    _need(mlx_biases, "mlx_biases", _F32, (N, G))
+    Bq, scales, zeros = _format_outputs(N, K, group_size, packed.device, Bq, scales, zeros)
+    _check(lib.gq4_from_mlx(K, N, group_size, _ptr(packed), _ptr(mlx_scales), _ptr(mlx_biases),
+                            _ptr(Bq), _ptr(scales), _ptr(zeros), _stream(stream)),
+           "gq4_from_mlx")
+    return Bq, scales, zeros
+
+
+# ---------------------------------------------------------------------------
 # Call sequences (one lane)
 # ---------------------------------------------------------------------------
 
@@ -387,7 +441,8 @@ def dequant(Bq, scales, zeros, K, group_size, W=None, stream=None):
 
 def device_error(clear: bool = True) -> int:
     """The library's sticky device error bits (bit 0: the one-lane kernel, bit 1: the
-    tensor-core kernel gave up a bounded wait)."""
+    tensor-core kernel, bit 2: a call sequence gave up a bounded wait; bit 3: the
+    quantizer met a non-finite group)."""
     bits = ctypes.c_uint(0)
     _check(lib.gq4_device_error(ctypes.byref(bits), int(clear)), "gq4_device_error")
     return int(bits.value)

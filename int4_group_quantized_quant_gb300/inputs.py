@@ -81,6 +81,38 @@ def activations(M: int, K: int, *tags: int) -> np.ndarray:
     return normal_f32((M, K), *tags, 10)
 
 
+def float_weights(N: int, K: int, *tags: int) -> np.ndarray:
+    """Unquantized linear weights f32 [N][K] (row n: output n's K inputs):
+    normal with standard deviation 0.02, each row shifted by its own normal
+    offset (standard deviation 0.005) so that groups are not centred."""
+    w = normal_f32((N, K), *tags, 30) * np.float32(0.02)
+    return (w + normal_f32((N, 1), *tags, 31) * np.float32(0.005)).astype(np.float32)
+
+
+@dataclass
+class MLXWeights:
+    """An MLX affine int4 matrix: packed u32 [N][K/8], scales and biases f32
+    [N][K/gs] with w = scale * q + bias."""
+    packed: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    K: int
+    N: int
+    gs: int
+
+
+MLX_BIAS_RANGE = (-0.18, -0.03)  # the span of -scale * zero over SCALE_RANGE x ZERO_RANGE
+
+
+def mlx_weights(K: int, N: int, gs: int, *tags: int) -> MLXWeights:
+    """Random words, scales uniform on SCALE_RANGE, biases uniform on
+    MLX_BIAS_RANGE (drawn independently)."""
+    G = K // gs
+    return MLXWeights(packed=words_u32((N, K // 8), *tags, 40),
+                      scales=uniform_f32((N, G), *SCALE_RANGE, *tags, 41),
+                      biases=uniform_f32((N, G), *MLX_BIAS_RANGE, *tags, 42), K=K, N=N, gs=gs)
+
+
 def norm_gain(K: int, *tags: int) -> np.ndarray:
     return uniform_f32((K,), *NORM_GAIN_RANGE, *tags, 20)
 

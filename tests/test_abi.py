@@ -281,3 +281,37 @@ def test_sequence_validation(gq4):
     alias = _seq_call(gq4, gq4.OP_MATVEC)
     alias.out[0] = alias.A
     assert _run_seq(gq4, [alias]) == gq4.ERR_ALIAS
+
+
+@no_gpu_only
+def test_quantize_and_mlx_checks(gq4):
+    lib = gq4.lib
+    K, N, gs = 1024, 64, 32
+    G = N * (K // gs)
+    # shape rules, NULLs, alignment
+    assert lib.gq4_quantize(K, N, 48, addr(0), addr(1), addr(2), addr(3), None) \
+        == gq4.ERR_INVALID_ARG
+    assert lib.gq4_quantize(K, N, gs, None, addr(1), addr(2), addr(3), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_quantize(K, N, gs, addr(0, 4), addr(1), addr(2), addr(3), None) \
+        == gq4.ERR_MISALIGNED
+    assert lib.gq4_quantize(K, N, gs, addr(0), addr(1, 4), addr(2), addr(3), None) \
+        == gq4.ERR_MISALIGNED
+    # outputs over W, or over each other
+    assert lib.gq4_quantize(K, N, gs, addr(0), addr(0, 4096), addr(2), addr(3), None) \
+        == gq4.ERR_ALIAS
+    assert lib.gq4_quantize(K, N, gs, addr(0), addr(1), addr(2), addr(2, 4 * (G - 1)), None) \
+        == gq4.ERR_ALIAS
+    # MLX: scales converted in place over the MLX scales, zeros over the biases
+    assert lib.gq4_from_mlx(K, N, gs, addr(0), addr(1), addr(2), addr(3), addr(1), addr(4),
+                            None) == gq4.ERR_ALIAS
+    assert lib.gq4_from_mlx(K, N, gs, addr(0), addr(1), addr(2), addr(3), addr(4), addr(2),
+                            None) == gq4.ERR_ALIAS
+    # words partly over the packed input (only the identical pointer is in place)
+    assert lib.gq4_from_mlx(K, N, gs, addr(0), addr(1), addr(2), addr(0, 16), addr(4), addr(5),
+                            None) == gq4.ERR_ALIAS
+    assert lib.gq4_from_mlx(K, N, gs, addr(0), None, addr(2), addr(3), addr(4), addr(5), None) \
+        == gq4.ERR_INVALID_ARG
+    assert lib.gq4_from_mlx(K, N, 96, addr(0), addr(1), addr(2), addr(3), addr(4), addr(5),
+                            None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_from_mlx(K, N, gs, addr(0, 8), addr(1), addr(2), addr(3), addr(4), addr(5),
+                            None) == gq4.ERR_MISALIGNED
