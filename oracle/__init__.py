@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     dequant_f32,
     dequant_f64,
     dot_cols,
+    embedding,
     from_mlx,
     gated_input_matvec,
     gated_matvec,

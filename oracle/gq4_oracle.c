@@ -22,6 +22,8 @@
  *   MLX         -- a worked word with scale 1/2 and bias -4; conversion agrees
  *                  with the page's dequant within rounding; degenerate groups
  *                  reproduce the bias exactly
+ *   embedding   -- rows equal a numpy binary32 dequant of byte-view codes of
+ *                  the chosen rows; out-of-range ids give NaN rows
  */
 #include "gq4_oracle.h"
 
@@ -449,5 +451,33 @@ int gq4o_from_mlx(int K, int N, int gs, const uint32_t *packed,
             zeros[gi] = z;
         }
     }
+    return 0;
+}
+
+/* ---- Embedding gather --------------------------------------------------- */
+
+int gq4o_embedding(int T, int K, int V, int gs, const int32_t *ids,
+                   const uint32_t *Bq, const float *scales, const float *zeros,
+                   float *out, int *bad_ids)
+{
+    if (T < 0 || !shape_ok(1, K, V, gs) || !Bq || !scales || !zeros) return -1;
+    if (T > 0 && (!ids || !out)) return -1;
+    int bad = 0;
+    for (int t = 0; t < T; ++t) {
+        const int32_t v = ids[t];
+        float *row = out + (size_t)t * K;
+        if (v < 0 || v >= V) {
+            for (int k = 0; k < K; ++k) row[k] = NAN;
+            ++bad;
+            continue;
+        }
+        for (int k = 0; k < K; ++k) {
+            const size_t g = group_index(K, gs, v, k);
+            volatile float d = (float)gq4o_nibble(Bq, K, v, k) - zeros[g];
+            volatile float w = d * scales[g];
+            row[k] = w;
+        }
+    }
+    if (bad_ids) *bad_ids = bad;
     return 0;
 }

@@ -165,6 +165,18 @@ int gq4o_from_mlx(int K, int N, int gs, const uint32_t *packed,
                   const float *mlx_scales, const float *mlx_biases,
                   uint32_t *Bq, float *scales, float *zeros);
 
+/* Int4 embedding gather (the decode step's first dispatch, EmbeddingInt4, and
+ * the per-layer-embedding row gather of the gpu bundle's executor, which
+ * dequantizes only the rows of the step's token ids from a table
+ * {packed, scales, zeros, width, groupSize}).  The table is V rows of width
+ * K in this format (row v = "column" v: K/8 words, K/gs groups).  For each of
+ * T token ids: out[t][k] = fl(fl(q(ids[t], k) - zero) * scale), the binary32
+ * dequant of gq4o_dequant_f32.  An id outside [0, V) gives a row of NaN and
+ * is counted in *bad_ids (nullable).  out is f32 [T][K]. */
+int gq4o_embedding(int T, int K, int V, int gs, const int32_t *ids,
+                   const uint32_t *Bq, const float *scales, const float *zeros,
+                   float *out, int *bad_ids);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,8 @@ def load_library(path: str):
         "gq4o_mlx_dequant_f64": (_int, [_int, _int, _int, _u32p, _f32p, _f32p, _f64p]),
         "gq4o_from_mlx": (_int, [_int, _int, _int, _u32p, _f32p, _f32p, _u32p, _f32p,
                                  _f32p]),
+        "gq4o_embedding": (_int, [_int, _int, _int, _int, _i32p, _u32p, _f32p, _f32p, _f32p,
+                                  _i32p]),
         "gq4o_gated_matvec": (_int, [_int, _int, _int, _int, _f32p, _f32p, _f32p,
                                      ctypes.c_float, _u32p, _f32p, _f32p, _u32p,
                                      _f32p, _f32p, _f64p, _f64p, _f64p, _f64p,
@@ -292,6 +294,18 @@ class Oracle:
                                       _ptr(z, _f32p)), "from_mlx")
         return Bq, s, z
 
+    def embedding(self, ids, Bq, scales, zeros, K, gs):
+        """(out f32 [T, K], bad_ids): rows ids of the int4 table dequantized in binary32."""
+        ids = _c(ids, np.int32).reshape(-1)
+        Bq, s, z = _c(Bq, np.uint32), _c(scales, np.float32), _c(zeros, np.float32)
+        V = Bq.shape[0]
+        out = np.empty((ids.size, K), np.float32)
+        bad = ctypes.c_int(0)
+        _check(self.lib.gq4o_embedding(ids.size, K, V, gs, _ptr(ids, _i32p), _ptr(Bq, _u32p),
+                                       _ptr(s, _f32p), _ptr(z, _f32p), _ptr(out, _f32p),
+                                       ctypes.byref(bad)), "embedding")
+        return out, bad.value
+
 
 def _default(name):
     def call(*args, **kwargs):
@@ -316,3 +330,4 @@ gated_input_matvec = _default("gated_input_matvec")
 quantize = _default("quantize")
 mlx_dequant_f64 = _default("mlx_dequant_f64")
 from_mlx = _default("from_mlx")
+embedding = _default("embedding")

@@ -569,6 +569,30 @@ def pin_mlx_degenerate(orc):
     assert np.array_equal(Bq[keep], packed[keep])
 
 
+def pin_embedding_rows(orc):
+    """Each gathered row equals an independent numpy binary32 dequant of the
+    byte-view codes of that table row, fl(fl(q - z) * s), for repeated,
+    first and last ids; an id of -1 or V gives a NaN row and is counted."""
+    r = _rng(36)
+    V, K, gs = 37, 192, 64
+    G = K // gs
+    Bq = r.integers(0, 2**32, size=(V, K // 8), dtype=np.uint32)
+    s = r.uniform(0.005, 0.02, size=(V, G)).astype(np.float32)
+    z = r.uniform(6.0, 9.0, size=(V, G)).astype(np.float32)
+    ids = np.array([5, 0, 36, 5, -1, 17, 37, 2], np.int32)
+    out, bad = orc.embedding(ids, Bq, s, z, K, gs)
+    assert bad == 2
+    codes = byte_view_codes(Bq, K, V).astype(np.float32)
+    for t, v in enumerate(ids):
+        if v < 0 or v >= V:
+            assert np.all(np.isnan(out[t]))
+            continue
+        sv = np.repeat(s[v], gs)
+        zv = np.repeat(z[v], gs)
+        expect = ((codes[v] - zv).astype(np.float32) * sv).astype(np.float32)
+        assert np.array_equal(out[t].view(np.uint32), expect.view(np.uint32))
+
+
 ALL_PINS = [
     pin_fixed_words, pin_byte_view, pin_pack_round_trip, pin_one_hot, pin_dequant_f32,
     pin_brute_force_exact, pin_abs_sum, pin_zero_point_exact, pin_lanes_independent,
@@ -578,4 +602,5 @@ ALL_PINS = [
     pin_gated_input_values,
     pin_quantize_grid, pin_quantize_nearest, pin_quantize_special_groups,
     pin_mlx_worked_example, pin_mlx_conversion, pin_mlx_degenerate,
+    pin_embedding_rows,
 ]

@@ -51,6 +51,11 @@ MUTANTS = {
     "quantize_nonfinite_unchecked": ("if (!isfinite(v[i])) bad = 1;", "if (!isfinite(v[i])) bad = 0;"),
     "mlx_bias_sign": ("volatile float z = -b / s;", "volatile float z = b / s;"),
     "mlx_degenerate_codes_zero": ("Bq[w0 + j] = 0x11111111u;", "Bq[w0 + j] = 0x00000000u;"),
+    "embedding_row_of_position": ("const size_t g = group_index(K, gs, v, k);\n            volatile float d = (float)gq4o_nibble(Bq, K, v, k)",
+                                  "const size_t g = group_index(K, gs, t % V, k);\n            volatile float d = (float)gq4o_nibble(Bq, K, t % V, k)"),
+    "embedding_last_id_rejected": ("if (v < 0 || v >= V) {", "if (v < 0 || v >= V - 1) {"),
+    "embedding_zero_dropped": ("volatile float d = (float)gq4o_nibble(Bq, K, v, k) - zeros[g];",
+                               "volatile float d = (float)gq4o_nibble(Bq, K, v, k);"),
     "dequant_f32_double_rounding_skipped": ("volatile float t = (float)gq4o_nibble(Bq, K, n, k) - zeros[g];",
                                             "volatile double t = (double)gq4o_nibble(Bq, K, n, k) - zeros[g];"),
 }
