@@ -651,7 +651,22 @@ def run_extras(args):
         for r in range(Rm):
             gq4.from_mlx(*mlx_in[r], gs, *mlx_out[r], stream=s)
 
+    # embedding gather: 8192 tokens from a 32000 x 4096 table (gs 128); the
+    # 128 MB output exceeds L2, the 74 MB table does not (ids are random)
+    Te, Ve = 8192, 32000
+    we = I.quant_weights(Kq, Ve, gs, 1600, 77)
+    emb_w = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda()
+                  for a in (we.Bq, we.scales, we.zeros))
+    emb_ids = [torch.from_numpy(I.rng(1600, 78, r).integers(0, Ve, size=Te, dtype=np.int32))
+               .cuda() for r in range(2)]
+    emb_out = [torch.empty((Te, Kq), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+    def embed(s):
+        for r in range(2):
+            gq4.embedding(emb_ids[r], *emb_w, gs, out=emb_out[r], stream=s)
+
     pairs = R // 2
+    t_emb = time_graph(embed) / 2
     t_quant = time_graph(quantize) / 2
     t_mlx = time_graph(convert) / Rm
     t_dual = time_graph(dual) / pairs
@@ -670,6 +685,8 @@ def run_extras(args):
          Kq * Nq * 4 + Kq * Nq // 2 + 8 * Nq * Gq, {"weight_sets": 2}),
         ("MLX convert 4096 -> 11008 (gs %d)" % gs, t_mlx, 2 * mlx_set,
          {"weight_sets": Rm}),
+        ("embedding 8192 tokens from 32000 x 4096 (gs %d)" % gs, t_emb,
+         Te * (Kq // 2 + 8 * (Kq // gs) + 4 * Kq + 4), {"weight_sets": 1, "outputs": 2}),
     ]
     for name, us, nbytes, extra in rows:
         gbs = nbytes / (us * 1e-6) / 1e9

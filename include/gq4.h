@@ -29,7 +29,11 @@
  *   - producing the format: the gpu bundle's loader (the backbone's linears
  *     quantized weight-only, group-wise to INT4 by quantizeInt4 /
  *     quantizeBackboneInt4, body not shown) and the gpu bundle 1.0.0
- *     dequantizeMLXProjection (MLX affine int4, w = scale * q + bias).
+ *     dequantizeMLXProjection (MLX affine int4, w = scale * q + bias);
+ *   - embedding gather: executor declarations, EmbeddingInt4 (the decode
+ *     step's first kernel) and setPleSource / streamPleRows (an int4 table
+ *     {packed, scales, zeros, width, groupSize} of which only the rows of the
+ *     step's token ids are dequantized).
  *
  * ---------------------------------------------------------------------------
  * Weight format (one int4 matrix of K inputs and N output columns, group size
@@ -225,6 +229,18 @@ GQ4_API gq4_status gq4_from_mlx(int K, int N, int group_size, const uint32_t *pa
                                 const float *mlx_scales, const float *mlx_biases, uint32_t *Bq,
                                 float *scales, float *zeros, cudaStream_t stream);
 
+/* Int4 embedding gather.  The table is V rows of width K in the format above
+ * (row v is "column" v: Bq u32 [V][K/8], scales and zeros f32 [V][K/gs]);
+ * ids is int32 [T] on the device; out is f32 [T][K]:
+ *   out[t][k] = fl(fl(q(ids[t], k) - zeros[ids[t]][k/gs]) * scales[...])
+ * (one binary32 rounding per operation).  An id outside [0, V) gives a row
+ * of NaN and sets device error bit 4; its table row is not read.  T = 0 is
+ * a no-op.  Shape rules as above with N = V; out 16-byte aligned, ids 4-byte;
+ * out must not overlap any input. */
+GQ4_API gq4_status gq4_embedding(int T, int K, int V, int group_size, const int32_t *ids,
+                                 const uint32_t *Bq, const float *scales, const float *zeros,
+                                 float *out, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * One-lane call sequences (decode of a whole layer stack in one launch).
  *
@@ -313,7 +329,8 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
  * waiting for a copy or for the other CTAs at a call boundary (every wait
  * inside the kernels is bounded in time, so a broken copy cannot hang the
  * GPU; the outputs of that call are then invalid), bit 3 when gq4_quantize
- * met a group with a non-finite value or range.  Copies the word to
+ * met a group with a non-finite value or range, bit 4 when gq4_embedding met
+ * an id outside its table.  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);

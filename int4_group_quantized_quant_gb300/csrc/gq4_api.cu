@@ -538,15 +538,36 @@ gq4_status gq4_from_mlx(int K, int N, int group_size, const uint32_t *packed,
                : GQ4_ERR_CUDA;
 }
 
+gq4_status gq4_embedding(int T, int K, int V, int group_size, const int32_t *ids,
+                         const uint32_t *Bq, const float *scales, const float *zeros, float *out,
+                         cudaStream_t stream)
+{
+    if (T < 0) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_shape(1, K, V, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, V, group_size, rs));
+    if (T == 0) return GQ4_OK;
+    if (!ids || !out) return GQ4_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(out, 16)) return GQ4_ERR_MISALIGNED;
+    rs.input(ids, (size_t)T * sizeof(int32_t));
+    rs.output(out, (size_t)T * (size_t)K * sizeof(float));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    return gq4::launch_embedding(T, K, V, group_size, ids, Bq, scales, zeros, out, stream) ==
+                   cudaSuccess
+               ? GQ4_OK
+               : GQ4_ERR_CUDA;
+}
+
 gq4_status gq4_device_error(unsigned int *bits, int clear)
 {
     if (!bits) return GQ4_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0, c = 0, d = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0, e = 0;
     if (gq4::read_device_error(&a, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_tc_device_error(&b, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_seq_device_error(&c, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_quant_device_error(&d, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    *bits = a | b | c | d;
+    if (gq4::read_embed_device_error(&e, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b | c | d | e;
     return GQ4_OK;
 }
 

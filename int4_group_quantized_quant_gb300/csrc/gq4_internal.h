@@ -92,6 +92,12 @@ cudaError_t launch_from_mlx(int K, int N, int gs, const uint32_t *packed, const 
                             cudaStream_t stream);
 cudaError_t read_quant_device_error(unsigned int *bits, bool clear);
 
+// Int4 embedding gather.
+cudaError_t launch_embedding(int T, int K, int V, int gs, const int32_t *ids, const uint32_t *Bq,
+                             const float *scales, const float *zeros, float *out,
+                             cudaStream_t stream);
+cudaError_t read_embed_device_error(unsigned int *bits, bool clear);
+
 // Test kernels.
 cudaError_t launch_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream);
 cudaError_t launch_dequant(int K, int N, int gs, const uint32_t *Bq, const float *scales,

@@ -70,6 +70,7 @@ _SIGS = {
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
     "gq4_quantize": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
     "gq4_from_mlx": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_embedding": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_unpack": [_i, _i, _vp, _vp, _vp],
     "gq4_dequant": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
 }
@@ -316,6 +317,22 @@ def from_mlx(packed, mlx_scales, mlx_biases, group_size, Bq=None, scales=None, z
     return Bq, scales, zeros
 
 
+def embedding(ids, Bq, scales, zeros, group_size, out=None, stream=None):
+    """out [T, K] = the int4 table's rows ids dequantized (gq4_embedding)."""
+    _need(ids, "ids", (torch.int32,))
+    if ids.dim() != 1:
+        raise ValueError("ids must be [T]")
+    V, K = Bq.shape[0], Bq.shape[1] * 8
+    _weights(Bq, scales, zeros, K, group_size)
+    T = ids.shape[0]
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.float32, device=Bq.device)
+    _need(out, "out", _F32, (T, K))
+    _check(lib.gq4_embedding(T, K, V, group_size, _ptr(ids), _ptr(Bq), _ptr(scales),
+                             _ptr(zeros), _ptr(out), _stream(stream)), "gq4_embedding")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Call sequences (one lane)
 # ---------------------------------------------------------------------------
@@ -442,7 +459,8 @@ def dequant(Bq, scales, zeros, K, group_size, W=None, stream=None):
 def device_error(clear: bool = True) -> int:
     """The library's sticky device error bits (bit 0: the one-lane kernel, bit 1: the
     tensor-core kernel, bit 2: a call sequence gave up a bounded wait; bit 3: the
-    quantizer met a non-finite group)."""
+    quantizer met a non-finite group; bit 4: the embedding gather met an id outside
+    its table)."""
     bits = ctypes.c_uint(0)
     _check(lib.gq4_device_error(ctypes.byref(bits), int(clear)), "gq4_device_error")
     return int(bits.value)

@@ -315,3 +315,19 @@ def test_quantize_and_mlx_checks(gq4):
                             None) == gq4.ERR_INVALID_ARG
     assert lib.gq4_from_mlx(K, N, gs, addr(0, 8), addr(1), addr(2), addr(3), addr(4), addr(5),
                             None) == gq4.ERR_MISALIGNED
+
+
+@no_gpu_only
+def test_embedding_checks(gq4):
+    lib = gq4.lib
+    T, K, V, gs = 8, 1024, 100, 32
+    w = [addr(1), addr(2), addr(3)]
+    assert lib.gq4_embedding(-1, K, V, gs, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_embedding(T, K, V, 48, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_embedding(T, K, V, gs, None, *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_embedding(T, K, V, gs, addr(0, 2), *w, addr(4), None) == gq4.ERR_MISALIGNED
+    assert lib.gq4_embedding(T, K, V, gs, addr(0), *w, addr(4, 4), None) == gq4.ERR_MISALIGNED
+    assert lib.gq4_embedding(T, K, V, gs, addr(0), *w, addr(1, 16), None) == gq4.ERR_ALIAS
+    assert lib.gq4_embedding(T, K, V, gs, addr(0), *w, addr(0, 16), None) == gq4.ERR_ALIAS
+    # T = 0 validates the table and enqueues nothing
+    assert lib.gq4_embedding(0, K, V, gs, None, *w, None, None) == gq4.OK
