@@ -43,6 +43,7 @@ HIDDEN, FFN, GS = 4096, 11008, 128
 QKV = (4096, 1024, 1024)
 EPS = 1e-6
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------
@@ -185,6 +186,15 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash(names=None):
@@ -665,6 +675,20 @@ def run_extras(args):
         for r in range(2):
             gq4.embedding(emb_ids[r], *emb_w, gs, out=emb_out[r], stream=s)
 
+    # prefill GEMM: 512 and 2048 prompt rows through a 4096 x 4096 projection
+    gemm_w = [tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda()
+                    for a in (w.Bq, w.scales, w.zeros))
+              for w in (I.quant_weights(4096, 4096, gs, 1600, 90 + r) for r in range(2))]
+    gemm_rows = (512, 2048)
+    gemm_A = {Mg: torch.from_numpy(I.activations(Mg, 4096, 1600, 91)).cuda() for Mg in gemm_rows}
+    gemm_C = {Mg: torch.empty((Mg, 4096), dtype=torch.float32, device="cuda") for Mg in gemm_rows}
+    t_gemm = {}
+    for Mg in gemm_rows:
+        def gemm(s, Mg=Mg):
+            for r in range(2):
+                gq4.gemm(gemm_A[Mg], *gemm_w[r], gs, C=gemm_C[Mg], stream=s)
+        t_gemm[Mg] = time_graph(gemm) / 2
+
     pairs = R // 2
     t_emb = time_graph(embed) / 2
     t_quant = time_graph(quantize) / 2
@@ -688,6 +712,15 @@ def run_extras(args):
         ("embedding 8192 tokens from 32000 x 4096 (gs %d)" % gs, t_emb,
          Te * (Kq // 2 + 8 * (Kq // gs) + 4 * Kq + 4), {"weight_sets": 1, "outputs": 2}),
     ]
+    tpeak, tpeak_src = bf16_peak()
+    for Mg in gemm_rows:
+        flops = 2.0 * Mg * 4096 * 4096
+        tf = flops / (t_gemm[Mg] * 1e-6) / 1e12
+        print(json.dumps({"extra": f"gemm {Mg} x 4096 -> 4096 (gs {gs})", "rows": Mg,
+                          "group_size": gs, "us_per_call": round(t_gemm[Mg], 3),
+                          "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / tpeak, 4),
+                          "peak": tpeak, "peak_source": tpeak_src, "weight_sets": 2,
+                          "timing": "CUDA graph of 2 calls, CUDA events"}))
     for name, us, nbytes, extra in rows:
         gbs = nbytes / (us * 1e-6) / 1e9
         print(json.dumps({"extra": name, "lanes": 1, "group_size": gs, "us_per_call": round(us, 3),

@@ -30,6 +30,8 @@
  *     quantized weight-only, group-wise to INT4 by quantizeInt4 /
  *     quantizeBackboneInt4, body not shown) and the gpu bundle 1.0.0
  *     dequantizeMLXProjection (MLX affine int4, w = scale * q + bias);
+ *   - prefill GEMM: executor declarations, dispatchEntries (prefill through
+ *     tiled matmul kernels over the same weights);
  *   - embedding gather: executor declarations, EmbeddingInt4 (the decode
  *     step's first kernel) and setPleSource / streamPleRows (an int4 table
  *     {packed, scales, zeros, width, groupSize} of which only the rows of the
@@ -92,6 +94,7 @@ extern "C" {
 #endif
 
 #define GQ4_MAX_LANES 32
+#define GQ4_MAX_GEMM_ROWS (1 << 20)
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -189,6 +192,24 @@ GQ4_API gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, 
                                            const float *G, const uint32_t *Bq,
                                            const float *scales, const float *zeros, float *C,
                                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill and wide batches: the int4 GEMM.
+ *
+ * The pages run prompt processing (prefill) through tiled matmul kernels
+ * over the same int4 weights (the executor's dispatchEntries).  gq4_gemm
+ * computes C[m][n] = sum_k A[m][k] * w(n,k) for any 1 <= M <=
+ * GQ4_MAX_GEMM_ROWS rows, with the weight format, shape rules, alignment,
+ * aliasing and stream rules of gq4_matvec (M = 1 to 32 included).  Rows are
+ * processed in chunks of up to 32 on the bf16 tensor-core kernel (a chunk
+ * of fewer than 16 rows is padded to 16), so every row has the bf16
+ * tolerance |error| <= 2e-2 * sum_k |a_k w_k| + 1e-6; where that kernel
+ * cannot take the call (scales or zeros not 16-byte aligned, a device other
+ * than sm_103) the chunks run on the f32 kernels, within the same bound.
+ * ------------------------------------------------------------------------ */
+GQ4_API gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A,
+                            const uint32_t *Bq, const float *scales, const float *zeros,
+                            float *C, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Producing the format (the step before the matvec).

@@ -493,6 +493,40 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
                : GQ4_ERR_CUDA;
 }
 
+gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
+                    const float *scales, const float *zeros, float *C, cudaStream_t stream)
+{
+    if (M < 1 || M > GQ4_MAX_GEMM_ROWS) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_shape(1, K, N, group_size));
+    RangeSet rs;
+    GQ4_TRY(check_activation(A, M, K, rs));
+    GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
+    if (!C) return GQ4_ERR_INVALID_ARG;
+    GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
+    if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    // chunks of up to 32 rows on the tensor-core kernel, in order on the
+    // stream (the chunks only read the weights, so the programmatic launch of
+    // one chunk while the previous finishes is safe)
+    for (int m0 = 0; m0 < M; m0 += 32) {
+        const int rows = M - m0 < 32 ? M - m0 : 32;
+        gq4::Call call = base_call(rows, K, N, group_size, A + (size_t)m0 * K);
+        call.Bq[0] = Bq;
+        call.scales[0] = scales;
+        call.zeros[0] = zeros;
+        call.epi = gq4::kEpiStore;
+        call.out[0] = C + (size_t)m0 * N;
+        cudaError_t err;
+        if (gq4::tc_rows_supported(call))
+            err = gq4::launch_tc(call, stream);
+        else if (rows == 1 && gq4::stream_path_supported(call))
+            err = gq4::launch_stream(call, stream);
+        else
+            err = gq4::launch_fp32(call, stream);
+        if (err != cudaSuccess) return GQ4_ERR_CUDA;
+    }
+    return GQ4_OK;
+}
+
 gq4_status gq4_quantize(int K, int N, int group_size, const float *W, uint32_t *Bq,
                         float *scales, float *zeros, cudaStream_t stream)
 {

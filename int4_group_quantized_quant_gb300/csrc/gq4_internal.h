@@ -68,6 +68,8 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream);
 // bf16 tensor-core path for 16 <= M <= 32 lanes (sm_103).
 bool tc_path_supported(const Call &call);
 cudaError_t launch_tc(const Call &call, cudaStream_t stream);
+// The same kernel for a chunk of 1..32 rows of a GEMM (fewer than 16 padded).
+bool tc_rows_supported(const Call &call);
 
 // One persistent launch for a sequence of one-lane calls (gq4_run_sequence):
 // whether the calls fit its ring, and the launch (up to 128 calls per

@@ -1166,7 +1166,16 @@ bool tc_path_supported(const Call &call)
 
 cudaError_t launch_tc(const Call &call, cudaStream_t stream)
 {
-    return call.M == 16 ? dispatch_tc<16>(call, stream) : dispatch_tc<32>(call, stream);
+    // fewer than 16 lanes (row chunks of a GEMM) run padded to 16
+    return call.M <= 16 ? dispatch_tc<16>(call, stream) : dispatch_tc<32>(call, stream);
+}
+
+bool tc_rows_supported(const Call &call)
+{
+    if (call.M < 1 || call.M > 32) return false;
+    Call c = call;
+    c.M = 16;  // every other condition as for 16 lanes
+    return tc_path_supported(c);
 }
 
 cudaError_t read_tc_device_error(unsigned int *bits, bool clear)

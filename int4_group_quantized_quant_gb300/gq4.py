@@ -68,6 +68,7 @@ _SIGS = {
     "gq4_swiglu_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
+    "gq4_gemm": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_quantize": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
     "gq4_from_mlx": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_embedding": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -154,6 +155,21 @@ def matvec(A, Bq, scales, zeros, group_size, C=None, stream=None):
     _need(C, "C", _F32, (M, N))
     _check(lib.gq4_matvec(M, K, N, group_size, _ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros),
                           _ptr(C), _stream(stream)), "gq4_matvec")
+    return C
+
+
+def gemm(A, Bq, scales, zeros, group_size, C=None, stream=None):
+    """C [M, N] = A [M, K] times the int4 matrix, any M >= 1 (gq4_gemm; bf16 tensor cores)."""
+    _need(A, "A", _F32)
+    if A.dim() != 2:
+        raise ValueError("A must be [M, K]")
+    M, K = A.shape
+    N = _weights(Bq, scales, zeros, K, group_size)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _need(C, "C", _F32, (M, N))
+    _check(lib.gq4_gemm(M, K, N, group_size, _ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros),
+                        _ptr(C), _stream(stream)), "gq4_gemm")
     return C
 
 

@@ -331,3 +331,17 @@ def test_embedding_checks(gq4):
     assert lib.gq4_embedding(T, K, V, gs, addr(0), *w, addr(0, 16), None) == gq4.ERR_ALIAS
     # T = 0 validates the table and enqueues nothing
     assert lib.gq4_embedding(0, K, V, gs, None, *w, None, None) == gq4.OK
+
+
+@no_gpu_only
+def test_gemm_checks(gq4):
+    lib = gq4.lib
+    K, N, gs = 1024, 64, 32
+    w = [addr(1), addr(2), addr(3)]
+    assert lib.gq4_gemm(0, K, N, gs, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_gemm((1 << 20) + 1, K, N, gs, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_gemm(100, K, N, 48, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
+    assert lib.gq4_gemm(100, K, N, gs, addr(0, 4), *w, addr(4), None) == gq4.ERR_MISALIGNED
+    # C over the tail of A (100 rows of 4 KB)
+    assert lib.gq4_gemm(100, K, N, gs, addr(0), *w, addr(0, 99 * 4096), None) == gq4.ERR_ALIAS
+    assert lib.gq4_gemm(100, K, N, gs, addr(0), *w, None, None) == gq4.ERR_INVALID_ARG
