@@ -684,9 +684,11 @@ def run_extras(args):
     gemm_C = {Mg: torch.empty((Mg, 4096), dtype=torch.float32, device="cuda") for Mg in gemm_rows}
     t_gemm = {}
     for Mg in gemm_rows:
-        def gemm(s, Mg=Mg):
+        ws = torch.empty(gq4.gemm_workspace_bytes(Mg, 4096), dtype=torch.uint8, device="cuda")
+
+        def gemm(s, Mg=Mg, ws=ws):
             for r in range(2):
-                gq4.gemm(gemm_A[Mg], *gemm_w[r], gs, C=gemm_C[Mg], stream=s)
+                gq4.gemm(gemm_A[Mg], *gemm_w[r], gs, C=gemm_C[Mg], workspace=ws, stream=s)
         t_gemm[Mg] = time_graph(gemm) / 2
 
     pairs = R // 2

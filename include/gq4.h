@@ -200,16 +200,25 @@ GQ4_API gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, 
  * over the same int4 weights (the executor's dispatchEntries).  gq4_gemm
  * computes C[m][n] = sum_k A[m][k] * w(n,k) for any 1 <= M <=
  * GQ4_MAX_GEMM_ROWS rows, with the weight format, shape rules, alignment,
- * aliasing and stream rules of gq4_matvec (M = 1 to 32 included).  Rows are
- * processed in chunks of up to 32 on the bf16 tensor-core kernel (a chunk
- * of fewer than 16 rows is padded to 16), so every row has the bf16
- * tolerance |error| <= 2e-2 * sum_k |a_k w_k| + 1e-6; where that kernel
- * cannot take the call (scales or zeros not 16-byte aligned, a device other
- * than sm_103) the chunks run on the f32 kernels, within the same bound.
+ * aliasing and stream rules of gq4_matvec.  Every row is computed on the
+ * bf16 tensor cores with f32 accumulation (|error| <= 2e-2 * sum_k |a_k w_k|
+ * + 1e-6).  With more than 32 rows and a workspace of at least
+ * gq4_gemm_workspace_bytes(M, K) bytes (device memory, 256-byte aligned, not
+ * overlapping any argument; its contents on entry do not matter and are
+ * overwritten with a bf16 copy of A) the rows run as tiles of a dedicated
+ * GEMM kernel that dequantizes each weight tile once per 64..256 rows.
+ * Otherwise (M <= 32, workspace NULL or too small) the rows run in chunks
+ * of up to 32 on the decode tensor-core kernel (fewer than 16 padded to 16).
+ * Where neither tensor-core kernel can take the call (scales or zeros not
+ * 16-byte aligned, a device other than sm_103) the chunks run on the f32
+ * kernels, within the same bound.
  * ------------------------------------------------------------------------ */
+GQ4_API size_t gq4_gemm_workspace_bytes(int M, int K);
+
 GQ4_API gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A,
                             const uint32_t *Bq, const float *scales, const float *zeros,
-                            float *C, cudaStream_t stream);
+                            float *C, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Producing the format (the step before the matvec).
@@ -351,7 +360,7 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
  * inside the kernels is bounded in time, so a broken copy cannot hang the
  * GPU; the outputs of that call are then invalid), bit 3 when gq4_quantize
  * met a group with a non-finite value or range, bit 4 when gq4_embedding met
- * an id outside its table.  Copies the word to
+ * an id outside its table; bit 1 also covers the GEMM kernel of gq4_gemm.  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);

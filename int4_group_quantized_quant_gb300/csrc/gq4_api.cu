@@ -493,8 +493,15 @@ gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq, const f
                : GQ4_ERR_CUDA;
 }
 
+size_t gq4_gemm_workspace_bytes(int M, int K)
+{
+    if (M < 1 || K < 1) return 0;
+    return gq4::gemm_workspace_bytes(M, K);
+}
+
 gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A, const uint32_t *Bq,
-                    const float *scales, const float *zeros, float *C, cudaStream_t stream)
+                    const float *scales, const float *zeros, float *C, void *workspace,
+                    size_t workspace_bytes, cudaStream_t stream)
 {
     if (M < 1 || M > GQ4_MAX_GEMM_ROWS) return GQ4_ERR_INVALID_ARG;
     GQ4_TRY(check_shape(1, K, N, group_size));
@@ -503,7 +510,18 @@ gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A, const u
     GQ4_TRY(check_weights(Bq, scales, zeros, K, N, group_size, rs));
     if (!C) return GQ4_ERR_INVALID_ARG;
     GQ4_TRY(check_output(C, (size_t)M * (size_t)N, rs));
+    const size_t need = gq4::gemm_workspace_bytes(M, K);
+    const bool use_ws = workspace && workspace_bytes >= need;
+    if (use_ws) {
+        if (!aligned(workspace, 256)) return GQ4_ERR_MISALIGNED;
+        rs.output(workspace, need);
+    }
     if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+    if (M > 32 && use_ws && gq4::gemm_path_supported(K, N, group_size, scales, zeros))
+        return gq4::launch_gemm(M, K, N, group_size, A, Bq, scales, zeros, C, workspace, stream) ==
+                       cudaSuccess
+                   ? GQ4_OK
+                   : GQ4_ERR_CUDA;
     // chunks of up to 32 rows on the tensor-core kernel, in order on the
     // stream (the chunks only read the weights, so the programmatic launch of
     // one chunk while the previous finishes is safe)
@@ -601,7 +619,9 @@ gq4_status gq4_device_error(unsigned int *bits, int clear)
     if (gq4::read_seq_device_error(&c, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_quant_device_error(&d, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_embed_device_error(&e, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    *bits = a | b | c | d | e;
+    unsigned int f = 0;
+    if (gq4::read_gemm_device_error(&f, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b | c | d | e | f;
     return GQ4_OK;
 }
 

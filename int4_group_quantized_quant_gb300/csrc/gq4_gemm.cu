@@ -1,0 +1,723 @@
+// gq4_gemm.cu -- the int4 GEMM for prefill and wide batches on the
+// 5th-generation tensor core: C[m][n] = sum_k A[m][k] * (q(n,k) - z) * s for
+// any number of rows M (the executor's prefill path runs the prompt through
+// tiled matmul kernels over the same int4 weights).
+//
+// D[n][m] = W[n][:] . A[m][:] in bf16 with f32 accumulation, tile by tile:
+//   * a tile is TR = 128 weight columns (the MMA's M) by MT = 64, 128 or 256
+//     rows of A (the MMA's N); one CTA per SM walks the tiles, n fastest, so
+//     the CTAs running together share their rows of A in L2;
+//   * the rows of A are first converted once to bf16 (gq4_gemm's workspace),
+//     with the eight values of each 8-code chunk in the order the dequant
+//     yields the codes, (0,4,1,5,2,6,3,7); a tile's rows then arrive per
+//     64-code K-block by a 2-D tensor-map copy into the 128-byte swizzled
+//     K-major layout the MMA reads, through their own ring;
+//   * the producer warp also streams the packed codes, scales and zeros of
+//     the tile's 128 columns in 256-code stages (tensor-map copies; the at
+//     most 3 rows past the last whole super-row of scales by cp.async);
+//   * 8 dequant warps turn each K-block of codes into bf16 (q - z) * s,
+//     rounded once, straight into tensor memory (the A operand), exactly as
+//     the decode tensor-core kernel does;
+//   * one thread issues the MMAs (128 x MT x 16, A from tensor memory, B from
+//     shared memory), accumulating the tile in tensor memory (MT columns);
+//   * 4 epilogue warps read the accumulator (thread = weight column) and
+//     store C row by row (32 consecutive columns per warp store).
+// Every wait is bounded; on expiry the kernel records bit 1 of the device
+// error word, stops waiting, drains what it issued and leaves.
+#include <cuda.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "gq4_internal.h"
+#include "gq4_tcgen05.cuh"
+
+namespace gq4 {
+
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+
+constexpr int kDqWarps = 8;    // warps 0..7
+constexpr int kEpWarps = 4;    // warps 8..11
+constexpr int kPrWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+constexpr int kEpBase = kDqWarps * 32;
+constexpr int kTR = 128;       // weight columns per tile
+constexpr int kNW = 8;         // tensor-memory slots of dequantized K-blocks
+constexpr int kStageK = 256;   // codes per weight stage
+constexpr int kBlockK = 64;    // codes per K-block
+constexpr int kMaxStages = 8;  // weight ring
+constexpr int kMaxAct = 8;     // activation ring
+constexpr int kMaxGps = 8;
+constexpr uint32_t kTmemCols = 512u;  // W slots 0..255, accumulator from 256
+
+struct GemmParams {
+    CUtensorMap codes;     // [N][K/8] u32, box {32, 128}, 128-byte swizzle
+    CUtensorMap sz[2];     // scales / zeros as [Q][P*G] super-rows, box {BW, 128/P}
+    CUtensorMap act;       // bf16 [M][K] (chunk-permuted), box {64, MT}, 128-byte swizzle
+    int M, K, N, gs, G;
+    int n_tiles_n, n_tiles;
+    int n_st;              // weight stages per tile
+    int S, SA;             // ring depths (weights, activations)
+    int gps, P, Q, BW, logP;
+    unsigned long long gmagic;  // ceil(2^40 / (gs/32))
+    uint32_t off_act, act_bytes, off_ring, stage_bytes, codes_bytes;
+    uint32_t sz_box_bytes, sz_box_stride, off_sz, off_tail, off_misc, off_bar;
+    uint32_t magic_bf16;   // 0x43004300
+    const float *scales;
+    const float *zeros;
+    float *C;
+};
+
+struct Bars {
+    uint64_t *full, *empty, *a_full, *a_empty, *w_full, *w_empty, *acc_full, *acc_empty, *drain;
+};
+
+__device__ __forceinline__ int chunk_group(int c, unsigned long long gmagic)
+{
+    return (int)(((unsigned long long)c * gmagic) >> 40);
+}
+
+// Bounded wait (see the decode tensor-core kernel): gives up when another
+// thread of the CTA gave up, or after the time limit (recording the error).
+__device__ __noinline__ bool gemm_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(&g_gemm_error, 2u);
+            return false;
+        }
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+
+    Bars bar;
+    {
+        uint64_t *b = reinterpret_cast<uint64_t *>(smem + p.off_bar);
+        bar.full = b;
+        bar.empty = b + kMaxStages;
+        bar.a_full = b + 2 * kMaxStages;
+        bar.a_empty = bar.a_full + kMaxAct;
+        bar.w_full = bar.a_empty + kMaxAct;
+        bar.w_empty = bar.w_full + kNW;
+        bar.acc_full = bar.w_empty + kNW;
+        bar.acc_empty = bar.acc_full + 1;
+        bar.drain = bar.acc_empty + 1;
+    }
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_misc);
+    volatile int *abort = reinterpret_cast<int *>(smem + p.off_misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_tl = (int)blockIdx.x < p.n_tiles
+                         ? (p.n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                         : 0;
+    const int KB = p.n_st * (kStageK / kBlockK);  // K-blocks per tile
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.S; ++s) {
+            mbar_init(&bar.full[s], 32);  // the producer lanes' cp.async arrivals
+            mbar_init(&bar.empty[s], kDqWarps);
+        }
+        for (int s = 0; s < p.SA; ++s) {
+            mbar_init(&bar.a_full[s], 1);
+            mbar_init(&bar.a_empty[s], 1);
+        }
+        for (int s = 0; s < kNW; ++s) {
+            mbar_init(&bar.w_full[s], kDqWarps);
+            mbar_init(&bar.w_empty[s], 1);
+        }
+        mbar_init(bar.acc_full, 1);
+        mbar_init(bar.acc_empty, kEpWarps);
+        mbar_init(bar.drain, 1);
+        *abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    auto tile_n0 = [&](int tl) { return ((int)blockIdx.x + tl * (int)gridDim.x) % p.n_tiles_n * kTR; };
+    auto tile_m0 = [&](int tl) { return ((int)blockIdx.x + tl * (int)gridDim.x) / p.n_tiles_n * MT; };
+
+    // =====================================================================
+    // Producer warp: weight stages and activation K-blocks.
+    // =====================================================================
+    if (warp == kPrWarp) {
+        if (lane == 0) {
+            prefetch_tensormap(&p.codes);
+            prefetch_tensormap(&p.sz[0]);
+            prefetch_tensormap(&p.sz[1]);
+            prefetch_tensormap(&p.act);
+        }
+        bool ok = true;
+        int issued = 0, a_issued = 0;
+        int slot = 0, phase = 0, aslot = 0, aphase = 0;
+        bool dep_waited = false;
+        for (int tl = 0; ok && tl < n_tl; ++tl) {
+            const int n0 = tile_n0(tl), m0 = tile_m0(tl);
+            for (int st = 0; ok && st < p.n_st; ++st) {
+                // ---- the stage's codes, scales and zeros ----
+                if (issued >= p.S) {
+                    bool got = true;
+                    if (lane == 0) got = gemm_wait(&bar.empty[slot], phase ^ 1, abort);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+                const int k0 = st * kStageK;
+                const int g0 = chunk_group(k0 >> 5, p.gmagic);
+                if (lane == 0) {
+                    mbar_expect_tx(&bar.full[slot], p.codes_bytes + 2u * p.P * p.sz_box_bytes);
+                    tma_load_2d(stage, &p.codes, k0 / 8, n0, &bar.full[slot]);
+#pragma unroll
+                    for (int arr = 0; arr < 2; ++arr)
+                        for (int rho = 0; rho < p.P; ++rho) {
+                            const int x = (rho * p.G + g0) & ~3;
+                            tma_load_2d(stage + p.off_sz + (arr * p.P + rho) * p.sz_box_stride, &p.sz[arr],
+                                        x, n0 >> p.logP, &bar.full[slot]);
+                        }
+                }
+                // rows past the last whole super-row (only in the last column tile)
+                const int tail0 = p.P * p.Q;
+                if (tail0 < p.N && n0 + kTR > tail0) {
+                    const int n_tail = p.N - tail0;  // < P
+                    const int g_last = chunk_group((min(k0 + kStageK, p.K) - 1) >> 5, p.gmagic);
+                    const int per = n_tail * p.gps;
+                    for (int it = lane; it < 2 * per; it += 32) {
+                        const int arr = it / per;
+                        const int rem = it - arr * per;
+                        const int t = rem / p.gps;
+                        const int gl = rem - t * p.gps;
+                        const int off = (t * p.G + g0) & 3;
+                        const bool valid = k0 < p.K && g0 + gl <= g_last;
+                        const float *src = arr ? p.zeros : p.scales;
+                        float *d = reinterpret_cast<float *>(stage + p.off_tail) + (arr * 4 + t) * p.BW + off + gl;
+                        cp_async_4(d, src + (valid ? (size_t)(tail0 + t) * p.G + g0 + gl : 0), valid);
+                    }
+                }
+                cp_async_mbar_arrive(&bar.full[slot]);
+                ++issued;
+                if (++slot == p.S) {
+                    slot = 0;
+                    phase ^= 1;
+                }
+                // ---- the stage's four K-blocks of activations ----
+                if (lane == 0) {
+                    if (!dep_waited) {
+                        // the activations are the conversion kernel's output
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        dep_waited = true;
+                    }
+                    for (int e = 0; e < kStageK / kBlockK; ++e) {
+                        if (a_issued >= p.SA && !gemm_wait(&bar.a_empty[aslot], aphase ^ 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bar.a_full[aslot], p.act_bytes);
+                        tma_load_2d(smem + p.off_act + (size_t)aslot * p.act_bytes, &p.act,
+                                    (st * (kStageK / kBlockK) + e) * kBlockK, m0, &bar.a_full[aslot]);
+                        ++a_issued;
+                        if (++aslot == p.SA) {
+                            aslot = 0;
+                            aphase ^= 1;
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+        }
+        if (!ok && lane == 0) {
+            // leave no copy in flight into this CTA's shared memory
+            for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
+                (void)mbar_wait(&bar.full[i % p.S], (i / p.S) & 1);
+            for (int i = (a_issued > p.SA ? a_issued - p.SA : 0); i < a_issued; ++i)
+                (void)mbar_wait(&bar.a_full[i % p.SA], (i / p.SA) & 1);
+        }
+    }
+
+    // =====================================================================
+    // Dequant warps: K-blocks of codes -> bf16 (q - z) * s in tensor memory.
+    // =====================================================================
+    else if (warp < kDqWarps) {
+        const int q4 = warp & 3;
+        const int h = warp >> 2;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const uint32_t magic = p.magic_bf16;
+        const int rho = r & (p.P - 1);
+        const int srow = r >> p.logP;
+        bool ok = true;
+        int kbg = 0;
+        int slot = 0, phase = 0;
+        for (int tl = 0; ok && tl < n_tl; ++tl) {
+            const int n0 = tile_n0(tl);
+            const int R = n0 + r;
+            for (int st = 0; ok && st < p.n_st; ++st) {
+                if (!__all_sync(0xffffffffu, gemm_wait(&bar.full[slot], phase, abort))) {
+                    ok = false;
+                    break;
+                }
+                const int k0 = st * kStageK;
+                const int c0 = k0 >> 5;
+                const int g0 = chunk_group(c0, p.gmagic);
+                const unsigned char *stage = smem + p.off_ring + (size_t)slot * p.stage_bytes;
+                const int g_last = chunk_group((min(k0 + kStageK, p.K) - 1) >> 5, p.gmagic);
+                const bool row_valid = R < p.N && k0 < p.K;
+                const int off = (rho * p.G + g0) & 3;
+                const float *s_src, *z_src;
+                if (R >= p.P * p.Q) {
+                    const int t = R - p.P * p.Q;
+                    const float *tail = reinterpret_cast<const float *>(stage + p.off_tail);
+                    s_src = tail + (0 * 4 + t) * p.BW + off;
+                    z_src = tail + (1 * 4 + t) * p.BW + off;
+                } else {
+                    s_src = reinterpret_cast<const float *>(stage + p.off_sz + (0 * p.P + rho) * p.sz_box_stride) +
+                            srow * p.BW + off;
+                    z_src = reinterpret_cast<const float *>(stage + p.off_sz + (1 * p.P + rho) * p.sz_box_stride) +
+                            srow * p.BW + off;
+                }
+                // bf16 constants of the current group: (128 + zi) twice, the
+                // scale twice, (zi - z) * scale twice; rows and groups past the
+                // matrix keep (128, 0, 0), which dequantizes any code to 0
+                int cur_gl = -1;
+                uint32_t c2 = 0x43004300u, s2 = 0u, d2 = 0u;
+                constexpr int KPS = 4;  // the stage's 4 K-blocks per step
+                bool got = true;
+#pragma unroll
+                for (int e = 0; e < KPS; ++e) {
+                    const int kb = kbg + e;
+                    if (got && kb >= kNW) got = gemm_wait(&bar.w_empty[kb % kNW], ((kb / kNW) - 1) & 1, abort);
+                }
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                uint4 wv[KPS];
+#pragma unroll
+                for (int e = 0; e < KPS; ++e)
+                    wv[e] = *reinterpret_cast<const uint4 *>(stage + r * 128 + (((2 * e + h) ^ (r & 7)) << 4));
+#pragma unroll
+                for (int e = 0; e < KPS; ++e) {
+                    const int ws = (kbg + e) % kNW;
+                    const int gl = chunk_group(c0 + 2 * e + h, p.gmagic) - g0;
+                    if (row_valid && gl != cur_gl && g0 + gl <= g_last) {
+                        cur_gl = gl;
+                        const float sv = s_src[gl], zv = z_src[gl];
+                        const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
+                        const float dzs = (zi - zv) * sv;
+                        c2 = bf16x2_pack(128.0f + zi, 128.0f + zi);
+                        s2 = bf16x2_pack(sv, sv);
+                        d2 = bf16x2_pack(dzs, dzs);
+                    }
+                    uint32_t o[16];
+                    const uint32_t words[4] = {wv[e].x, wv[e].y, wv[e].z, wv[e].w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint32_t w = words[wi];
+                        o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w, magic), c2), s2, d2);
+                        o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 4, magic), c2), s2, d2);
+                        o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 8, magic), c2), s2, d2);
+                        o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 12, magic), c2), s2, d2);
+                    }
+                    tmem_st16(tmem_base + lane_off + (uint32_t)(ws * 32) + 16 * h, o);
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int e = 0; e < KPS; ++e) mbar_arrive(&bar.w_full[(kbg + e) % kNW]);
+                    mbar_arrive(&bar.empty[slot]);
+                }
+                kbg += KPS;
+                if (++slot == p.S) {
+                    slot = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    }
+
+    // =====================================================================
+    // MMA warp (one thread issues).
+    // =====================================================================
+    else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTR, MT);
+            const uint32_t act_s = smem_addr(smem + p.off_act);
+            const uint32_t d = tmem_base + 256u;
+            bool ok = true, any = false;
+            int kbg = 0;
+            for (int tl = 0; ok && tl < n_tl; ++tl) {
+                if (tl >= 1 && !gemm_wait(bar.acc_empty, (tl - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                for (int kb = 0; kb < KB; ++kb, ++kbg) {
+                    const int ws = kbg % kNW;
+                    const int as = kbg % p.SA;
+                    if (!gemm_wait(&bar.w_full[ws], (kbg / kNW) & 1, abort) ||
+                        !gemm_wait(&bar.a_full[as], (kbg / p.SA) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t bdesc = smem_desc_sw128(act_s + (uint32_t)as * p.act_bytes, 1024);
+                    const uint32_t a0 = tmem_base + (uint32_t)(ws * 32);
+#pragma unroll
+                    for (int jj = 0; jj < kBlockK / 16; ++jj)
+                        tc_mma_ts(d, a0 + 8 * jj, bdesc + (uint64_t)(2 * jj), idesc, (kb | jj) != 0 ? 1u : 0u);
+                    any = true;
+                    tc_commit(&bar.w_empty[ws]);
+                    tc_commit(&bar.a_empty[as]);
+                }
+                if (!ok) break;
+                tc_commit(bar.acc_full);
+            }
+            if (!ok && any) {
+                // let the MMAs in flight finish before tensor memory is freed
+                tc_commit(bar.drain);
+                (void)mbar_wait(bar.drain, 0);
+            }
+        }
+        __syncwarp();
+    }
+
+    // =====================================================================
+    // Epilogue warps: accumulator -> C.
+    // =====================================================================
+    else {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        bool ok = true;
+        for (int tl = 0; tl < n_tl; ++tl) {
+            ok = __all_sync(0xffffffffu, ok && gemm_wait(bar.acc_full, tl & 1, abort));
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int n0 = tile_n0(tl), m0 = tile_m0(tl);
+            const int col = n0 + r;
+            float *cbase = p.C + (size_t)m0 * p.N + col;
+#pragma unroll 1
+            for (int c = 0; c < MT / 16; ++c) {
+                uint32_t u[16];
+                tmem_ld16(tmem_base + lane_off + 256u + 16 * c, u);
+                tmem_wait_ld();
+                if (col < p.N) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int m = 16 * c + e;
+                        if (m0 + m < p.M) cbase[(size_t)m * p.N] = __uint_as_float(u[e]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.acc_empty);
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// f32 rows -> bf16 rows, each 8-value chunk in the order (0,4,1,5,2,6,3,7).
+__global__ void __launch_bounds__(256) act_to_bf16_kernel(long long n_chunks, const float4 *__restrict__ A,
+                                                          uint4 *__restrict__ out)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < n_chunks; c += stride) {
+        const float4 lo = __ldg(A + 2 * c), hi = __ldg(A + 2 * c + 1);
+        uint4 r;
+        r.x = bf16x2_pack(lo.x, hi.x);
+        r.y = bf16x2_pack(lo.y, hi.y);
+        r.z = bf16x2_pack(lo.z, hi.z);
+        r.w = bf16x2_pack(lo.w, hi.w);
+        out[c] = r;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+uint32_t rup(uint32_t x, uint32_t a)
+{
+    return (x + a - 1) / a * a;
+}
+
+int gcd_i(int a, int b)
+{
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Most scale groups one 256-code stage (starting at a multiple of 256) spans.
+int stage_groups(int gs)
+{
+    int most = 1;
+    for (int k0 = 0; k0 < kStageK * gs; k0 += kStageK) {
+        const int g = (k0 + kStageK - 1) / gs - k0 / gs + 1;
+        most = g > most ? g : most;
+        if (k0 % gs == 0 && k0 > 0) break;
+    }
+    return most;
+}
+
+int device_sms()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+// Rows per tile: the MT with the least estimated time, counting per K-block
+// max(dequant, MMA) with the MMA of 128 x 256 x 64 about 2.5 dequant units,
+// and whole waves of tiles over the SMs.
+int choose_mt(int M, int N, int sms)
+{
+    const int tn = (N + kTR - 1) / kTR;
+    int best = 256;
+    double best_cost = 0.0;
+    for (int mt = 256; mt >= 64; mt /= 2) {
+        const long long tiles = (long long)tn * ((M + mt - 1) / mt);
+        const long long waves = (tiles + sms - 1) / sms;
+        const double per_kb = mt * 2.5 / 256.0 > 1.0 ? mt * 2.5 / 256.0 : 1.0;
+        const double cost = (double)waves * (per_kb + 0.02 * mt / 64.0);
+        if (mt == 256 || cost < best_cost * 0.97) {
+            best = mt;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+template <int MT>
+cudaError_t launch_gemm_mt(int M, int K, int N, int gs, const uint32_t *Bq, const float *scales,
+                           const float *zeros, float *C, const uint16_t *abf, cudaStream_t stream)
+{
+    auto kern = gemm_kernel<MT>;
+    int dev = 0, optin = 0;
+    cudaError_t err;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return err;
+    static std::atomic<int> ready_dev{-1};
+    if (ready_dev.load(std::memory_order_acquire) != dev) {
+        if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin)) != cudaSuccess)
+            return err;
+        ready_dev.store(dev, std::memory_order_release);
+    }
+    EncodeTiledFn encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const int sms = device_sms();
+    if (sms <= 0) return cudaErrorInvalidValue;
+
+    GemmParams prm{};
+    prm.M = M;
+    prm.K = K;
+    prm.N = N;
+    prm.gs = gs;
+    prm.G = K / gs;
+    prm.n_tiles_n = (N + kTR - 1) / kTR;
+    const long long tiles = (long long)prm.n_tiles_n * ((M + MT - 1) / MT);
+    if (tiles > 0x7fffffffll) return cudaErrorInvalidValue;
+    prm.n_tiles = (int)tiles;
+    prm.n_st = (K + kStageK - 1) / kStageK;
+    prm.gps = stage_groups(gs);
+    if (prm.gps > kMaxGps) return cudaErrorInvalidValue;
+    prm.P = 4 / gcd_i(prm.G, 4);
+    prm.logP = prm.P == 1 ? 0 : prm.P == 2 ? 1 : 2;
+    prm.Q = N / prm.P;
+    prm.BW = (3 + prm.gps + 3) / 4 * 4;
+    {
+        const unsigned long long d = (unsigned long long)(gs / 32);
+        prm.gmagic = ((1ull << 40) + d - 1) / d;
+    }
+    prm.codes_bytes = (uint32_t)kTR * 128u;
+    prm.sz_box_bytes = (uint32_t)(kTR / prm.P) * (uint32_t)prm.BW * 4u;
+    prm.sz_box_stride = rup(prm.sz_box_bytes, 128u);
+    prm.off_sz = prm.codes_bytes;
+    prm.off_tail = prm.off_sz + 2u * (uint32_t)prm.P * prm.sz_box_stride;
+    prm.stage_bytes = rup(prm.off_tail + 2u * 4u * (uint32_t)prm.BW * 4u, 1024u);
+    prm.act_bytes = (uint32_t)MT * 128u;
+    prm.magic_bf16 = 0x43004300u;
+    prm.scales = scales;
+    prm.zeros = zeros;
+    prm.C = C;
+    // shared memory: activation ring, weight ring, misc, barriers (+ 1024 alignment pad)
+    const uint32_t misc_bar = 256u + (2 * kMaxStages + 2 * kMaxAct + 2 * kNW + 3) * 8u;
+    const uint32_t budget = (uint32_t)optin - 1024u - misc_bar;
+    int SA = 4;
+    int S = 0;
+    for (; SA >= 2; --SA) {
+        const uint32_t left = budget > (uint32_t)SA * prm.act_bytes ? budget - (uint32_t)SA * prm.act_bytes : 0u;
+        S = (int)(left / prm.stage_bytes);
+        if (S >= 2) break;
+    }
+    if (SA < 2 || S < 2) return cudaErrorInvalidValue;
+    if (S > kMaxStages) S = kMaxStages;
+    // deeper activation ring with what is left
+    while (SA < kMaxAct && (uint32_t)(SA + 1) * prm.act_bytes + (uint32_t)S * prm.stage_bytes <= budget) ++SA;
+    prm.S = S;
+    prm.SA = SA;
+    prm.off_act = 0;
+    prm.off_ring = (uint32_t)SA * prm.act_bytes;
+    prm.off_misc = prm.off_ring + (uint32_t)S * prm.stage_bytes;
+    prm.off_bar = prm.off_misc + 256u;
+    const uint32_t smem = prm.off_bar + (2 * kMaxStages + 2 * kMaxAct + 2 * kNW + 3) * 8u + 1024u;
+    if (smem > (uint32_t)optin) return cudaErrorInvalidValue;
+
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+        const cuuint32_t box[2] = {32u, (cuuint32_t)kTR};
+        const cuuint32_t estr[2] = {1u, 1u};
+        if (encode(&prm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(Bq), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)prm.P * prm.G, (cuuint64_t)(N / prm.P)};
+        const cuuint64_t strides[1] = {(cuuint64_t)prm.P * prm.G * 4u};
+        const cuuint32_t box[2] = {(cuuint32_t)prm.BW, (cuuint32_t)(kTR / prm.P)};
+        const cuuint32_t estr[2] = {1u, 1u};
+        for (int arr = 0; arr < 2; ++arr) {
+            const float *base = arr == 0 ? scales : zeros;
+            if (encode(&prm.sz[arr], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2u};
+        const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)MT};
+        const cuuint32_t estr[2] = {1u, 1u};
+        if (encode(&prm.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(abf), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(prm.n_tiles < sms ? prm.n_tiles : sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    // the producer waits for the conversion kernel (griddepcontrol.wait)
+    // before its first activation copy; weights stream at once
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, kern, prm)) != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int M, int K)
+{
+    return ((size_t)M * (size_t)K * 2u + 255u) / 256u * 256u;
+}
+
+bool gemm_path_supported(int K, int N, int gs, const float *scales, const float *zeros)
+{
+    const int P = 4 / gcd_i(K / gs, 4);
+    if (N < P) return false;
+    if ((reinterpret_cast<uintptr_t>(scales) & 15u) != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(zeros) & 15u) != 0) return false;
+    if (stage_groups(gs) > kMaxGps) return false;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm(int M, int K, int N, int gs, const float *A, const uint32_t *Bq, const float *scales,
+                        const float *zeros, float *C, void *workspace, cudaStream_t stream)
+{
+    const int sms = device_sms();
+    if (sms <= 0) return cudaErrorInvalidValue;
+    uint16_t *abf = static_cast<uint16_t *>(workspace);
+    const long long n_chunks = (long long)M * (K / 8);
+    const long long want = (n_chunks + 255) / 256;
+    const long long cap = (long long)sms * 8;
+    act_to_bf16_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(
+        n_chunks, reinterpret_cast<const float4 *>(A), reinterpret_cast<uint4 *>(abf));
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    switch (choose_mt(M, N, sms)) {
+    case 64: return launch_gemm_mt<64>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);
+    case 128: return launch_gemm_mt<128>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);
+    default: return launch_gemm_mt<256>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);
+    }
+}
+
+cudaError_t read_gemm_device_error(unsigned int *bits, bool clear)
+{
+    cudaError_t err = cudaMemcpyFromSymbol(bits, g_gemm_error, sizeof(unsigned int));
+    if (err != cudaSuccess || !clear) return err;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace gq4

@@ -86,6 +86,13 @@ cudaError_t seq_static_scratch(void **ptr);
 cudaError_t read_device_error(unsigned int *bits, bool clear);
 cudaError_t read_tc_device_error(unsigned int *bits, bool clear);
 
+// The int4 GEMM for more than 32 rows (bf16 copy of A in the workspace).
+size_t gemm_workspace_bytes(int M, int K);
+bool gemm_path_supported(int K, int N, int gs, const float *scales, const float *zeros);
+cudaError_t launch_gemm(int M, int K, int N, int gs, const float *A, const uint32_t *Bq, const float *scales,
+                        const float *zeros, float *C, void *workspace, cudaStream_t stream);
+cudaError_t read_gemm_device_error(unsigned int *bits, bool clear);
+
 // Producing the format: the group-wise quantizer and the MLX converter.
 cudaError_t launch_quantize(int K, int N, int gs, const float *W, uint32_t *Bq, float *scales,
                             float *zeros, cudaStream_t stream);

@@ -68,7 +68,7 @@ _SIGS = {
     "gq4_swiglu_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
-    "gq4_gemm": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
+    "gq4_gemm": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "gq4_quantize": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
     "gq4_from_mlx": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_embedding": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -87,9 +87,11 @@ lib.gq4_device_error.restype = _i
 lib.gq4_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _i]
 lib.gq4_sequence_workspace_bytes.restype = ctypes.c_size_t
 lib.gq4_sequence_workspace_bytes.argtypes = []
+lib.gq4_gemm_workspace_bytes.restype = ctypes.c_size_t
+lib.gq4_gemm_workspace_bytes.argtypes = [_i, _i]
 
 EXPORTED = list(_SIGS) + ["gq4_status_string", "gq4_version", "gq4_device_error",
-                          "gq4_sequence_workspace_bytes"]
+                          "gq4_sequence_workspace_bytes", "gq4_gemm_workspace_bytes"]
 
 
 class GQ4Error(RuntimeError):
@@ -158,8 +160,14 @@ def matvec(A, Bq, scales, zeros, group_size, C=None, stream=None):
     return C
 
 
-def gemm(A, Bq, scales, zeros, group_size, C=None, stream=None):
-    """C [M, N] = A [M, K] times the int4 matrix, any M >= 1 (gq4_gemm; bf16 tensor cores)."""
+def gemm_workspace_bytes(M, K) -> int:
+    return int(lib.gq4_gemm_workspace_bytes(M, K))
+
+
+def gemm(A, Bq, scales, zeros, group_size, C=None, workspace=None, stream=None):
+    """C [M, N] = A [M, K] times the int4 matrix, any M >= 1 (gq4_gemm; bf16 tensor cores).
+    ``workspace`` (a CUDA tensor of at least gemm_workspace_bytes(M, K) bytes) enables the
+    GEMM kernel for M > 32; ``workspace=False`` runs the row chunks without one."""
     _need(A, "A", _F32)
     if A.dim() != 2:
         raise ValueError("A must be [M, K]")
@@ -168,8 +176,15 @@ def gemm(A, Bq, scales, zeros, group_size, C=None, stream=None):
     if C is None:
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _need(C, "C", _F32, (M, N))
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, K), dtype=torch.uint8, device=A.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not False:
+        if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     _check(lib.gq4_gemm(M, K, N, group_size, _ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros),
-                        _ptr(C), _stream(stream)), "gq4_gemm")
+                        _ptr(C), ws_ptr, ws_bytes, _stream(stream)), "gq4_gemm")
     return C
 
 

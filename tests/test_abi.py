@@ -338,10 +338,18 @@ def test_gemm_checks(gq4):
     lib = gq4.lib
     K, N, gs = 1024, 64, 32
     w = [addr(1), addr(2), addr(3)]
-    assert lib.gq4_gemm(0, K, N, gs, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
-    assert lib.gq4_gemm((1 << 20) + 1, K, N, gs, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
-    assert lib.gq4_gemm(100, K, N, 48, addr(0), *w, addr(4), None) == gq4.ERR_INVALID_ARG
-    assert lib.gq4_gemm(100, K, N, gs, addr(0, 4), *w, addr(4), None) == gq4.ERR_MISALIGNED
+    ws = gq4.gemm_workspace_bytes(100, K)
+    assert ws >= 100 * K * 2
+
+    def g(M, gs_, A, C, W=None, wb=0):
+        return lib.gq4_gemm(M, K, N, gs_, A, *w, C, W, wb, None)
+    assert g(0, gs, addr(0), addr(4)) == gq4.ERR_INVALID_ARG
+    assert g((1 << 20) + 1, gs, addr(0), addr(4)) == gq4.ERR_INVALID_ARG
+    assert g(100, 48, addr(0), addr(4)) == gq4.ERR_INVALID_ARG
+    assert g(100, gs, addr(0, 4), addr(4)) == gq4.ERR_MISALIGNED
     # C over the tail of A (100 rows of 4 KB)
-    assert lib.gq4_gemm(100, K, N, gs, addr(0), *w, addr(0, 99 * 4096), None) == gq4.ERR_ALIAS
-    assert lib.gq4_gemm(100, K, N, gs, addr(0), *w, None, None) == gq4.ERR_INVALID_ARG
+    assert g(100, gs, addr(0), addr(0, 99 * 4096)) == gq4.ERR_ALIAS
+    assert g(100, gs, addr(0), None) == gq4.ERR_INVALID_ARG
+    # workspace: misaligned, or over C
+    assert g(100, gs, addr(0), addr(4), addr(5, 16), ws) == gq4.ERR_MISALIGNED
+    assert g(100, gs, addr(0), addr(4), addr(4, 256), ws) == gq4.ERR_ALIAS
