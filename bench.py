@@ -548,6 +548,21 @@ def run_profile_case(args):
     b.build()
     from int4_group_quantized_quant_gb300 import gq4
     torch.cuda.set_device(0)
+    if args.profile == "gemm":
+        # prefill GEMM: 2048 rows through one 4096 x 4096 projection (gs 128)
+        from int4_group_quantized_quant_gb300 import inputs as I
+        Mg, K = 2048, 4096
+        w = I.quant_weights(K, 4096, GS, 1600, 90)
+        Wd = tuple(torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda()
+                   for a in (w.Bq, w.scales, w.zeros))
+        A = torch.from_numpy(I.activations(Mg, K, 1600, 91)).cuda()
+        C = torch.empty((Mg, 4096), dtype=torch.float32, device="cuda")
+        ws = torch.empty(gq4.gemm_workspace_bytes(Mg, K), dtype=torch.uint8, device="cuda")
+        for _ in range(args.steps):
+            gq4.gemm(A, *Wd, GS, C=C, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": "gemm", "rows": Mg, "launch_rounds": args.steps}))
+        return
     stack = Stack(gq4, args.layers, args.lanes)
     stream = torch.cuda.current_stream()
     for _ in range(args.steps):
@@ -744,7 +759,7 @@ def main():
     ap.add_argument("--roofline-rounds", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["gated", "down", "quad", "step"], default=None,
+    ap.add_argument("--profile", choices=["gated", "down", "quad", "step", "gemm"], default=None,
                     help="run a small launch sequence of one kernel for ncu (no timing)")
     ap.add_argument("--extras", action="store_true",
                     help="time the dual and gated-input matvecs (one JSON line each)")

@@ -30,8 +30,8 @@
  *     quantized weight-only, group-wise to INT4 by quantizeInt4 /
  *     quantizeBackboneInt4, body not shown) and the gpu bundle 1.0.0
  *     dequantizeMLXProjection (MLX affine int4, w = scale * q + bias);
- *   - prefill GEMM: executor declarations, dispatchEntries (prefill through
- *     tiled matmul kernels over the same weights);
+ *   - prefill GEMM: executor declarations, dispatchEntries (prefill as tiled
+ *     matrix multiplies over the same weights);
  *   - embedding gather: executor declarations, EmbeddingInt4 (the decode
  *     step's first kernel) and setPleSource / streamPleRows (an int4 table
  *     {packed, scales, zeros, width, groupSize} of which only the rows of the
@@ -196,8 +196,9 @@ GQ4_API gq4_status gq4_swiglu_gated_matvec(int M, int K, int N, int group_size, 
 /* ------------------------------------------------------------------------
  * Prefill and wide batches: the int4 GEMM.
  *
- * The pages run prompt processing (prefill) through tiled matmul kernels
- * over the same int4 weights (the executor's dispatchEntries).  gq4_gemm
+ * On the pages, prompt processing (prefill) multiplies all the prompt's rows
+ * by the same int4 weights in tiled matrix-multiply kernels (the executor's
+ * dispatchEntries).  gq4_gemm
  * computes C[m][n] = sum_k A[m][k] * w(n,k) for any 1 <= M <=
  * GQ4_MAX_GEMM_ROWS rows, with the weight format, shape rules, alignment,
  * aliasing and stream rules of gq4_matvec.  Every row is computed on the
