@@ -586,9 +586,12 @@ def run_profile_case(args):
 
 
 def run_extras(args):
-    """Time the dual projection and the gated-input matvecs (one lane, 7B-sized
-    4096 x 4096 matrices), each in a CUDA graph over rotating weight sets
-    larger than 4x L2, against the plain matvec; one JSON line per op."""
+    """Time the widened entry points, one JSON line per op: the dual projection
+    and the gated-input matvecs (one lane, 4096 x 4096, in a CUDA graph over
+    rotating weight sets larger than 4x L2, against the plain matvec), the
+    prefill GEMM (512 and 2048 rows through 4096 x 4096, against the bf16
+    peak), the quantizer and the MLX converter (4096 x 11008) and the
+    embedding gather (8192 ids from a 32000 x 4096 table)."""
     import torch
     from int4_group_quantized_quant_gb300 import build as b
     b.build()
@@ -762,7 +765,8 @@ def main():
     ap.add_argument("--profile", choices=["gated", "down", "quad", "step", "gemm"], default=None,
                     help="run a small launch sequence of one kernel for ncu (no timing)")
     ap.add_argument("--extras", action="store_true",
-                    help="time the dual and gated-input matvecs (one JSON line each)")
+                    help="time the dual, gated-input, GEMM, quantizer, MLX and embedding "
+                         "entry points (one JSON line each)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and args.profile is None:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
