@@ -33,6 +33,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gq4_host.h"
 #include "gq4_internal.h"
 #include "gq4_tcgen05.cuh"
 
@@ -505,31 +506,6 @@ __global__ void __launch_bounds__(256) act_to_bf16_kernel(long long n_chunks, co
 // Host side
 // ---------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, []() {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-uint32_t rup(uint32_t x, uint32_t a)
-{
-    return (x + a - 1) / a * a;
-}
-
 uint32_t gemm_smem_budget(int optin)
 {
     const uint32_t misc_bar = 256u + (2 * kMaxStages + 2 * kMaxAct + 2 * kNW + 3) * 8u;
@@ -539,41 +515,12 @@ uint32_t gemm_smem_budget(int optin)
 // Bytes of one weight stage (codes, scale and zero boxes, tail rows).
 uint32_t weight_stage_bytes(int K, int gs, int gps)
 {
-    const int G = K / gs;
-    int a = G, b = 4;
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
-    }
-    const int P = 4 / a;
+    const int P = 4 / gcd_int(K / gs, 4);
     const int BW = (3 + gps + 3) / 4 * 4;
     const uint32_t box = (uint32_t)(kTR / P) * (uint32_t)BW * 4u;
-    const uint32_t stride = rup(box, 128u);
+    const uint32_t stride = round_up(box, 128u);
     const uint32_t tail_off = (uint32_t)kTR * 128u + 2u * (uint32_t)P * stride;
-    return rup(tail_off + 2u * 4u * (uint32_t)BW * 4u, 1024u);
-}
-
-int gcd_i(int a, int b)
-{
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
-
-// Most scale groups one 256-code stage (starting at a multiple of 256) spans.
-int stage_groups(int gs)
-{
-    int most = 1;
-    for (int k0 = 0; k0 < kStageK * gs; k0 += kStageK) {
-        const int g = (k0 + kStageK - 1) / gs - k0 / gs + 1;
-        most = g > most ? g : most;
-        if (k0 % gs == 0 && k0 > 0) break;
-    }
-    return most;
+    return round_up(tail_off + 2u * 4u * (uint32_t)BW * 4u, 1024u);
 }
 
 int device_sms()
@@ -638,7 +585,7 @@ cudaError_t launch_gemm_mt(int M, int K, int N, int gs, const uint32_t *Bq, cons
             return err;
         ready_dev.store(dev, std::memory_order_release);
     }
-    EncodeTiledFn encode = encode_fn();
+    EncodeTiledFn encode = encode_tiled_fn();
     if (!encode) return cudaErrorNotSupported;
     const int sms = device_sms();
     if (sms <= 0) return cudaErrorInvalidValue;
@@ -654,9 +601,9 @@ cudaError_t launch_gemm_mt(int M, int K, int N, int gs, const uint32_t *Bq, cons
     if (tiles > 0x7fffffffll) return cudaErrorInvalidValue;
     prm.n_tiles = (int)tiles;
     prm.n_st = (K + kStageK - 1) / kStageK;
-    prm.gps = stage_groups(gs);
+    prm.gps = groups_per_stage(gs, kStageK);
     if (prm.gps > kMaxGps) return cudaErrorInvalidValue;
-    prm.P = 4 / gcd_i(prm.G, 4);
+    prm.P = 4 / gcd_int(prm.G, 4);
     prm.logP = prm.P == 1 ? 0 : prm.P == 2 ? 1 : 2;
     prm.Q = N / prm.P;
     prm.BW = (3 + prm.gps + 3) / 4 * 4;
@@ -666,10 +613,10 @@ cudaError_t launch_gemm_mt(int M, int K, int N, int gs, const uint32_t *Bq, cons
     }
     prm.codes_bytes = (uint32_t)kTR * 128u;
     prm.sz_box_bytes = (uint32_t)(kTR / prm.P) * (uint32_t)prm.BW * 4u;
-    prm.sz_box_stride = rup(prm.sz_box_bytes, 128u);
+    prm.sz_box_stride = round_up(prm.sz_box_bytes, 128u);
     prm.off_sz = prm.codes_bytes;
     prm.off_tail = prm.off_sz + 2u * (uint32_t)prm.P * prm.sz_box_stride;
-    prm.stage_bytes = rup(prm.off_tail + 2u * 4u * (uint32_t)prm.BW * 4u, 1024u);
+    prm.stage_bytes = round_up(prm.off_tail + 2u * 4u * (uint32_t)prm.BW * 4u, 1024u);
     prm.act_bytes = (uint32_t)MT * 128u;
     prm.magic_bf16 = 0x43004300u;
     prm.scales = scales;
@@ -748,16 +695,16 @@ size_t gemm_workspace_bytes(int M, int K)
 
 bool gemm_path_supported(int K, int N, int gs, const float *scales, const float *zeros)
 {
-    const int P = 4 / gcd_i(K / gs, 4);
+    const int P = 4 / gcd_int(K / gs, 4);
     if (N < P) return false;
     if ((reinterpret_cast<uintptr_t>(scales) & 15u) != 0) return false;
     if ((reinterpret_cast<uintptr_t>(zeros) & 15u) != 0) return false;
-    if (stage_groups(gs) > kMaxGps) return false;
+    if (groups_per_stage(gs, kStageK) > kMaxGps) return false;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
-    return major == 10 && minor == 3 && encode_fn() != nullptr;
+    return major == 10 && minor == 3 && encode_tiled_fn() != nullptr;
 }
 
 cudaError_t launch_gemm(int M, int K, int N, int gs, const float *A, const uint32_t *Bq, const float *scales,
@@ -777,7 +724,7 @@ cudaError_t launch_gemm(int M, int K, int N, int gs, const float *A, const uint3
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
         return err;
-    switch (choose_mt(M, N, sms, gemm_smem_budget(optin), weight_stage_bytes(K, gs, stage_groups(gs)))) {
+    switch (choose_mt(M, N, sms, gemm_smem_budget(optin), weight_stage_bytes(K, gs, groups_per_stage(gs, kStageK)))) {
     case 64: return launch_gemm_mt<64>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);
     case 128: return launch_gemm_mt<128>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);
     default: return launch_gemm_mt<256>(M, K, N, gs, Bq, scales, zeros, C, abf, stream);

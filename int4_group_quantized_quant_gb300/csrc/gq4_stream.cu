@@ -40,6 +40,7 @@
 #include <cstdint>
 
 #include "gq4_device.cuh"
+#include "gq4_host.h"
 #include "gq4_internal.h"
 #include "gq4_onelane.cuh"
 #include "gq4_tma.cuh"
@@ -394,21 +395,6 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
             }
         }
     }
-}
-
-int gcd_int(int a, int b)
-{
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
-
-uint32_t round_up(uint32_t x, uint32_t a)
-{
-    return (x + a - 1) / a * a;
 }
 
 template <int NMAT, int PRO, int EPI, int R, int SPW>

@@ -49,6 +49,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gq4_host.h"
 #include "gq4_internal.h"
 #include "gq4_tcgen05.cuh"
 
@@ -859,31 +860,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
 // Host side
 // ---------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn()
-{
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, []() {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-uint32_t round_up(uint32_t x, uint32_t a)
-{
-    return (x + a - 1) / a * a;
-}
-
 struct TcPlan {
     int ks, TR, n_tiles, n_clusters, S, gps;
     uint32_t smem;
@@ -896,16 +872,6 @@ struct StageGeom {
     int P, BW;
     uint32_t codes_bytes, sz_box_bytes, sz_box_stride, off_sz, off_tail, stage_bytes;
 };
-
-int gcd_int(int a, int b)
-{
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
 
 StageGeom stage_geom(int TR, int nmat, int G, int gps)
 {
@@ -920,20 +886,6 @@ StageGeom stage_geom(int TR, int nmat, int G, int gps)
     const uint32_t tail = (uint32_t)nmat * 2u * 4u * (uint32_t)g.BW * 4u;
     g.stage_bytes = (g.off_tail + tail + 1023u) / 1024u * 1024u;
     return g;
-}
-
-// Most scale groups one 256-code stage (starting at a multiple of 256) spans,
-// counted without clipping at K, so every K-block of a stage -- including
-// those past K in the last stage -- finds its constant row in the stage.
-int groups_per_stage(int gs)
-{
-    int most = 1;
-    for (int k0 = 0; k0 < kStageK * gs; k0 += kStageK) {
-        const int g = (k0 + kStageK - 1) / gs - k0 / gs + 1;
-        most = g > most ? g : most;
-        if (k0 % gs == 0 && k0 > 0) break;  // the pattern repeats
-    }
-    return most;
 }
 
 constexpr int kMaxDevices = 64;
@@ -975,7 +927,7 @@ int max_clusters(int dev, int ks, const void *kern)
 bool plan_tc(const Call &call, int MP, int dev, const void *kern, int smem_optin, TcPlan &best)
 {
     const int n_st = (call.K + kStageK - 1) / kStageK;
-    const int gps = groups_per_stage(call.gs);
+    const int gps = groups_per_stage(call.gs, kStageK);
     if (gps > kMaxGps) return false;
     const int nmat = call.nmat;
     double best_cost = 0.0;
@@ -1182,7 +1134,7 @@ bool tc_path_supported(const Call &call)
         if ((reinterpret_cast<uintptr_t>(call.scales[m]) & 15u) != 0) return false;
         if ((reinterpret_cast<uintptr_t>(call.zeros[m]) & 15u) != 0) return false;
     }
-    if (groups_per_stage(call.gs) > kMaxGps) return false;
+    if (groups_per_stage(call.gs, kStageK) > kMaxGps) return false;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
