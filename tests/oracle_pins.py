@@ -242,6 +242,30 @@ def pin_norm_constant(orc):
         assert np.allclose(a, expect, rtol=(K + 8) * 2.0 ** -53, atol=0), (c, eps, a[0, 0], expect)
 
 
+def pin_norm_gain_closed_form(orc):
+    """A_a = c, A_b = 0 and a gain of distinct powers of two (then one-hot):
+    a_k = c * W_k / sqrt(c^2 + eps) element by element (closed form, 50 digits).
+
+    Every W_k differs from its neighbours, so a dropped gain, a gain read at
+    the wrong index or a gain applied once for the whole vector each fail."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    K = 96
+    gains = [np.float32(2.0 ** ((k * 5) % 11 - 5)) for k in range(K)]
+    one_hot = [np.float32(0.0)] * K
+    one_hot[37] = np.float32(8.0)
+    for c, eps, W in [(0.75, 1e-6, gains), (-3.0, 0.5, gains), (2.0, 1e-6, one_hot)]:
+        A_a = np.full((1, K), c, np.float32)
+        A_b = np.zeros((1, K), np.float32)
+        Wv = np.array(W, np.float32)
+        x, a, _ = orc.norm(A_a, A_b, Wv, eps, K)
+        cf = Decimal(float(np.float32(c)))
+        base = cf / (cf * cf + Decimal(float(np.float32(eps)))).sqrt()
+        expect = np.array([float(base * Decimal(float(w))) for w in W])
+        assert np.all(x == np.float32(c))
+        assert np.all(np.abs(a[0] - expect) <= (K + 8) * 2.0 ** -53 * np.abs(expect)), (c, eps)
+
+
 def pin_norm_scale_invariance(orc):
     """With eps = 0, doubling x leaves the normalised vector unchanged exactly."""
     K = 512
@@ -596,7 +620,7 @@ def pin_embedding_rows(orc):
 ALL_PINS = [
     pin_fixed_words, pin_byte_view, pin_pack_round_trip, pin_one_hot, pin_dequant_f32,
     pin_brute_force_exact, pin_abs_sum, pin_zero_point_exact, pin_lanes_independent,
-    pin_quad_routing, pin_norm_constant, pin_norm_scale_invariance, pin_norm_residual,
+    pin_quad_routing, pin_norm_constant, pin_norm_gain_closed_form, pin_norm_scale_invariance, pin_norm_residual,
     pin_gated_closed_forms, pin_silu_values, pin_gated_norm,
     pin_gated_input_saturation,
     pin_gated_input_values,

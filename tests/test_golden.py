@@ -74,3 +74,11 @@ def test_norm_eps_default(orc):
     _, a, _ = orc.norm(A, None, Wn, eps, K)
     expect = float(Decimal(c["expected_a"]))
     assert np.all(np.abs(a - expect) <= 2e-16 * expect)
+    # a gain of distinct powers of two: a_k = c * W_k / sqrt(c^2 + eps)
+    g = d["constant_input_gain"]
+    K = g["K"]
+    A = np.full((1, K), g["value"], np.float32)
+    Wn = np.array(g["W_norm"], np.float32)
+    _, a, _ = orc.norm(A, None, Wn, eps, K)
+    expect = np.array([float(Decimal(v)) for v in g["expected_a"]])
+    assert np.all(np.abs(a[0] - expect) <= 2e-16 * np.abs(expect))

@@ -36,6 +36,7 @@ MUTANTS = {
     "norm_residual_second_addend_dropped": ("volatile float xk = ab ? aa[k] + ab[k] : aa[k];\n            if (x)",
                                             "volatile float xk = aa[k];\n            if (x)"),
     "norm_gain_dropped": ("* inv_rms * (double)W_norm[k]", "* inv_rms"),
+    "norm_gain_index_off_by_one": ("* inv_rms * (double)W_norm[k]", "* inv_rms * (double)W_norm[(k + 1) % K]"),
     "norm_sqrt_dropped": ("1.0 / sqrt(sum_sq", "1.0 / (sum_sq"),
     "silu_sign": ("t / (1.0 + exp(-t))", "t / (1.0 + exp(t))"),
     "gate_up_swapped": ("out[at] = silu(gv) * uv;", "out[at] = silu(uv) * gv;"),
@@ -58,6 +59,14 @@ MUTANTS = {
                                "volatile float d = (float)gq4o_nibble(Bq, K, v, k);"),
     "dequant_f32_double_rounding_skipped": ("volatile float t = (float)gq4o_nibble(Bq, K, n, k) - zeros[g];",
                                             "volatile double t = (double)gq4o_nibble(Bq, K, n, k) - zeros[g];"),
+}
+
+
+# Mutants that a closed form (not a restatement of the oracle's formula) must
+# catch: the named pin has to be among the failing ones.
+CAUGHT_BY = {
+    "norm_gain_dropped": "pin_norm_gain_closed_form",
+    "norm_gain_index_off_by_one": "pin_norm_gain_closed_form",
 }
 
 
@@ -87,3 +96,5 @@ def test_mutant_is_caught(name, source, tmp_path):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"mutant {name} passed every pin"
+    if name in CAUGHT_BY:
+        assert CAUGHT_BY[name] in failed, f"mutant {name} not caught by {CAUGHT_BY[name]}: {failed}"
