@@ -217,6 +217,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_narrow_kernel(QuantPar
             if (pos == 0) store_group_params(p, gi[u], m, bad);
         }
     }
+    // The matvec kernels may start streaming these weights as soon as this
+    // grid's blocks have exited (programmatic dependent launch, before their
+    // dependency wait): make every store visible GPU-wide before exit.
+    __threadfence();
 }
 
 // Groups of more than 32 words: one warp per group, lanes striding over its
@@ -253,6 +257,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_wide_kernel(QuantParam
         }
         if (lane == 0) store_group_params(p, gi, m, bad);
     }
+    // The matvec kernels may start streaming these weights as soon as this
+    // grid's blocks have exited (programmatic dependent launch, before their
+    // dependency wait): make every store visible GPU-wide before exit.
+    __threadfence();
 }
 
 // MLX conversion: one thread per 4 words (32 codes, always inside one
@@ -301,6 +309,9 @@ __global__ void __launch_bounds__(256) from_mlx_kernel(long long n_chunks, int w
             }
         }
     }
+    // visible GPU-wide before exit: a following matvec may stream these
+    // weights before its dependency wait (programmatic dependent launch)
+    __threadfence();
 }
 
 int resident_blocks(const void *kernel)

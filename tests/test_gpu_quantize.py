@@ -210,15 +210,52 @@ def test_from_mlx_in_place(gq4):
     assert_same_params("zeros", host(z), rz)
 
 
+def _stale_weights(K, N, gs, tag):
+    """Device buffers (Bq, scales, zeros) holding other weights, settled before a
+    producer overwrites them: a matvec that read them stale fails parity."""
+    w = I.quant_weights(K, N, gs, tag, 99)
+    bufs = tuple(dev(a) for a in (w.Bq, w.scales, w.zeros))
+    torch.cuda.synchronize()
+    return bufs
+
+
 def test_from_mlx_matvec(gq4):
-    """A converted MLX matrix in the matvec: within the fp32 tolerance of the oracle's
-    matvec of the MLX weights dequantized by the page's formula."""
+    """gq4_from_mlx immediately followed by gq4_matvec on the same stream (nothing
+    in between, no host synchronisation): the matvec streams the converted
+    weights, compared with the oracle's matvec of the oracle's conversion."""
     K, N, gs = 4096, 257, 64
     m = I.mlx_weights(K, N, gs, 1712)
-    Bq, s, z = gq4.from_mlx(dev(m.packed), dev(m.scales), dev(m.biases), gs)
-    A = I.activations(1, K, 1712)
-    C = host(gq4.matvec(dev(A), Bq, s, z, gs))
-    Wm = oracle.mlx_dequant_f64(m.packed, m.scales, m.biases, K, N, gs)
-    ref = A.astype(np.float64) @ Wm.T
-    S = np.abs(A.astype(np.float64)) @ np.abs(Wm.T)
-    check_close("matvec of converted MLX", C, ref, tol_fp32(S))
+    packed, ms, mb = dev(m.packed), dev(m.scales), dev(m.biases)
+    Bq, s, z = _stale_weights(K, N, gs, 1712)
+    A = dev(I.activations(1, K, 1712))
+    C = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        gq4.from_mlx(packed, ms, mb, gs, Bq, s, z)
+        gq4.matvec(A, Bq, s, z, gs, C=C)
+        torch.cuda.synchronize()
+        rBq, rs, rz = oracle.from_mlx(m.packed, m.scales, m.biases, K, N, gs)
+        ref, S = oracle.matvec(host(A), rBq, rs, rz, K, N, gs)
+        check_close("matvec of converted MLX", host(C), ref, tol_fp32(S))
+        # back to stale contents for the next round
+        Bq.copy_(_stale_weights(K, N, gs, 1712)[0])
+        torch.cuda.synchronize()
+
+
+def test_quantize_then_matvec_chain(gq4):
+    """gq4_quantize immediately followed by gq4_matvec on the same stream (nothing
+    in between, no host synchronisation), on the 4096 -> 11008 gate projection:
+    the matvec sees the new codes, scales and zeros."""
+    K, N, gs = 4096, 11008, 128
+    W = dev(I.float_weights(N, K, 1713))
+    Bq, s, z = _stale_weights(K, N, gs, 1713)
+    A = dev(I.activations(1, K, 1713))
+    C = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    gq4.quantize(W, gs, Bq, s, z)
+    gq4.matvec(A, Bq, s, z, gs, C=C)
+    torch.cuda.synchronize()
+    rBq, rs, rz, _ = oracle.quantize(host(W), gs)
+    ref, S = oracle.matvec(host(A), rBq, rs, rz, K, N, gs)
+    check_close("matvec after quantize", host(C), ref, tol_fp32(S))
+    assert gq4.device_error() == 0
