@@ -69,9 +69,17 @@
  *     Stream order holds for activations, norm inputs and outputs.  One
  *     exception for weights: calls with M = 1 or 16 <= M <= 32 are launched
  *     with programmatic dependent launch, so such a call may start reading
- *     its Bq, scales and zeros while the call just before it on the same
- *     stream (if it is one of these) is still running.  The weights of a call
- *     must therefore not be written by the call immediately preceding it.
+ *     its Bq, scales and zeros before the kernel just before it on the same
+ *     stream has completed: while it runs, if it is one of these matvecs
+ *     (which signal early), else once its blocks have exited.  Hence:
+ *       - the weights of a call must not be outputs of the matvec call
+ *         immediately preceding it;
+ *       - any other kernel that writes a call's weights and immediately
+ *         precedes it on the stream must make those stores visible GPU-wide
+ *         before its blocks exit (every writing thread executes
+ *         __threadfence() after its last store, as gq4_quantize and
+ *         gq4_from_mlx do), or the caller puts a non-kernel operation
+ *         (an event wait, a copy) or a host synchronisation in between.
  *   - Results are deterministic: the same inputs give the same bits.
  *   - Arithmetic: with M = 1 or 2 <= M <= 15 lanes every product and sum is
  *     f32 (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot
@@ -324,6 +332,15 @@ GQ4_API size_t gq4_sequence_workspace_bytes(void);
 GQ4_API gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace,
                                     cudaStream_t stream);
 
+/* How gq4_run_sequence and gq4_run_sequence_static would run `calls`
+ * (no counterpart on the pages: it reports the library's own plan).
+ * *launches receives the number of persistent launches the sequence takes
+ * (one per 128 calls), or 0 when it would run as individual launches of the
+ * single-call kernels.  The calls are validated as gq4_run_sequence
+ * validates them (the workspace aside); the same statuses are returned and
+ * nothing is enqueued.  Host only: reads the current device's attributes. */
+GQ4_API gq4_status gq4_sequence_launches(const gq4_call *calls, int n_calls, int *launches);
+
 /* Allocation-free form of gq4_run_sequence, for callers that cannot
  * allocate device memory.  The pages have no counterpart to it: it changes
  * only where the launch's scratch lives.  Same calls, validation, semantics
@@ -334,10 +351,12 @@ GQ4_API gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *wo
  * GQ4_ERR_INVALID_ARG before anything is enqueued.  Nothing is allocated:
  * no cudaMalloc, cudaFree or allocating library routine; the array's
  * address is looked up once per device.  The counters must start at zero:
- * every call enqueues a cudaMemsetAsync of them on `stream` before its
- * launch.  All such calls on one device share the array, so calls that
- * overlap on the GPU (other streams, other host threads) race: the caller
- * must order them. */
+ * once every call has passed validation, a call that runs as the persistent
+ * launch enqueues a cudaMemsetAsync of them on `stream` right before that
+ * launch (a rejected call enqueues nothing; a sequence that runs as
+ * individual launches does not touch the array).  All such calls on one
+ * device share the array, so calls that overlap on the GPU (other streams,
+ * other host threads) race: the caller must order them. */
 GQ4_API gq4_status gq4_run_sequence_static(const gq4_call *calls, int n_calls, cudaStream_t stream);
 
 /* Integer unpack test kernel: q[n*K + k] = q(n,k) as u8 [N][K].

@@ -413,44 +413,86 @@ size_t gq4_sequence_workspace_bytes(void)
     return gq4::kSeqWorkspaceBytes;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Validates a call list against the launch scratch `scratch` (bytes
+// [scratch, scratch + kSeqWorkspaceBytes) must not overlap any call's
+// buffers) and builds the calls.  `persistent` tells whether the list runs
+// as one persistent launch (every call plannable, scale/zero rows 16-byte
+// aligned) or call by call.  Nothing is enqueued.
+gq4_status prepare_sequence(const gq4_call *calls, int n_calls, const void *scratch,
+                            std::vector<gq4::Call> &built, bool &persistent)
+{
+    built.assign((size_t)n_calls, gq4::Call{});
+    persistent = true;
+    for (int i = 0; i < n_calls; ++i) {
+        GQ4_TRY(build_seq_call(calls[i], built[(size_t)i]));
+        const gq4::Call &c = built[(size_t)i];
+        const size_t mk = (size_t)c.M * (size_t)c.K * sizeof(float);
+        // the scratch is the launch's own: no call may touch it
+        RangeSet rs;
+        rs.input(c.A, mk);
+        for (int m = 0; m < c.nmat; ++m) {
+            rs.input(c.Bq[m], (size_t)c.N * (size_t)c.K / 2);
+            rs.input(c.scales[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
+            rs.input(c.zeros[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
+        }
+        for (int j = 0; j < 4; ++j) rs.input(c.out[j], (size_t)c.M * (size_t)c.seg_len[j] * sizeof(float));
+        if (c.norm) {
+            rs.input(c.norm->A_b, mk);
+            rs.input(c.norm->W_norm, (size_t)c.K * sizeof(float));
+            rs.input(c.norm->residual_out, mk);
+            rs.input(c.norm->norm_out, mk);
+        }
+        rs.output(scratch, gq4::kSeqWorkspaceBytes);
+        if (!rs.disjoint()) return GQ4_ERR_ALIAS;
+        // the persistent kernel copies scale/zero rows in bulk (16-byte bases)
+        for (int m = 0; m < c.nmat; ++m)
+            if (!aligned(c.scales[m], 16) || !aligned(c.zeros[m], 16)) persistent = false;
+    }
+    if (persistent) persistent = gq4::sequence_plannable(built.data(), n_calls);
+    return GQ4_OK;
+}
+
+gq4_status run_prepared(const std::vector<gq4::Call> &built, bool persistent, void *scratch,
+                        cudaStream_t stream)
+{
+    if (persistent)
+        return gq4::launch_sequence(built.data(), (int)built.size(), scratch, stream) == cudaSuccess
+                   ? GQ4_OK
+                   : GQ4_ERR_CUDA;
+    // otherwise the calls run one by one (same semantics, stream order)
+    for (const gq4::Call &c : built) GQ4_TRY(run(c, stream));
+    return GQ4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 gq4_status gq4_run_sequence(const gq4_call *calls, int n_calls, void *workspace, cudaStream_t stream)
 {
     if (n_calls < 0 || (n_calls > 0 && !calls)) return GQ4_ERR_INVALID_ARG;
     if (n_calls == 0) return GQ4_OK;
     if (!workspace) return GQ4_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return GQ4_ERR_MISALIGNED;
-    std::vector<gq4::Call> built((size_t)n_calls);
-    bool persistent = true;
-    for (int i = 0; i < n_calls; ++i) {
-        GQ4_TRY(build_seq_call(calls[i], built[(size_t)i]));
-        const gq4::Call &c = built[(size_t)i];
-        // the workspace is the launch's own scratch: no call may touch it
-        RangeSet rs;
-        rs.input(c.A, (size_t)c.K * sizeof(float));
-        for (int m = 0; m < c.nmat; ++m) {
-            rs.input(c.Bq[m], (size_t)c.N * (size_t)c.K / 2);
-            rs.input(c.scales[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
-            rs.input(c.zeros[m], (size_t)c.N * (size_t)(c.K / c.gs) * sizeof(float));
-        }
-        for (int j = 0; j < 4; ++j) rs.input(c.out[j], (size_t)c.seg_len[j] * sizeof(float));
-        if (c.norm) {
-            rs.input(c.norm->A_b, (size_t)c.K * sizeof(float));
-            rs.input(c.norm->W_norm, (size_t)c.K * sizeof(float));
-            rs.input(c.norm->residual_out, (size_t)c.K * sizeof(float));
-            rs.input(c.norm->norm_out, (size_t)c.K * sizeof(float));
-        }
-        rs.output(workspace, gq4::kSeqWorkspaceBytes);
-        if (!rs.disjoint()) return GQ4_ERR_ALIAS;
-        // the persistent kernel copies scale/zero rows in bulk (16-byte bases)
-        for (int m = 0; m < c.nmat; ++m)
-            if (!aligned(c.scales[m], 16) || !aligned(c.zeros[m], 16)) persistent = false;
-    }
-    if (persistent && gq4::sequence_plannable(built.data(), n_calls)) {
-        return gq4::launch_sequence(built.data(), n_calls, workspace, stream) == cudaSuccess ? GQ4_OK
-                                                                                            : GQ4_ERR_CUDA;
-    }
-    // otherwise the calls run one by one (same semantics, stream order)
-    for (int i = 0; i < n_calls; ++i) GQ4_TRY(run(built[(size_t)i], stream));
+    std::vector<gq4::Call> built;
+    bool persistent = false;
+    GQ4_TRY(prepare_sequence(calls, n_calls, workspace, built, persistent));
+    return run_prepared(built, persistent, workspace, stream);
+}
+
+gq4_status gq4_sequence_launches(const gq4_call *calls, int n_calls, int *launches)
+{
+    if (!launches || n_calls < 0 || (n_calls > 0 && !calls)) return GQ4_ERR_INVALID_ARG;
+    *launches = 0;
+    if (n_calls == 0) return GQ4_OK;
+    std::vector<gq4::Call> built;
+    bool persistent = false;
+    GQ4_TRY(prepare_sequence(calls, n_calls, nullptr, built, persistent));
+    if (persistent) *launches = (n_calls + gq4::kSeqMaxCalls - 1) / gq4::kSeqMaxCalls;
     return GQ4_OK;
 }
 
@@ -463,9 +505,14 @@ gq4_status gq4_run_sequence_static(const gq4_call *calls, int n_calls, cudaStrea
     if (need > gq4::seq_static_scratch_bytes()) return GQ4_ERR_INVALID_ARG;
     void *scratch = nullptr;
     if (gq4::seq_static_scratch(&scratch) != cudaSuccess) return GQ4_ERR_CUDA;
-    // what must start at zero: the barrier counters
-    if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return GQ4_ERR_CUDA;
-    return gq4_run_sequence(calls, n_calls, scratch, stream);
+    // every check runs before anything is enqueued
+    std::vector<gq4::Call> built;
+    bool persistent = false;
+    GQ4_TRY(prepare_sequence(calls, n_calls, scratch, built, persistent));
+    // what must start at zero (the barrier counters), only for the
+    // persistent launch that uses them
+    if (persistent && cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return GQ4_ERR_CUDA;
+    return run_prepared(built, persistent, scratch, stream);
 }
 
 gq4_status gq4_unpack(int K, int N, const uint32_t *Bq, uint8_t *q, cudaStream_t stream)

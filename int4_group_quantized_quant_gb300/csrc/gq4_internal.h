@@ -75,6 +75,7 @@ bool tc_rows_supported(const Call &call);
 // whether the calls fit its ring, and the launch (up to 128 calls per
 // launch).  The workspace holds the grid barrier's counter and generation.
 constexpr size_t kSeqWorkspaceBytes = 128;
+constexpr int kSeqMaxCalls = 128;  // calls per persistent launch
 bool sequence_plannable(const Call *calls, int n);
 cudaError_t launch_sequence(const Call *calls, int n, void *workspace, cudaStream_t stream);
 cudaError_t read_seq_device_error(unsigned int *bits, bool clear);

@@ -68,6 +68,7 @@ _SIGS = {
     "gq4_swiglu_gated_matvec": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "gq4_run_sequence": [ctypes.POINTER(Call), _i, _vp, _vp],
     "gq4_run_sequence_static": [ctypes.POINTER(Call), _i, _vp],
+    "gq4_sequence_launches": [ctypes.POINTER(Call), _i, ctypes.POINTER(_i)],
     "gq4_gemm": [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp],
     "gq4_quantize": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp],
     "gq4_from_mlx": [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
@@ -457,6 +458,14 @@ def run_sequence(calls, workspace, stream=None):
     arr = (Call * max(len(calls), 1))(*[c.desc for c in calls])
     _check(lib.gq4_run_sequence(arr, len(calls), _ptr(workspace), _stream(stream)),
            "gq4_run_sequence")
+
+
+def sequence_launches(calls) -> int:
+    """Persistent launches the calls would take (gq4_sequence_launches; 0 = run call by call)."""
+    arr = (Call * max(len(calls), 1))(*[c.desc for c in calls])
+    n = _i(0)
+    _check(lib.gq4_sequence_launches(arr, len(calls), ctypes.byref(n)), "gq4_sequence_launches")
+    return int(n.value)
 
 
 def run_sequence_static(calls, stream=None):

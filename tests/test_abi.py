@@ -281,6 +281,15 @@ def test_sequence_validation(gq4):
     alias = _seq_call(gq4, gq4.OP_MATVEC)
     alias.out[0] = alias.A
     assert _run_seq(gq4, [alias]) == gq4.ERR_ALIAS
+    # the plan query validates the same way and enqueues nothing
+    import ctypes
+    n = ctypes.c_int(-1)
+    arr = (gq4.Call * 1)(bad_shape)
+    assert gq4.lib.gq4_sequence_launches(arr, 1, ctypes.byref(n)) == gq4.ERR_INVALID_ARG
+    arr = (gq4.Call * 1)(alias)
+    assert gq4.lib.gq4_sequence_launches(arr, 1, ctypes.byref(n)) == gq4.ERR_ALIAS
+    assert gq4.lib.gq4_sequence_launches(None, 0, ctypes.byref(n)) == gq4.OK and n.value == 0
+    assert gq4.lib.gq4_sequence_launches(None, 0, None) == gq4.ERR_INVALID_ARG
 
 
 @no_gpu_only

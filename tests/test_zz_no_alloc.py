@@ -4,7 +4,11 @@ Two sequences in a row through the library's fixed scratch: a one-layer
 7B-shaped decode chain (quad QKV, O, gated gate/up with its norm prologue,
 down) and then the same chain again, each checked against the oracle on the
 inputs the GPU produced, and bit for bit against gq4_run_sequence with a
-caller workspace.
+caller workspace.  The library's plan query (gq4_sequence_launches) and,
+where the profiler lists kernels, the kernel names show that the
+persistent kernel (the one that uses the fixed scratch) ran; a chain of
+more calls than one launch takes shows the array carried from one launch
+to the next.
 """
 
 import numpy as np
@@ -79,4 +83,64 @@ def test_static_scratch_two_calls_in_a_row():
     gq4.run_sequence(calls, ws)
     torch.cuda.synchronize()
     assert np.array_equal(host(outs["hn"]).view(np.uint32), results[0].view(np.uint32))
+    assert gq4.device_error() == 0
+
+
+def _cuda_kernels(fn):
+    """Names of the CUDA kernels run by fn(), from the profiler."""
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = []
+    for e in prof.events():
+        if str(getattr(e, "device_type", "")).endswith("CUDA"):
+            names.append(e.name)
+    return names
+
+
+def test_static_scratch_runs_the_persistent_kernel():
+    gq4 = gq4_module()
+    gq4.device_error(clear=True)
+    calls, outs, w = _layer(gq4, 4096, 11008, (4096, 1024, 1024), 128, 1301)
+    # the library's plan: one persistent launch (the kernel that uses the scratch)
+    assert gq4.sequence_launches(calls) == 1
+    names = _cuda_kernels(lambda: gq4.run_sequence_static(calls))
+    if not names:
+        pytest.skip("the profiler lists no CUDA kernels in this process")
+    assert any("seq_kernel" in n for n in names), names
+    assert not any("stream_matvec_kernel" in n for n in names), names
+    _verify(outs, w, 128)
+    assert gq4.device_error() == 0
+
+
+def test_static_scratch_longer_than_one_launch():
+    """133 chained small matvecs, h_{i+1} = W_i h_i, twice in a row: the
+    second launch of each sequence reuses the array after the first one's
+    exit reset, and the second sequence after the first's."""
+    gq4 = gq4_module()
+    gq4.device_error(clear=True)
+    K, gs = 256, 64
+    h = dev(I.activations(1, K, 1302))
+    calls, chain = [], []
+    for i in range(133):
+        wi = I.quant_weights(K, K, gs, 1302, i, scale_range=(0.001, 0.004))
+        nxt = _nan(1, K)
+        calls.append(gq4.seq_matvec(h, *wdev(wi), gs, nxt))
+        chain.append((h, wi, nxt))
+        h = nxt
+    # two persistent launches, the second reusing the array after the first's reset
+    assert gq4.sequence_launches(calls) == 2
+    finals = []
+    for _ in range(2):
+        for _, _, C in chain:
+            C.fill_(float("nan"))
+        gq4.run_sequence_static(calls)
+        torch.cuda.synchronize()
+        for i in (0, 1, 127, 128, 132):
+            A, wi, C = chain[i]
+            ref, S = oracle.matvec(host(A), wi.Bq, wi.scales, wi.zeros, K, K, gs)
+            check_close(f"link {i}", host(C), ref, tol_fp32(S))
+        finals.append(host(chain[-1][2]).copy())
+    assert np.array_equal(finals[0].view(np.uint32), finals[1].view(np.uint32))
     assert gq4.device_error() == 0
