@@ -87,5 +87,5 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
 
 if __name__ == "__main__":
-    flags = [a for a in sys.argv[1:] if a.startswith("-X") or a.startswith("--")]
+    flags = [a for a in sys.argv[1:] if a.startswith(("-X", "--", "-D"))]
     print(build(force=True, verbose=True, extra_flags=flags))

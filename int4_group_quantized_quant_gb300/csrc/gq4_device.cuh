@@ -154,32 +154,6 @@ __device__ __forceinline__ int chunk_group(int gc, unsigned long long magic)
     return (int)(((unsigned long long)gc * magic) >> 40);
 }
 
-// Per (column, group) zero-point constants.  The integer part of the zero
-// is folded into the magic offset, exactly: with zi = round(clamp(z, 0, 15)),
-//   f - (2^23 + 16^p zi) = 16^p (q - zi)          (an exact small integer),
-// and the fractional part dz = zi - z multiplies the chunk's activation sum:
-//   sum_k a_k (q_k - z) = sum_k a_k (q_k - zi) + dz * sum_k a_k.
-// When the zero is an integer in 0..15 (as for codes equal to their zero),
-// dz is exactly 0 and so is the correction.
-struct ZeroFold {
-    f32x2 nc01, nc23;  // -(2^23 + 16^p zi) for p = 0, 1 and p = 2, 3
-    float dz;
-};
-
-__device__ __forceinline__ ZeroFold fold_zero(float z)
-{
-    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
-    const float rz = zc + kMagic;  // 2^23 + round(zc)
-    const uint32_t rb = __float_as_uint(rz);
-    const uint32_t zi = rb - kMagicBits;
-    const uint32_t nb = rb | 0x80000000u;  // bits of -(2^23 + zi)
-    ZeroFold f;
-    f.nc01 = pack2(__uint_as_float(nb), __uint_as_float(nb + zi * 15u));
-    f.nc23 = pack2(__uint_as_float(nb + zi * 255u), __uint_as_float(nb + zi * 4095u));
-    f.dz = (rz - kMagic) - z;
-    return f;
-}
-
 // Shared-memory slot of activation float4 j (0..7) of chunk t: chunk groups
 // of R chunks are XOR-swizzled so that 32 lanes reading 32 consecutive
 // groups hit distinct banks.
@@ -190,103 +164,114 @@ __device__ __forceinline__ int act_index(int t, int j)
 }
 
 // ---------------------------------------------------------------------------
-// One-lane path: fp16 code pairs.  A LOP3 places two codes of a word as the
-// low mantissa bits of the two halves of an fp16 pair whose exponent is that
-// of 1024 (bits 0x6400 per half):
+// One-lane path, integer form.  The activations of a chunk group (R
+// consecutive 32-code chunks inside one scale group) are written as 24-bit
+// fixed-point integers with the group's own power-of-two scale:
 //
-//     halves = 0x64006400 | (x & (0x000F000F << 4p))  =>  1024 + 16^p q, p in {0, 1}
+//     X_k = rint(a_k * 2^(22 - E)),   2^(E-1) <= max_k |a_k| < 2^E,
 //
-// (exact: 16^p q <= 240 stays inside the 10-bit mantissa).  With t = w >> 8
-// the four masks give the pairs (0,4) (1,5) (2,6) (3,7) of a word, codes
-// 0, 2, 4, 6 at p = 0 and 1, 3, 5, 7 at p = 1: five ALU operations per word
-// instead of nine.  One mixed-precision add (PTX `add.rn.f32.f16`, sm_100
-// and later) then widens a half to f32 and adds -(1024 + 16^p zi) in one
-// rounding, which is exact: the result 16^p (q - zi) is a small integer.
-// The activation that multiplies the code is pre-scaled by 16^-p, so the
-// packed FMA forms a * (q - zi) exactly before its single rounding, the same
-// arithmetic as the f32 magic form above with half the logic operations.
+// so |X_k| <= 2^22 and |X_k * 2^(E-22) - a_k| <= 2^(E-23) <= max_k |a_k| * 2^-22.
+// Each X_k splits exactly into three bytes, X = 65536 B2 + 256 B1 + B0 with
+// B2 in [-64, 64] (signed) and B1, B0 in [0, 255] (the two's-complement
+// bytes of X).  The dot product of a column's codes with one byte piece is
+// then an exact integer sum, four products per dp4a instruction (PTX dp4a,
+// byte lanes multiplied pairwise and added to a 32-bit accumulator):
+//
+//     even = w & 0x0F0F0F0F   bytes (q0, q2, q4, q6)
+//     odd  = w - even         bytes (16 q1, 16 q3, 16 q5, 16 q7)
+//
+// against activation words holding the matching bytes of (k0, k2, k4, k6)
+// and (k1, k3, k5, k7).  Per word: one logic operation, one integer add and
+// six dp4a for the three pieces.  With T_p = sum_k (q_k - zi) B_p,k (exact:
+// the integer zero point comes off through the group's piece sums),
+//
+//     sum_k a_k (q_k - z) ~= 2^(E-22) (65536 T2 + 256 T1 + T0) + (zi - z) sum_k a_k.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kHalfMagicBits = 0x64006400u;
-
-// Per (column, group) zero-point constants of the fp16 form: the integer
-// part zi = round(clamp(z, 0, 15)) goes into the widening adds, the
-// fractional part dz = zi - z multiplies the chunk group's activation sum
-// (sum_k a_k (q_k - z) = sum_k a_k (q_k - zi) + dz * sum_k a_k).  An integer
-// zero point in 0..15 gives dz = 0 exactly.
-struct HalfZero {
-    float nz0;  // -(1024 + zi)       (codes at p = 0)
-    float nz1;  // -(1024 + 16 zi)    (codes at p = 1)
-    float dz;
-};
-
-__device__ __forceinline__ HalfZero half_zero(float z)
+__device__ __forceinline__ int dp4a_s8u8(uint32_t a_s8x4, uint32_t b_u8x4, int c)
 {
-    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
-    const float zi = __fsub_rn(__fadd_rn(zc, kMagic), kMagic);  // round to nearest integer
-    HalfZero h;
-    h.nz0 = -1024.0f - zi;
-    h.nz1 = fmaf(-16.0f, zi, -1024.0f);
-    h.dz = zi - z;
-    return h;
-}
-
-// f32(low / high half of x, as fp16) + c, one rounding.
-__device__ __forceinline__ float widen_add_lo(uint32_t x, float c)
-{
-    float r;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, l, %2;\n\t}"
-        : "=f"(r) : "r"(x), "f"(c));
-    return r;
-}
-
-__device__ __forceinline__ float widen_add_hi(uint32_t x, float c)
-{
-    float r;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.f16 %0, h, %2;\n\t}"
-        : "=f"(r) : "r"(x), "f"(c));
-    return r;
-}
-
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t masked_magic_bits(uint32_t x, uint32_t magic)
-{
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(MASK), "r"(magic));
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_s8x4), "r"(b_u8x4), "r"(c));
     return d;
 }
 
-// acc += the eight products of one word with its activations.  `lo` holds
-// the activations of codes (0, 4, 1, 5) and `hi` those of (2, 6, 3, 7), the
-// ones of codes 1, 3, 5, 7 pre-scaled by 1/16 (see pair_activations).
-// `magic` is kHalfMagicBits, passed in from a kernel parameter.
-__device__ __forceinline__ f32x2 word_dot(uint32_t w, ulonglong2 lo, ulonglong2 hi, const HalfZero &z,
-                                          uint32_t magic, f32x2 acc)
+__device__ __forceinline__ int dp4a_u8u8(uint32_t a_u8x4, uint32_t b_u8x4, int c)
 {
-    const uint32_t t = w >> 8;
-    const uint32_t h04 = masked_magic_bits<0x000F000Fu>(w, magic);
-    const uint32_t h15 = masked_magic_bits<0x00F000F0u>(w, magic);
-    const uint32_t h26 = masked_magic_bits<0x000F000Fu>(t, magic);
-    const uint32_t h37 = masked_magic_bits<0x00F000F0u>(t, magic);
-    acc = fma2(lo.x, pack2(widen_add_lo(h04, z.nz0), widen_add_hi(h04, z.nz0)), acc);
-    acc = fma2(lo.y, pack2(widen_add_lo(h15, z.nz1), widen_add_hi(h15, z.nz1)), acc);
-    acc = fma2(hi.x, pack2(widen_add_lo(h26, z.nz0), widen_add_hi(h26, z.nz0)), acc);
-    acc = fma2(hi.y, pack2(widen_add_lo(h37, z.nz1), widen_add_hi(h37, z.nz1)), acc);
-    return acc;
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_u8x4), "r"(b_u8x4), "r"(c));
+    return d;
 }
 
-// The eight activations a0..a7 of one word (x0 = a0..a3, x1 = a4..a7) in
-// the order word_dot reads them, pre-scaled: (a0, a4, a1/16, a5/16) and
-// (a2, a6, a3/16, a7/16).
-__device__ __forceinline__ void pair_activations(float4 x0, float4 x1, float4 &lo, float4 &hi)
+// Integer accumulators of one weight stream over a chunk group, piece p
+// (p = 0, 1, 2 for B2, B1, B0): e[p] starts at -zi * sum_k B_p,k and adds
+// q * B_p over the even codes; o[p] starts at kI8Magic and adds 16 q * B_p
+// over the odd codes.
+struct I8Acc {
+    int e[3];
+    int o[3];
+};
+
+// Start value of the odd accumulators: the bits of the float 1.5 * 2^23, so
+// that 16 e + o is directly the bit pattern of 1.5 * 2^23 + 16 T (exact for
+// |16 T| < 2^22) and one float subtraction recovers 16 T.
+constexpr int kI8Magic = 0x4B400000;
+constexpr float kI8MagicF = 12582912.0f;  // 1.5 * 2^23
+
+// acc += the eight codes of word w against the activation bytes of its
+// even (ae[p]) and odd (ao[p]) codes, pieces p = 2, 1, 0 in slots 0, 1, 2.
+// `mask` is 0x0F0F0F0F from a kernel parameter.
+__device__ __forceinline__ void word_dot_i8(uint32_t w, uint32_t mask, uint32_t ae2, uint32_t ao2,
+                                            uint32_t ae1, uint32_t ao1, uint32_t ae0, uint32_t ao0,
+                                            I8Acc &acc)
 {
-    lo = make_float4(x0.x, x1.x, x0.y * 0.0625f, x1.y * 0.0625f);
-    hi = make_float4(x0.z, x1.z, x0.w * 0.0625f, x1.w * 0.0625f);
+    const uint32_t ev = w & mask;
+    const uint32_t od = w - ev;
+    acc.e[0] = dp4a_s8u8(ae2, ev, acc.e[0]);
+    acc.o[0] = dp4a_s8u8(ao2, od, acc.o[0]);
+    acc.e[1] = dp4a_u8u8(ae1, ev, acc.e[1]);
+    acc.o[1] = dp4a_u8u8(ao1, od, acc.o[1]);
+    acc.e[2] = dp4a_u8u8(ae0, ev, acc.e[2]);
+    acc.o[2] = dp4a_u8u8(ao0, od, acc.o[2]);
 }
 
-// Sum of the unscaled activations held by one paired float4.
-__device__ __forceinline__ float paired_sum(float4 v)
+// Integer part zi = round(clamp(z, 0, 15)) of a zero point, as an integer
+// and as the float fractional correction dz = zi - z.
+struct IntZero {
+    int zi;
+    float dz;
+};
+
+__device__ __forceinline__ IntZero int_zero(float z)
 {
-    return (v.x + v.y) + 16.0f * (v.z + v.w);
+    const float zc = fminf(fmaxf(z, 0.0f), 15.0f);
+    const float r = __fadd_rn(zc, kMagic);  // 2^23 + round(zc), exact
+    IntZero iz;
+    iz.zi = (int)(__float_as_uint(r) - kMagicBits);
+    iz.dz = __fsub_rn(r, kMagic) - z;
+    return iz;
+}
+
+// Accumulators of one stream at the start of a chunk group: the integer
+// zero point comes off through the piece sums sB[p] = sum_k B_p,k of the
+// group's activations (16 e + o then carries 16 sum_k (q_k - zi) B_p,k).
+__device__ __forceinline__ void int_group_init(I8Acc &acc, int zi, const int (&sB)[3])
+{
+#pragma unroll
+    for (int p = 0; p < 3; ++p) {
+        acc.e[p] = -zi * sB[p];
+        acc.o[p] = kI8Magic;
+    }
+}
+
+// sum_k a_k (q_k - z) of one stream over a chunk group: `fac16` = 2^(E-22)/16,
+// `asum` = sum_k a_k (f32), dz = zi - z.
+__device__ __forceinline__ float int_group_value(const I8Acc &acc, float fac16, float dz, float asum)
+{
+    float f[3];
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+        f[p] = __int_as_float(acc.e[p] * 16 + acc.o[p]) - kI8MagicF;  // 16 T_p, exact
+    const float t = fmaf(fmaf(f[0], 256.0f, f[1]), 256.0f, f[2]);  // 16 (65536 T2 + 256 T1 + T0)
+    return fmaf(fac16, t, dz * asum);
 }
 
 }  // namespace gq4

@@ -22,11 +22,12 @@
 //     before staging call i+1's activations, which may be call i's outputs.  Activations are read through L2 (ld.global.cg),
 //     never from a possibly stale L1 line.
 //   * Within a call the arithmetic is the one-lane streaming kernel's
-//     (gq4_onelane.cuh): the activations staged once per CTA, paired,
-//     pre-scaled and swizzled; warp slots of four columns (or two gate and
-//     two up columns); fp16-pair unpack with the zero's integer part taken
-//     out in one exact widening add and its fractional part applied through
-//     chunk-group activation sums; one xor reduce-scatter per slot.
+//     (gq4_onelane.cuh): the activations staged once per CTA as 24-bit
+//     fixed-point byte pieces with a power-of-two scale per chunk group;
+//     warp slots of four columns (or two gate and two up columns); integer
+//     dp4a sums per chunk group with the zero's integer part taken out
+//     exactly and its fractional part applied through the group's
+//     activation sum; one xor reduce-scatter per slot.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -47,12 +48,12 @@ __device__ unsigned int g_seq_error = 0;
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kActBatch = 2;  // activation float4 per consumer thread per prologue batch (register budget: the kernel holds every call variant)
+constexpr int kActBatch = 4;  // activation float4 per consumer thread per prologue batch (register budget: the kernel holds every call variant)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kCT = kConsumerWarps * 32;
 constexpr int kSPW = 4;          // weight streams per warp slot
 constexpr int kMaxStages = 16;
-constexpr int kMaxCalls = 128;   // calls per launch (kernel-parameter space)
+constexpr int kMaxCalls = kSeqMaxCalls;  // calls per launch (kernel-parameter space)
 constexpr uint32_t kSmemLimit = 220u * 1024u;
 constexpr uint32_t kStageMin = 16u * 1024u;
 
@@ -97,8 +98,8 @@ struct SeqParams {
     int n_calls;
     int S;                    // ring depth
     uint32_t stage_bytes;
-    uint32_t off_act, off_asum, off_norm, off_bar;
-    uint32_t magic_bits;      // kHalfMagicBits, read from the parameter bank
+    uint32_t off_act, off_norm, off_bar;
+    uint32_t magic_bits;      // 0x0F0F0F0F (even-code mask), read from the parameter bank
     unsigned int *bar_count;  // grid barrier: arrivals so far in this launch
     unsigned int *bar_exit;   // CTAs that have finished this launch
     SeqCall calls[kMaxCalls];
@@ -197,8 +198,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int ctid = threadIdx.x;
-    float4 *s_act = reinterpret_cast<float4 *>(smem + p.off_act);
-    float *s_asum = reinterpret_cast<float *>(smem + p.off_asum);
+    uint4 *s_act = reinterpret_cast<uint4 *>(smem + p.off_act);
     float *s_norm = reinterpret_cast<float *>(smem + p.off_norm);
     int col_begin, col_end;
     cta_columns(c, col_begin, col_end);
@@ -207,13 +207,14 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
 
     // ---- prologue: activations (through L2: earlier calls may have written
     // them) ----
-    stage_activations<R, NORM ? kProNorm : kProNone, kCT, kActBatch, LoadL2>(c.K, c.A, c.A_b, c.W_norm, c.eps, c.residual_out,
-                                                       c.norm_out, blockIdx.x == 0, s_act, s_asum, s_norm,
-                                                       ctid, 1);
+    // inv: the norm prologue's inverse RMS, applied to each finished dot product
+    const float inv = stage_activations_i8<R, NORM ? kProNorm : kProNone, kCT, kActBatch, LoadL2>(
+        c.K, c.A, c.A_b, c.W_norm, c.eps, c.residual_out, blockIdx.x == 0, s_act, s_norm, ctid, 1);
     if (first_call && ctid == 0) mbar_arrive(sh.ready);
 
     // ---- warp slots ----
-    const uint32_t magic = p.magic_bits;
+    const uint32_t mask = p.magic_bits;
+    const int swap = chunk_swap<R>(lane);
     for (int i = warp; i < n_slots; i += kConsumerWarps) {
         const int stage = i / c.wps;
         const int sub = i - stage * c.wps;
@@ -251,8 +252,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
         // One chunk group (R chunks) of all kSPW streams.
         auto group_dot = [&](int jg, const uint4 (&wq)[kSPW][R]) {
             const int grp = chunk_group(jg * R, c.group_magic);
-            float sc[kSPW];
-            HalfZero hz[kSPW];
+            float sc[kSPW], zz[kSPW];
 #pragma unroll
             for (int q = 0; q < kSPW; ++q) {
                 const int mat = NMAT == 2 ? (q / CPS) : 0;
@@ -260,9 +260,9 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
                 lc = lc < nc ? lc : 0;
                 const int si = (sc0 + lc) * c.G + grp;
                 sc[q] = srow[mat][si];
-                hz[q] = half_zero(zrow[mat][si]);
+                zz[q] = zrow[mat][si];
             }
-            chunk_group_dot<kSPW, R>(s_act, jg, s_asum[jg], wq, sc, hz, magic, acc);
+            chunk_group_dot_i8<kSPW, R>(s_act, jg, swap, wq, sc, zz, mask, acc);
         };
 
         if (!failed) {
@@ -272,7 +272,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
                 for (int q = 0; q < kSPW; ++q) {
                     const uint4 *w = slot_words(q);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + r];
+                    for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + (r ^ swap)];
                 }
                 group_dot(jg, wq);
             }
@@ -306,6 +306,7 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
         for (int off = 4; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
         // lane 0 -> stream 0, lane 8 -> 1, lane 16 -> 2, lane 24 -> 3
         const int q_of_lane = ((lane >> 4) << 1) | ((lane >> 3) & 1);
+        if constexpr (NORM) total *= inv;
         if (failed) total = __int_as_float(0x7fffffff);
 
         // ---- epilogue ----
@@ -335,6 +336,10 @@ __device__ __forceinline__ void consume_call(const SeqParams &p, const SeqCall &
                 }
             }
         }
+    }
+    if constexpr (NORM) {
+        if (blockIdx.x == 0 && c.norm_out)
+            write_norm_out<kCT, LoadL2>(c.K, c.A, c.A_b, c.W_norm, inv, c.norm_out, ctid);
     }
 }
 
@@ -551,14 +556,13 @@ bool plan_sequence(const Call *calls, int n, SeqParams &prm, size_t &smem)
     // any call (at least kStageMin), so that long columns (one slot per
     // entry) get as many entries in flight as shared memory allows
     uint32_t sb = kStageMin;
-    int kc_max = 0, kp_max = 0;
+    int kc_max = 0;
     for (int i = 0; i < n; ++i) {
         SeqCall &sc = prm.calls[i];
         plan_call_shape(calls[i], sc);
         const uint32_t one = entry_bytes(sc, slot_step(sc));
         sb = one > sb ? one : sb;
         kc_max = sc.KC > kc_max ? sc.KC : kc_max;
-        kp_max = sc.KP > kp_max ? sc.KP : kp_max;
     }
     sb = rup(sb, 128u);
     for (int i = 0; i < n; ++i) {
@@ -572,19 +576,17 @@ bool plan_sequence(const Call *calls, int n, SeqParams &prm, size_t &smem)
         sc.mat_sz = rup((uint32_t)sc.stage_cols * (uint32_t)sc.G * 4u, 16u);
     }
     const uint32_t act = rup((uint32_t)kc_max * 128u, 128u);
-    const uint32_t asum = rup((uint32_t)kp_max * 4u, 128u);
     const uint32_t bars = rup((2 * kMaxStages + 1) * 8u + 2 * kMaxStages * 4u, 128u);
-    const uint32_t fixed = act + asum + 128u + bars;
+    const uint32_t fixed = act + 128u + bars;
     if (fixed + 2u * sb > kSmemLimit) return false;
     int S = (int)((kSmemLimit - fixed) / sb);
     if (S > kMaxStages) S = kMaxStages;
     prm.S = S;
     prm.stage_bytes = sb;
     prm.off_act = rup((uint32_t)S * sb, 128u);
-    prm.off_asum = prm.off_act + act;
-    prm.off_norm = prm.off_asum + asum;
+    prm.off_norm = prm.off_act + act;
     prm.off_bar = prm.off_norm + 128u;
-    prm.magic_bits = kHalfMagicBits;
+    prm.magic_bits = 0x0F0F0F0Fu;
     smem = prm.off_bar + bars;
     return true;
 }

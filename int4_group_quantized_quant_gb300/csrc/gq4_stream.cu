@@ -24,16 +24,18 @@
 //     slot (lane l owns 32-code chunk groups l, l+32, ...) and reduces it
 //     once with an xor reduce-scatter.  No cross-warp reduction, no group
 //     barriers in the steady state.
-//   * Activations are staged once per CTA in shared memory, paired and
-//     pre-scaled for the fp16-pair unpack and XOR-swizzled so that a warp's
+//   * Activations are staged once per CTA in shared memory as 24-bit
+//     fixed-point byte pieces with a power-of-two scale per chunk group,
+//     arranged per packed word for dp4a and XOR-swizzled so that a warp's
 //     128-bit loads are conflict-free (gq4_onelane.cuh); every activation
-//     load serves all SPW streams.  The RMSNorm prologue (x = A + A_b,
-//     inverse RMS, gain) is applied while staging, together with each chunk
-//     group's activation sum.
-//   * Codes are unpacked two per logic operation as fp16 pairs and widened
-//     with the integer part of the zero point subtracted in one exact add;
-//     the fractional part is applied once per chunk group through the
-//     activation sum (see gq4_device.cuh).
+//     load serves all SPW streams.  The RMSNorm prologue stages x * W_norm
+//     (x = A + A_b) and returns the inverse RMS, applied once to each
+//     finished dot product.
+//   * Per word, one logic operation and one add split the codes into even
+//     and odd byte lanes and six dp4a accumulate them against the three
+//     activation pieces, exactly in integers; per chunk group the integer
+//     part of the zero point comes off through the piece sums and the
+//     fractional part through the activation sum (see gq4_device.cuh).
 //   * Every mbarrier wait is bounded in time; on expiry the kernel records
 //     an error in a device word (gq4_device_error) and leaves.
 #include <atomic>
@@ -71,9 +73,9 @@ struct StreamParams {
     uint32_t stage_bytes;
     uint32_t off_w[2];              // within a stage
     uint32_t off_s[2], off_z[2];    // scale/zero rows of the CTA's range
-    uint32_t off_act, off_asum, off_norm, off_bar;
+    uint32_t off_act, off_norm, off_bar;
     unsigned long long group_magic;
-    uint32_t magic_bits;  // kHalfMagicBits, read from the parameter bank
+    uint32_t magic_bits;  // 0x0F0F0F0F (even-code mask), read from the parameter bank
     const float *A;
     const float *A_b;
     const float *W_norm;
@@ -132,8 +134,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // and only then for the barrier phase: a parity wait alone could match the
     // phase two steps back while the previous occupant is still landing.
     int *s_seq = reinterpret_cast<int *>(srows + 1);
-    float4 *s_act = reinterpret_cast<float4 *>(smem + p.off_act);
-    float *s_asum = reinterpret_cast<float *>(smem + p.off_asum);
+    uint4 *s_act = reinterpret_cast<uint4 *>(smem + p.off_act);
     float *s_norm = reinterpret_cast<float *>(smem + p.off_norm);
 
     constexpr int CPS = NMAT == 2 ? SPW / 2 : SPW;  // columns per warp slot (per matrix)
@@ -241,9 +242,9 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // grid to complete (its writes visible).  The producer does not wait: the
     // weights do not depend on it, so they stream in meanwhile.
     grid_dependency_wait();
-    stage_activations<R, PRO, kCT, kActBatch, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, p.eps,
-                                                             p.residual_out, p.norm_out, blockIdx.x == 0,
-                                                             s_act, s_asum, s_norm, ctid, 1);
+    // inv: the norm prologue's inverse RMS, applied to each finished dot product
+    const float inv = stage_activations_i8<R, PRO, kCT, kActBatch, LoadReadOnly>(
+        p.K, p.A, p.A_b, p.W_norm, p.eps, p.residual_out, blockIdx.x == 0, s_act, s_norm, ctid, 1);
     named_barrier(2, kThreads);  // the producer has initialised the mbarriers
     if (ctid == 0) mbar_arrive(ready);
 
@@ -254,7 +255,8 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
     // outputs become NaN) but still releases its stages.
     bool failed = !mbar_wait(srows, 0);
     if (failed) record_error(1u);
-    const uint32_t magic = p.magic_bits;
+    const uint32_t mask = p.magic_bits;
+    const int swap = chunk_swap<R>(lane);
     const float *srow[NMAT];
     const float *zrow[NMAT];
 #pragma unroll
@@ -298,8 +300,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
         // One chunk group (R chunks) of all SPW streams.
         auto group_dot = [&](int jg, const uint4 (&wq)[SPW][R]) {
             const int grp = chunk_group(jg * R, p.group_magic);
-            float sc[SPW];
-            HalfZero hz[SPW];
+            float sc[SPW], zz[SPW];
 #pragma unroll
             for (int q = 0; q < SPW; ++q) {
                 const int mat = NMAT == 2 ? (q / CPS) : 0;
@@ -307,9 +308,9 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
                 lc = lc < nc ? lc : 0;
                 const int si = (lc0 + lc) * p.G + grp;
                 sc[q] = srow[mat][si];
-                hz[q] = half_zero(zrow[mat][si]);
+                zz[q] = zrow[mat][si];
             }
-            chunk_group_dot<SPW, R>(s_act, jg, s_asum[jg], wq, sc, hz, magic, acc);
+            chunk_group_dot_i8<SPW, R>(s_act, jg, swap, wq, sc, zz, mask, acc);
         };
 
         if (!failed) {
@@ -319,7 +320,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
                 for (int q = 0; q < SPW; ++q) {
                     const uint4 *w = slot_words(q);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + r];
+                    for (int r = 0; r < R; ++r) wq[q][r] = w[jg * R + (r ^ swap)];
                 }
                 group_dot(jg, wq);
             }
@@ -357,6 +358,7 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
             for (int off = 8; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
             q_of_lane = lane >> 4;  // lane 0 -> stream 0, lane 16 -> stream 1
         }
+        if constexpr (PRO == kProNorm) total *= inv;
         if (failed) total = __int_as_float(0x7fffffff);
 
         // ---- epilogue ----
@@ -394,6 +396,10 @@ stream_matvec_kernel(const __grid_constant__ StreamParams p)
                 }
             }
         }
+    }
+    if constexpr (PRO == kProNorm) {
+        if (blockIdx.x == 0 && p.norm_out)
+            write_norm_out<kCT, LoadReadOnly>(p.K, p.A, p.A_b, p.W_norm, inv, p.norm_out, ctid);
     }
 }
 
@@ -465,16 +471,16 @@ bool plan_stream(const Call &call, StreamParams &prm, int &R, int &spw, size_t &
     // Measured on the 11008-long down projection: 13.6 -> 10.2 us.
     const bool long_cols = call.K > 8192;
     // two consecutive chunks per chunk group when a scale group spans them
-    R = (!long_cols && call.gs >= 64 && prm.KC % 2 == 0) ? 2 : 1;
+    // (the integer sums of a chunk group stay exact up to 64 codes)
+    R = (call.gs >= 64 && prm.KC % 2 == 0) ? 2 : 1;
     prm.KP = prm.KC / R;
     prm.unit = 4 / gcd_int(prm.G, 4);
     prm.n_units = (call.N + prm.unit - 1) / prm.unit;
     if (grid > prm.n_units) grid = prm.n_units;
     prm.max_cols = ((prm.n_units + grid - 1) / grid) * prm.unit;
     const uint32_t act_bytes = round_up((uint32_t)prm.KC * 128u, 128u);
-    const uint32_t asum_bytes = round_up((uint32_t)prm.KP * 4u, 128u);
     const uint32_t rows_bytes = round_up((uint32_t)prm.max_cols * prm.G * 4u, 128u);
-    const uint32_t fixed = act_bytes + asum_bytes + 2u * call.nmat * rows_bytes + 128u +
+    const uint32_t fixed = act_bytes + 2u * call.nmat * rows_bytes + 128u +
                            (2 * kMaxStages + 2) * 8u + kMaxStages * 4u;
     const int spw_first = long_cols ? 2 : 4, spw_last = 2;
     // stage size cap (gate/up pairs: 24 KB, measured 16.1 -> 15.4 us on
@@ -506,8 +512,7 @@ bool plan_stream(const Call &call, StreamParams &prm, int &R, int &spw, size_t &
                 off += rows_bytes;
             }
             prm.off_act = off;
-            prm.off_asum = prm.off_act + act_bytes;
-            prm.off_norm = prm.off_asum + asum_bytes;
+            prm.off_norm = prm.off_act + act_bytes;
             prm.off_bar = prm.off_norm + 128u;
             smem = prm.off_bar + (2 * kMaxStages + 2) * sizeof(uint64_t) + kMaxStages * sizeof(int);
             return smem <= kSmemLimit + 4096u;
@@ -549,7 +554,7 @@ cudaError_t launch_stream(const Call &call, cudaStream_t stream)
     if (sms <= 0 || !plan_stream(call, prm, R, spw, smem, sms)) return cudaErrorInvalidValue;
     const unsigned long long cpgrp = (unsigned long long)(call.gs / 32);
     prm.group_magic = ((1ull << 40) + cpgrp - 1) / cpgrp;
-    prm.magic_bits = kHalfMagicBits;
+    prm.magic_bits = 0x0F0F0F0Fu;
     prm.A = call.A;
     if (call.norm) {
         prm.A_b = call.norm->A_b;

@@ -90,13 +90,6 @@ __device__ __forceinline__ bool wait_shared_eq(const int *p, int want)
     }
 }
 
-// Hint: fetch `bytes` (multiple of 16, 16-byte aligned) of global memory into
-// L2 (no completion tracking, no shared memory).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
-}
-
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
