@@ -71,6 +71,17 @@ def step_bytes(M, layers):
     return layers * sum(layer_call_bytes(M).values())
 
 
+def stack_config(layers, M, world):
+    """The bench line's `config` (the same for both arms)."""
+    return {
+        "workload": f"7B-shaped decode layer stack, {layers} layers, int4 group 128, M={M}",
+        "lanes": M, "layers": layers, "hidden": HIDDEN, "ffn": FFN, "qkv": list(QKV),
+        "group_size": GS, "bytes_per_step": step_bytes(M, layers),
+        "l2": "inputs larger than L2: each step streams 3.2 GB of weights (L2 129 MB)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 # ---------------------------------------------------------------------------
 # Distributed helpers (replicas: each rank runs its own stack)
 # ---------------------------------------------------------------------------
@@ -235,23 +246,30 @@ def profiled_traffic(kernel_tag: str):
 # The device-resident stack
 # ---------------------------------------------------------------------------
 
+def to_device(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    return torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).cuda()
+
+
 class Stack:
-    def __init__(self, gq4, layers: int, M: int, seed: int = 4):
+    def __init__(self, gq4, layers: int, M: int, seed: int = 4, weights=None):
+        """The stack at M lanes; `weights` (another Stack's .layers) shares the
+        device-resident weights instead of uploading them again."""
         import torch
         from int4_group_quantized_quant_gb300 import inputs as I
         self.gq4 = gq4
         self.M = M
-        self.layers = []
         dev = torch.device("cuda")
-
-        def up(a):
-            a = np.ascontiguousarray(a)
-            return torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a).to(dev)
-
-        for li in range(layers):
-            L = I.stack_layer(li, seed)
-            self.layers.append({k: (up(v.Bq), up(v.scales), up(v.zeros)) if k != "W_norm" else up(v)
-                                for k, v in L.items()})
+        up = to_device
+        if weights is not None:
+            self.layers = weights
+        else:
+            self.layers = []
+            for li in range(layers):
+                L = I.stack_layer(li, seed)
+                self.layers.append({k: (up(v.Bq), up(v.scales), up(v.zeros)) if k != "W_norm" else up(v)
+                                    for k, v in L.items()})
         f32 = dict(dtype=torch.float32, device=dev)
         nq = sum(QKV)
         self.h0 = up(I.stack_input(M, seed))
@@ -301,6 +319,281 @@ class Stack:
             self.layer(li, h, h_next, stream)
             h = h_next
         return h
+
+
+# ---------------------------------------------------------------------------
+# Per-config lines: configs 0-3 at their stated shapes, the stack at more
+# lanes, the prefill GEMM, and the sequence kernel against the graph of calls
+# ---------------------------------------------------------------------------
+
+def lane_path(M):
+    """(kernel description, profile tag prefix) of the path an M-lane call takes."""
+    if M == 1:
+        return "one-lane streaming kernel, CUDA cores", "M1"
+    if M < 16:
+        return "multi-lane fp32 kernel, CUDA cores", f"M{M}"
+    return "tensor-core kernel (tcgen05, bf16 operands, f32 accumulate)", f"M{M}"
+
+
+def graph_time_us(body, steps, warmup, stream):
+    """µs per replay of a CUDA graph of body(stream), CUDA events on the replay stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            body(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / steps
+    del g
+    return us
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(fn_cols, N, reps=3):
+    """(median µs single-threaded, median µs on all host cores, cores) of an
+    oracle call split by columns: fn_cols(c0, c1) runs the oracle on columns
+    [c0, c1).  The C oracle releases the GIL, so threads run it in parallel;
+    the oracle itself is unchanged (each column's sum is still sequential)."""
+    from concurrent.futures import ThreadPoolExecutor
+    cores = host_cores()
+    one = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn_cols(0, N)
+        one.append(time.perf_counter() - t0)
+    bounds = [N * i // cores for i in range(cores + 1)]
+    parts = [(bounds[i], bounds[i + 1]) for i in range(cores) if bounds[i + 1] > bounds[i]]
+    par = []
+    with ThreadPoolExecutor(max_workers=len(parts)) as pool:
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            list(pool.map(lambda b: fn_cols(*b), parts))
+            par.append(time.perf_counter() - t0)
+    return statistics.median(one) * 1e6, statistics.median(par) * 1e6, len(parts)
+
+
+def config_cases(gq4):
+    """Configs 0-3 at their stated shapes and distributions: for each, a
+    description, the algorithmic bytes of one call, the bytes of one weight
+    set, a device-call maker over rotating weight sets, and the oracle over
+    a column range."""
+    import torch
+    from int4_group_quantized_quant_gb300 import inputs as I
+    cases = []
+
+    def dev_w(w):
+        return (to_device(w.Bq), to_device(w.scales), to_device(w.zeros))
+
+    def mat_bytes(K, N, gs):
+        return K * N // 2 + 8 * N * (K // gs)
+
+    def wslice(w, c0, c1):
+        return w.Bq[c0:c1], w.scales[c0:c1], w.zeros[c0:c1]
+
+    # config 0: single matvec 1024 x 1024, gs 32
+    d = I.single_matvec()
+    K, N, gs = d["K"], d["N"], d["gs"]
+    A, C = to_device(d["A"]), torch.empty((1, N), dtype=torch.float32, device="cuda")
+    cases.append(dict(
+        name="c0", workload=f"single int4 matvec M=1, K={K}, N={N}, group_size={gs}",
+        call_bytes=mat_bytes(K, N, gs) + 4 * K + 4 * N, set_bytes=mat_bytes(K, N, gs),
+        w0=dev_w(d["w"]), N=N,
+        call=lambda W, s, A=A, C=C, gs=gs: gq4.matvec(A, *W, gs, C=C, stream=s),
+        oracle=lambda orc, c0, c1, d=d: orc.matvec(d["A"], *wslice(d["w"], c0, c1), d["K"], c1 - c0,
+                                                   d["gs"])))
+
+    # config 1: quad QKV 2560 -> 10240 split 4096/5120/6144, gs 64
+    d = I.quad_qkv()
+    K, N, gs, n0, n1, n2 = d["K"], d["N"], d["gs"], d["n0"], d["n1"], d["n2"]
+    A = to_device(d["A"])
+    outs = [torch.empty((1, n), dtype=torch.float32, device="cuda")
+            for n in (n0, n1 - n0, n2 - n1, N - n2)]
+
+    def quad_oracle(orc, c0, c1, d=d):
+        cl = lambda v: min(max(v - c0, 0), c1 - c0)
+        return orc.quad_matvec(d["A"], *wslice(d["w"], c0, c1), d["K"], c1 - c0, d["gs"],
+                               cl(d["n0"]), cl(d["n1"]), cl(d["n2"]))
+    cases.append(dict(
+        name="c1", workload=f"quad-output QKV matvec M=1, K={K}, N={N}, split {n0}/{n1}/{n2}, "
+                            f"group_size={gs}",
+        call_bytes=mat_bytes(K, N, gs) + 4 * K + 4 * N, set_bytes=mat_bytes(K, N, gs),
+        w0=dev_w(d["w"]), N=N,
+        call=lambda W, s, A=A, outs=outs, gs=gs, sp=(n0, n1, n2):
+            gq4.quad_matvec(A, *W, gs, *sp, outs=outs, stream=s),
+        oracle=quad_oracle))
+
+    # config 2: norm-prologue matvec 4096 -> 4096, gs 64, eps 1e-6
+    d = I.norm_prologue()
+    K, N, gs = d["K"], d["N"], d["gs"]
+    A, Ab, Wn = to_device(d["A"]), to_device(d["A_b"]), to_device(d["W_norm"])
+    C = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    cases.append(dict(
+        name="c2", workload=f"norm-prologue matvec M=1, K={K}, N={N}, group_size={gs}, eps=1e-6",
+        call_bytes=mat_bytes(K, N, gs) + 3 * 4 * K + 4 * N, set_bytes=mat_bytes(K, N, gs),
+        w0=dev_w(d["w"]), N=N,
+        call=lambda W, s, A=A, Ab=Ab, Wn=Wn, C=C, gs=gs, eps=d["eps"]:
+            gq4.norm_matvec(A, *W, gs, W_norm=Wn, eps=eps, A_b=Ab, C=C, stream=s),
+        oracle=lambda orc, c0, c1, d=d: orc.norm_matvec(d["A"], d["A_b"], d["W_norm"], d["eps"],
+                                                        *wslice(d["w"], c0, c1), d["K"], c1 - c0,
+                                                        d["gs"])))
+
+    # config 3: SiLU-gated gate/up 4096 -> 2 x 11008, gs 128
+    d = I.gated_gate_up()
+    K, N, gs = d["K"], d["N"], d["gs"]
+    A = to_device(d["A"])
+    out = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    cases.append(dict(
+        name="c3", workload=f"SiLU-gated gate/up matvec M=1, K={K}, N={N} x 2, group_size={gs}",
+        call_bytes=2 * mat_bytes(K, N, gs) + 4 * K + 4 * N, set_bytes=2 * mat_bytes(K, N, gs),
+        w0=dev_w(d["wg"]) + dev_w(d["wu"]), N=N,
+        call=lambda W, s, A=A, out=out, gs=gs: gq4.gated_matvec(A, *W, gs, out=out, stream=s),
+        oracle=lambda orc, c0, c1, d=d: orc.gated_matvec(d["A"], *wslice(d["wg"], c0, c1),
+                                                         *wslice(d["wu"], c0, c1), d["K"],
+                                                         c1 - c0, d["gs"])))
+    return cases
+
+
+def measure_per_config(gq4, stack, args, peak, with_oracle):
+    """One entry per config; each config's calls replayed in a CUDA graph over
+    rotating weight sets of at least 4x L2, so that every call reads HBM."""
+    import torch
+    out = {}
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    stream = torch.cuda.Stream()
+    orc = None
+    if with_oracle:
+        import oracle
+        orc = oracle.load()
+    for case in config_cases(gq4):
+        R = max(2, -(-4 * l2 // case["set_bytes"]))
+        sets = [case["w0"]] + [tuple(t.clone() for t in case["w0"]) for _ in range(R - 1)]
+
+        def body(s, sets=sets, call=case["call"]):
+            for W in sets:
+                call(W, s)
+        us = graph_time_us(body, max(args.steps, 20), args.warmup, stream) / R
+        gbs = case["call_bytes"] / (us * 1e-6) / 1e9
+        e = {"workload": case["workload"], "us_per_call": round(us, 3),
+             "bytes_per_call": case["call_bytes"], "GB/s": round(gbs, 1),
+             "frac_of_hbm_peak": round(gbs / peak, 4), "weight_sets": R,
+             "kernel": lane_path(1)[0],
+             "timing": f"CUDA graph of {R} calls over distinct weight sets "
+                       f"({R * case['set_bytes'] / 1e6:.0f} MB > 4x L2), CUDA events"}
+        if orc is not None:
+            one, par, cores = time_oracle(lambda c0, c1, o=case["oracle"]: o(orc, c0, c1), case["N"])
+            e["oracle"] = {"us_single_thread": round(one, 1), "us_all_cores": round(par, 1),
+                           "cores": cores, "kind": "C fp64 oracle, columns split over threads",
+                           "GB/s_all_cores": round(case["call_bytes"] / (par * 1e-6) / 1e9, 4)}
+        out[case["name"]] = e
+        del sets
+    torch.cuda.empty_cache()
+
+    # the stack at more lanes (same device weights as the one-lane stack)
+    for M in args.stack_lanes:
+        st = Stack(gq4, len(stack.layers), M, weights=stack.layers)
+        us = graph_time_us(lambda s, st=st: st.step(s), max(args.steps, 10), args.warmup, stream)
+        sb = step_bytes(M, len(stack.layers))
+        gbs = sb / (us * 1e-6) / 1e9
+        kern, _ = lane_path(M)
+        e = {"workload": f"7B-shaped decode layer stack, {len(stack.layers)} layers, int4 group 128, "
+                         f"M={M}",
+             "us_per_step": round(us, 2), "bytes_per_step": sb, "GB/s": round(gbs, 1),
+             "frac_of_hbm_peak": round(gbs / peak, 4), "vs_M1_step": None, "kernel": kern,
+             "timing": "CUDA graph of one step (128 C-ABI calls), CUDA events"}
+        if orc is not None:
+            e["oracle"] = stack_oracle_sample(orc, M)
+        out[f"c4_M{M}"] = e
+        del st
+    return out
+
+
+def stack_oracle_sample(orc, M):
+    """The oracle on a bounded sample of the M-lane stack: layer 0's O
+    projection (4096 -> 4096) at M lanes, one thread and all cores, scaled to
+    a whole 32-layer step by algorithmic bytes."""
+    from int4_group_quantized_quant_gb300 import inputs as I
+    L = I.stack_layer(0)
+    w = L["o"]
+    A = I.stack_input(M)[:, :HIDDEN].copy()
+    fn = lambda c0, c1: orc.matvec(A, w.Bq[c0:c1], w.scales[c0:c1], w.zeros[c0:c1], HIDDEN,
+                                   c1 - c0, GS)
+    one, par, cores = time_oracle(fn, HIDDEN, reps=1)
+    scale = step_bytes(M, 32) / layer_call_bytes(M)["o"]
+    return {"us_per_step_single_thread": round(one * scale, 0),
+            "us_per_step_all_cores": round(par * scale, 0), "cores": cores,
+            "sample": f"layer 0's O projection 4096 -> 4096 at M={M} (C fp64 oracle), scaled to "
+                      f"a 32-layer step by algorithmic bytes"}
+
+
+def measure_gemm(gq4, args):
+    """Prefill GEMM, 2048 rows through a 4096 x 4096 projection (gs 128), two
+    alternating weight sets, against the measured bf16 peak."""
+    import torch
+    from int4_group_quantized_quant_gb300 import inputs as I
+    Mg, K, N = 2048, 4096, 4096
+    ws = [tuple(to_device(a) for a in (w.Bq, w.scales, w.zeros))
+          for w in (I.quant_weights(K, N, GS, 1600, 90 + r) for r in range(2))]
+    A = to_device(I.activations(Mg, K, 1600, 91))
+    C = torch.empty((Mg, N), dtype=torch.float32, device="cuda")
+    work = torch.empty(gq4.gemm_workspace_bytes(Mg, K), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def body(s):
+        for W in ws:
+            gq4.gemm(A, *W, GS, C=C, workspace=work, stream=s)
+    us = graph_time_us(body, max(args.steps, 20), args.warmup, stream) / 2
+    tpeak, tsrc = bf16_peak()
+    tf = 2.0 * Mg * K * N / (us * 1e-6) / 1e12
+    return {"workload": f"prefill GEMM {Mg} x {K} -> {N}, int4 group {GS}", "us_per_call": round(us, 2),
+            "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / tpeak, 4), "peak": tpeak,
+            "peak_source": tsrc, "bound": "tensor",
+            "kernel": "tcgen05 GEMM (bf16 operands dequantized in registers, f32 accumulate)",
+            "timing": "CUDA graph of 2 calls over 2 weight sets, CUDA events"}
+
+
+def measure_sequence(gq4, stack, args, graph_us):
+    """The M = 1 step as one gq4_run_sequence launch (persistent kernel with a
+    grid barrier between calls) against the graph of single calls."""
+    import torch
+    calls, _ = stack.sequence()
+    ws = gq4.sequence_workspace()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            gq4.run_sequence(calls, ws, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(args.steps, 10)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            gq4.run_sequence(calls, ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / n
+    return {"workload": "7B-shaped stack, 32 layers, M=1, as gq4_run_sequence",
+            "us_per_step": round(us, 2), "graph_of_calls_us_per_step": round(graph_us, 2),
+            "ratio_to_graph": round(us / graph_us, 4),
+            "timing": "one persistent launch per step (128 calls), eager, CUDA events"}
 
 
 # ---------------------------------------------------------------------------
@@ -406,16 +699,10 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32",
         "data": "synthetic (seeded; int4 codes uniform 0..15, scales U[0.005,0.02], zeros U[6,9], "
                 "activations N(0,1), norm gain U[0.5,1.5])",
-        "config": {
-            "workload": f"7B-shaped decode layer stack, {layers} layers, int4 group 128, M={M}",
-            "lanes": M, "layers": layers, "hidden": HIDDEN, "ffn": FFN, "qkv": list(QKV),
-            "group_size": GS, "bytes_per_step": sbytes,
-            "l2": "inputs larger than L2: each step streams 3.2 GB of weights (L2 129 MB)",
-            "timing": "CUDA graph of one step, replayed; CUDA events on the replay stream",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": stack_config(layers, M, world),
+        "timing": "CUDA graph of one step (128 C-ABI calls), replayed; CUDA events on the replay stream",
         "roofline": {
-            "kernel": "gq4 gated gate/up + RMSNorm prologue, 4096 -> 2 x 11008 (one-lane streaming kernel, CUDA cores)",
+            "kernel": f"gq4 gated gate/up + RMSNorm prologue, 4096 -> 2 x 11008, M={M} ({lane_path(M)[0]})",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -423,7 +710,7 @@ def run_ours(args, rank, world, local_rank):
             else "fallback 6.8 TB/s",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic("gated_norm_4096x2x11008_M1"),
+            "traffic": profiled_traffic(f"gated_norm_4096x2x11008_{lane_path(M)[1]}"),
             "bytes_per_launch": gated_bytes,
             "avg_launch_us": round(gated_avg_s * 1e6, 3),
             "launches_timed": len(gated_ms),
@@ -440,6 +727,16 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * stack.launches_per_step(),
         "clocks": clock_info,
     }
+    # per-config lines (rank 0 of a replica run measures them on its own GPU)
+    if rank == 0 and not args.no_per_config:
+        pc = measure_per_config(gq4, stack, args, peak, with_oracle=not args.no_cpu_baseline)
+        for key in list(pc):
+            if key.startswith("c4_M"):
+                pc[key]["vs_M1_step"] = round(pc[key]["us_per_step"] / (ms_step * 1e3), 3)
+        pc["gemm_2048"] = measure_gemm(gq4, args)
+        if M == 1:
+            pc["sequence_M1"] = measure_sequence(gq4, stack, args, ms_step * 1e3)
+        line["per_config"] = pc
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(M, args.cpu_seconds)
     if rank == 0:
@@ -465,28 +762,72 @@ def oracle_layer(orc, L, h, M):
     return d.astype(np.float32)
 
 
+def oracle_layer_parallel(orc, L, h, M, pool, cores):
+    """oracle_layer with each call's columns split over `cores` threads (the C
+    oracle releases the GIL; its arithmetic is unchanged, every column's sum
+    still sequential, so the results are the same bits)."""
+    n0, n1, n2 = QKV[0], QKV[0] + QKV[1], sum(QKV)
+
+    def split(N):
+        b = [N * i // cores for i in range(cores + 1)]
+        return [(b[i], b[i + 1]) for i in range(cores) if b[i + 1] > b[i]]
+
+    def cols(fn, N):
+        parts = list(pool.map(lambda r: fn(*r), split(N)))
+        return np.concatenate(parts, axis=1)
+
+    def mv(A, w, K, N):
+        return cols(lambda c0, c1: orc.matvec(A, w.Bq[c0:c1], w.scales[c0:c1], w.zeros[c0:c1], K,
+                                              c1 - c0, GS)[0], N)
+    qkv = mv(h, L["qkv"], HIDDEN, n2)
+    q = np.ascontiguousarray(qkv[:, :n0]).astype(np.float32)
+    o = mv(q, L["o"], HIDDEN, HIDDEN).astype(np.float32)
+    g = cols(lambda c0, c1: orc.gated_matvec(
+        h, L["gate"].Bq[c0:c1], L["gate"].scales[c0:c1], L["gate"].zeros[c0:c1],
+        L["up"].Bq[c0:c1], L["up"].scales[c0:c1], L["up"].zeros[c0:c1], HIDDEN, c1 - c0, GS,
+        A_b=o, W_norm=L["W_norm"], eps=EPS)["out"], FFN)
+    return mv(g.astype(np.float32), L["down"], FFN, HIDDEN).astype(np.float32)
+
+
 def cpu_baseline(M, seconds):
-    """The oracle as it stands on the host, over whole layers until ~seconds of CPU work."""
+    """The oracle as it stands on the host over whole layers of the stack:
+    on all host cores (each call's columns split over threads) for about
+    `seconds`, and single-threaded for about `seconds`."""
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     from int4_group_quantized_quant_gb300 import inputs as I
     orc = oracle.load()
-    h = I.stack_input(M)
-    done, t_total, li = 0, 0.0, 0
-    while True:
-        L = I.stack_layer(li)
-        t0 = time.perf_counter()
-        h = oracle_layer(orc, L, h, M)
-        t_total += time.perf_counter() - t0
-        done += 1
-        li += 1
-        if t_total >= seconds or li >= 32:
-            break
-    sbytes = done * sum(layer_call_bytes(M).values())
-    return {"value": round(sbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1,
+    lbytes = sum(layer_call_bytes(M).values())
+    cores = host_cores()
+    layers = [I.stack_layer(li) for li in range(4)]
+
+    def timed(run_layer):
+        h = I.stack_input(M)
+        done, t_total = 0, 0.0
+        while True:
+            t0 = time.perf_counter()
+            h = run_layer(layers[done % len(layers)], h)
+            t_total += time.perf_counter() - t0
+            done += 1
+            if t_total >= seconds or done >= 32:
+                return done, t_total, h
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        dp, tp, _ = timed(lambda L, h: oracle_layer_parallel(orc, L, h, M, pool, cores))
+        # the split changes no bits: layer 0 both ways
+        h0 = I.stack_input(M)
+        same = bool(np.array_equal(oracle_layer_parallel(orc, layers[0], h0, M, pool, cores)
+                                   .view(np.uint32), oracle_layer(orc, layers[0], h0, M).view(np.uint32)))
+    d1, t1, _ = timed(lambda L, h: oracle_layer(orc, L, h, M))
+    return {"value": round(dp * lbytes / tp / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{done} of 32 layers of the same stack at M={M} (4 calls each), "
-                      f"single-threaded C fp64 oracle, {t_total:.1f} s",
-            "us_per_layer": round(t_total / done * 1e6, 1)}
+            "sample": f"{dp} layers of the same stack at M={M} (4 calls each, the first 4 layers' "
+                      f"weights in turn), C fp64 oracle with each call's columns split over "
+                      f"{cores} threads, {tp:.1f} s",
+            "us_per_layer": round(tp / dp * 1e6, 1),
+            "single_thread": {"value": round(d1 * lbytes / t1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "us_per_layer": round(t1 / d1 * 1e6, 1),
+                              "sample": f"{d1} layers, single-threaded, {t1:.1f} s"},
+            "threaded_equals_single": same}
 
 
 def run_reference(args, rank, world):
@@ -494,25 +835,30 @@ def run_reference(args, rank, world):
         return
     import oracle
     from int4_group_quantized_quant_gb300 import inputs as I
+    from concurrent.futures import ThreadPoolExecutor
     orc = oracle.load()
     M = args.lanes
+    cores = host_cores()
+    pool = ThreadPoolExecutor(max_workers=cores)
     h = I.stack_input(M)
     li = 0
-    # warm-up layers (untimed), then K timed steps of one layer each (a bounded sample)
+    # warm-up layers (untimed), then K timed steps of one layer each (a bounded
+    # sample), each call's columns split over the host's cores
     for _ in range(args.warmup):
-        h = oracle_layer(orc, I.stack_layer(li % args.layers), h, M)
+        h = oracle_layer_parallel(orc, I.stack_layer(li % args.layers), h, M, pool, cores)
         li += 1
     t_total = 0.0
     for _ in range(args.steps):
         L = I.stack_layer(li % args.layers)
         t0 = time.perf_counter()
-        h = oracle_layer(orc, L, h, M)
+        h = oracle_layer_parallel(orc, L, h, M, pool, cores)
         t_total += time.perf_counter() - t0
         li += 1
+    pool.shutdown()
     lbytes = sum(layer_call_bytes(M).values())
     value = args.steps * lbytes / t_total / 1e9
     sample = (f"{args.steps} timed layers (of the {args.layers}-layer stack) at M={M}, 4 calls "
-              f"each, single-threaded C fp64 oracle")
+              f"each, C fp64 oracle with each call's columns split over {cores} threads")
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -527,10 +873,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded, same generator and distributions as the GPU arm)",
-        "config": {"workload": f"7B-shaped decode layer stack, {args.layers} layers, int4 group "
-                               f"128, M={M}", "lanes": M, "layers": args.layers,
-                   "step": "one layer (bounded sample)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "config": stack_config(args.layers, M, world),
+        "timing": "host wall clock over a bounded sample: one layer per step, scaled to GB/s by "
+                  "the layer's algorithmic bytes",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -760,8 +1106,13 @@ def main():
     ap.add_argument("--lanes", type=int, default=1, help="decode lanes M (1..32)")
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--roofline-rounds", type=int, default=3)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config entries (configs 0-3, the stack at more lanes, "
+                         "the prefill GEMM, the sequence kernel)")
+    ap.add_argument("--stack-lanes", type=int, nargs="*", default=[4, 16, 32],
+                    help="lane counts of the extra stack entries")
     ap.add_argument("--profile", choices=["gated", "down", "quad", "step", "gemm"], default=None,
                     help="run a small launch sequence of one kernel for ncu (no timing)")
     ap.add_argument("--extras", action="store_true",
