@@ -926,6 +926,9 @@ def run_profile_case(args):
                 L = stack.layers[li]
                 gq4.quad_matvec(stack.h0, *L["qkv"], GS, stack.n0, stack.n1, stack.n2,
                                 outs=[stack.q, stack.k, stack.v, None], stream=stream)
+            elif args.profile == "o":
+                L = stack.layers[li]
+                gq4.matvec(stack.q, *L["o"], GS, C=stack.o, stream=stream)
     torch.cuda.synchronize()
     print(json.dumps({"profile_case": args.profile, "layers": args.layers, "lanes": args.lanes,
                       "launch_rounds": args.steps}))
@@ -1113,7 +1116,7 @@ def main():
                          "the prefill GEMM, the sequence kernel)")
     ap.add_argument("--stack-lanes", type=int, nargs="*", default=[4, 16, 32],
                     help="lane counts of the extra stack entries")
-    ap.add_argument("--profile", choices=["gated", "down", "quad", "step", "gemm"], default=None,
+    ap.add_argument("--profile", choices=["gated", "down", "quad", "o", "step", "gemm"], default=None,
                     help="run a small launch sequence of one kernel for ncu (no timing)")
     ap.add_argument("--extras", action="store_true",
                     help="time the dual, gated-input, GEMM, quantizer, MLX and embedding "

@@ -256,6 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
     const int n_stages_total = n_tl * spr;
     // tensor memory: kNW dequantized K-blocks per matrix, two accumulators per matrix
     constexpr int kNW = NMAT == 1 ? 12 : 6;
+    // K-blocks per hand-off step between the dequant warps and the MMA thread
+    // (one wait, one arrival and one commit per step, not per K-block: each
+    // barrier round trip costs ~0.2 us, more than a K-block's MMAs), and the
+    // steps tensor memory holds
+    constexpr int kKPS = NMAT == 1 ? 4 : 2;
+    constexpr int kNS = kNW / kKPS;
+    static_assert(kNW % kKPS == 0 && kNS <= kMaxNW, "tensor-memory steps");
     constexpr uint32_t kTmemCols = 512u;
     static_assert(NMAT * kNW * 32 + NMAT * 2 * 32 <= (int)kTmemCols, "tensor-memory map");
 
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
             mbar_init(&sh.full[s], 32);  // the producer lanes' cp.async arrivals
             mbar_init(&sh.empty[s], kDqWarps);
         }
-        for (int s = 0; s < kNW; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(&sh.w_full[s], kDqWarps);
             mbar_init(&sh.w_empty[s], 1);
         }
@@ -396,15 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         // the activations may be the previous kernel's outputs
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if constexpr (NORM) {
-            // One pass over A and A_b: x = A + A_b to bf16 in place (and x
-            // itself to residual_out), its square sum; then the staged x is
-            // scaled by the inverse RMS and the gain in place.  The operand is
-            // thus bf16(bf16(x) * inv * W) on every cluster; norm_out is
-            // written exactly, in f32, from x recomputed.
+            // One pass over A, A_b and W_norm: x = A + A_b (x itself to
+            // residual_out), its square sum, and bf16(x * W_norm) staged as
+            // the operand.  The inverse RMS is a per-lane scalar: the
+            // epilogue applies it to each finished dot product, once the
+            // cluster's square sums are in, and writes norm_out (exact f32,
+            // from x recomputed) meanwhile.  Staging thus needs no cluster
+            // round trip.
             constexpr int kU = 4;
             const size_t row_off = (size_t)(m < p.M ? m : 0) * p.K;
-            auto load_x = [&](int c0, float4 (&x)[kU][2]) {
-                float4 b[kU][2];
+            const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float part = 0.0f;
+            for (int c0 = sub; c0 < n_chunks; c0 += kU * TPL) {
+                float4 x[kU][2], b[kU][2], g[kU][2];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
                     const int c = c0 + u * TPL;
@@ -413,29 +424,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                     const float4 *a4 = reinterpret_cast<const float4 *>(p.A + row_off + (in ? k : 0));
                     const float4 *b4 = reinterpret_cast<const float4 *>(
                         (p.A_b ? p.A_b : p.A) + row_off + (in ? k : 0));
-                    const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + (in ? k : 0));
                     x[u][0] = in ? __ldg(a4) : z4;
                     x[u][1] = in ? __ldg(a4 + 1) : z4;
                     b[u][0] = in && p.A_b ? __ldg(b4) : z4;
                     b[u][1] = in && p.A_b ? __ldg(b4 + 1) : z4;
+                    g[u][0] = in ? __ldg(w4) : z4;
+                    g[u][1] = in ? __ldg(w4 + 1) : z4;
                 }
-#pragma unroll
-                for (int u = 0; u < kU; ++u)
-#pragma unroll
-                    for (int v = 0; v < 2; ++v) {
-                        x[u][v].x += b[u][v].x; x[u][v].y += b[u][v].y;
-                        x[u][v].z += b[u][v].z; x[u][v].w += b[u][v].w;
-                    }
-            };
-            float part = 0.0f;
-            for (int c0 = sub; c0 < n_chunks; c0 += kU * TPL) {
-                float4 x[kU][2];
-                load_x(c0, x);
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
                     const int c = c0 + u * TPL;
                     if (c >= n_chunks) continue;
                     const int k = k_base + 8 * c;
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        x[u][v].x += b[u][v].x; x[u][v].y += b[u][v].y;
+                        x[u][v].z += b[u][v].z; x[u][v].w += b[u][v].w;
+                    }
                     if (p.residual_out && m < p.M && k < p.K && writer(m, c)) {
                         float4 *ro = reinterpret_cast<float4 *>(p.residual_out + row_off + k);
                         ro[0] = x[u][0];
@@ -447,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                         part = fmaf(x[u][v].y, x[u][v].y, part);
                         part = fmaf(x[u][v].z, x[u][v].z, part);
                         part = fmaf(x[u][v].w, x[u][v].w, part);
+                        x[u][v].x *= g[u][v].x; x[u][v].y *= g[u][v].y;
+                        x[u][v].z *= g[u][v].z; x[u][v].w *= g[u][v].w;
                     }
                     *reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7)) =
                         pack_chunk(x[u][0], x[u][1]);
@@ -460,51 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
             if (ks > 1) cluster_wait();  // peers' barriers are initialised
             cwaited = true;
             if (tid == 0) {
+                // this CTA's square sums, released to every rank's epilogue
                 fence_acq_rel_cluster();
                 for (int j = 0; j < ks; ++j) mbar_arrive_cluster(dsmem_addr(smem_addr(sh.norm_full), j));
-            }
-            ok = __all_sync(0xffffffffu, tc_wait(sh.norm_full, 0, abort, true));
-            float total = 0.0f;
-            if (ok && m < p.M) {
-                for (int j = 0; j < ks; ++j) total += dsmem_ld_f32(dsmem_addr(smem_addr(&sh.part[m]), j));
-            }
-            const float inv = 1.0f / sqrtf(total / (float)p.K + p.eps);
-            // scale the staged x in place: element order in a chunk is
-            // (0,4,1,5,2,6,3,7), low half first
-            for (int c = sub; c < n_chunks; c += TPL) {
-                const int k = k_base + 8 * c;
-                uint4 *slot_p = reinterpret_cast<uint4 *>(act + (size_t)(c >> 3) * (MP * 128) + act_chunk_offset(m, c & 7));
-                if (!(ok && m < p.M && k < p.K)) {
-                    *slot_p = make_uint4(0u, 0u, 0u, 0u);
-                    continue;
-                }
-                const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + k);
-                const float4 g0 = __ldg(w4), g1 = __ldg(w4 + 1);
-                const uint4 xv = *slot_p;
-                auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
-                auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
-                uint4 o;
-                o.x = bf16x2_pack(lo(xv.x) * inv * g0.x, hi(xv.x) * inv * g1.x);
-                o.y = bf16x2_pack(lo(xv.y) * inv * g0.y, hi(xv.y) * inv * g1.y);
-                o.z = bf16x2_pack(lo(xv.z) * inv * g0.z, hi(xv.z) * inv * g1.z);
-                o.w = bf16x2_pack(lo(xv.w) * inv * g0.w, hi(xv.w) * inv * g1.w);
-                *slot_p = o;
-                if (p.norm_out && writer(m, c)) {
-                    // exact f32 side output from x recomputed
-                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + row_off + k);
-                    float4 x0 = __ldg(a4), x1 = __ldg(a4 + 1);
-                    if (p.A_b) {
-                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + row_off + k);
-                        const float4 b0 = __ldg(b4), b1 = __ldg(b4 + 1);
-                        x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
-                        x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
-                    }
-                    float4 *no = reinterpret_cast<float4 *>(p.norm_out + row_off + k);
-                    no[0] = make_float4((x0.x * inv) * g0.x, (x0.y * inv) * g0.y, (x0.z * inv) * g0.z,
-                                        (x0.w * inv) * g0.w);
-                    no[1] = make_float4((x1.x * inv) * g1.x, (x1.y * inv) * g1.y, (x1.z * inv) * g1.z,
-                                        (x1.w * inv) * g1.w);
-                }
             }
         } else {
             // batches of kU chunks: all loads issued before the first conversion
@@ -602,15 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
             // gate/up, whose tensor-memory ring is shorter): the step's codes
             // are loaded first, its tensor-memory stores are in flight
             // together, then one wait, then its slots go to the MMA
-            constexpr int KPS = NMAT == 1 ? 4 : 2;
+            constexpr int KPS = kKPS;
 #pragma unroll 1
             for (int jp = 0; jp < kStageK / kBlockK; jp += KPS, kbg += KPS) {
+                // one wait for the step's tensor-memory slots
+                const int stg = kbg / KPS;
                 bool got = true;
-#pragma unroll
-                for (int e = 0; e < KPS; ++e) {
-                    const int kb = kbg + e;
-                    if (got && kb >= kNW) got = tc_wait(&sh.w_empty[kb % kNW], ((kb / kNW) - 1) & 1, abort, false);
-                }
+                if (stg >= kNS) got = tc_wait(&sh.w_empty[stg % kNS], ((stg / kNS) - 1) & 1, abort, false);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -666,10 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int e = 0; e < KPS; ++e) mbar_arrive(&sh.w_full[(kbg + e) % kNW]);
-                }
+                if (lane == 0) mbar_arrive(&sh.w_full[stg % kNS]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[slot]);
@@ -702,25 +663,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after_sync();
-                for (int kb = 0; kb < KBr; ++kb, ++kbg) {
-                    const int ws = kbg % kNW;
-                    if (!tc_poll(&sh.w_full[ws], (kbg / kNW) & 1, abort)) {
+                // one step (kKPS K-blocks; KBr is a multiple of it) per wait
+                // and per commit
+                for (int kb0 = 0; kb0 < KBr; kb0 += kKPS, kbg += kKPS) {
+                    const int stg = kbg / kKPS;
+                    if (!tc_poll(&sh.w_full[stg % kNS], (stg / kNS) & 1, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    // descriptors advance by whole 16-byte units: one add per MMA
-                    const uint64_t bdesc0 = desc_base + (uint64_t)((uint32_t)kb * (MP * 128) >> 4);
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat) {
-                        const uint32_t a0 = tmem_base + w_col(mat, ws);
-                        const uint32_t d = tmem_base + acc_col(mat, b);
+                    for (int e = 0; e < kKPS; ++e) {
+                        const int kb = kb0 + e;
+                        const int ws = (kbg + e) % kNW;
+                        // descriptors advance by whole 16-byte units: one add per MMA
+                        const uint64_t bdesc0 = desc_base + (uint64_t)((uint32_t)kb * (MP * 128) >> 4);
 #pragma unroll
-                        for (int jj = 0; jj < kBlockK / 16; ++jj)
-                            tc_mma_ts(d, a0 + 8 * jj, bdesc0 + (uint64_t)(2 * jj), idesc, (kb | jj) != 0 ? 1u : 0u);
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            const uint32_t a0 = tmem_base + w_col(mat, ws);
+                            const uint32_t d = tmem_base + acc_col(mat, b);
+#pragma unroll
+                            for (int jj = 0; jj < kBlockK / 16; ++jj)
+                                tc_mma_ts(d, a0 + 8 * jj, bdesc0 + (uint64_t)(2 * jj), idesc,
+                                          (kb | jj) != 0 ? 1u : 0u);
+                        }
                     }
                     any = true;
-                    tc_commit(&sh.w_empty[ws]);
+                    tc_commit(&sh.w_empty[stg % kNS]);
                 }
                 if (!ok) break;
                 tc_commit(&sh.acc_full[b]);
@@ -748,6 +717,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
         bool ok = true;
         if (ks > 1) cluster_wait();
         cwaited = true;
+        // the norm prologue's inverse RMS per lane (1 without the prologue)
+        float *s_inv = reinterpret_cast<float *>(smem + p.off_misc + 256);
+        if constexpr (NORM) {
+            // every rank's square sums (rank order), then 1 / sqrt(mean + eps)
+            ok = __all_sync(0xffffffffu, tc_wait(sh.norm_full, 0, abort, true));
+            if (et < p.M) {
+                float total = 0.0f;
+                if (ok) {
+                    for (int j = 0; j < ks; ++j) total += dsmem_ld_f32(dsmem_addr(smem_addr(&sh.part[et]), j));
+                }
+                s_inv[et] = 1.0f / sqrtf(total / (float)p.K + p.eps);
+            }
+            named_barrier(2, kEpWarps * 32);
+            // norm_out = (x * inv) * W_norm in f32 from x recomputed, each
+            // 8-code chunk of a lane written once over the clusters: chunk c
+            // of lane m of this rank's K range by cluster (m * n_chunks + c)
+            // mod n_clusters
+            if (ok && p.norm_out) {
+                const int n_chunks = KBr * 8;
+                const int k_base = st0 * kStageK;
+                for (int idx = et; idx < p.M * n_chunks; idx += kEpWarps * 32) {
+                    const int m = idx / n_chunks;
+                    const int c = idx - m * n_chunks;
+                    const int k = k_base + 8 * c;
+                    if (k >= p.K || (m * n_chunks + c) % p.n_clusters != cid) continue;
+                    const size_t o = (size_t)m * p.K + k;
+                    const float4 *a4 = reinterpret_cast<const float4 *>(p.A + o);
+                    const float4 *w4 = reinterpret_cast<const float4 *>(p.W_norm + k);
+                    float4 x0 = __ldg(a4), x1 = __ldg(a4 + 1);
+                    if (p.A_b) {
+                        const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + o);
+                        const float4 b0 = __ldg(b4), b1 = __ldg(b4 + 1);
+                        x0.x += b0.x; x0.y += b0.y; x0.z += b0.z; x0.w += b0.w;
+                        x1.x += b1.x; x1.y += b1.y; x1.z += b1.z; x1.w += b1.w;
+                    }
+                    const float4 g0 = __ldg(w4), g1 = __ldg(w4 + 1);
+                    const float iv = s_inv[m];
+                    float4 *no = reinterpret_cast<float4 *>(p.norm_out + o);
+                    no[0] = make_float4((x0.x * iv) * g0.x, (x0.y * iv) * g0.y, (x0.z * iv) * g0.z,
+                                        (x0.w * iv) * g0.w);
+                    no[1] = make_float4((x1.x * iv) * g1.x, (x1.y * iv) * g1.y, (x1.z * iv) * g1.z,
+                                        (x1.w * iv) * g1.w);
+                }
+            }
+        }
         for (int tl = 0; tl < n_tl; ++tl) {
             const int b = tl & 1;
             // every outcome is made warp-uniform: the tensor-memory loads are
@@ -779,8 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                 // the thread reads back only what it wrote (its row)
                 const int col = row0 + r;
                 if (ok && r < p.TR && col < p.N) {
-                    for (int m = 0; m < p.M; ++m)
-                        store_out<EPI>(p, m, col, red[m * 128 + r], red[((NMAT - 1) * MP + m) * 128 + r]);
+                    for (int m = 0; m < p.M; ++m) {
+                        const float iv = NORM ? s_inv[m] : 1.0f;
+                        store_out<EPI>(p, m, col, red[m * 128 + r] * iv,
+                                       red[((NMAT - 1) * MP + m) * 128 + r] * iv);
+                    }
                 }
                 continue;
             }
@@ -827,10 +844,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                     }
                     const float g[4] = {sum[0].x, sum[0].y, sum[0].z, sum[0].w};
                     const float u4[4] = {sum[NMAT - 1].x, sum[NMAT - 1].y, sum[NMAT - 1].z, sum[NMAT - 1].w};
+                    const float iv = NORM ? s_inv[m] : 1.0f;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int col = row0 + rr + e;
-                        if (rr + e < p.TR && col < p.N) store_out<EPI>(p, m, col, g[e], u4[e]);
+                        if (rr + e < p.TR && col < p.N) store_out<EPI>(p, m, col, g[e] * iv, u4[e] * iv);
                     }
                 }
             }
@@ -1057,7 +1075,7 @@ cudaError_t launch_tc_variant(const Call &call, cudaStream_t stream)
     prm.off_ring = round_up(act, 1024u);
     prm.off_red = prm.off_ring + (uint32_t)pl.S * prm.stage_bytes;
     prm.off_misc = prm.off_red + round_up(red, 1024u);
-    prm.off_bar = prm.off_misc + 256u;
+    prm.off_bar = prm.off_misc + 384u;  // part[32], tensor-memory base, abort flag, inv[32]
     if (prm.off_bar + 80u * 8u + 1024u > pl.smem) return cudaErrorInvalidValue;
     prm.magic_bf16 = 0x43004300u;
     prm.A = call.A;
