@@ -122,12 +122,28 @@ __device__ __forceinline__ void fence_acq_rel_cluster()
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
+// Non-blocking test of an mbarrier phase (no suspension).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait on an mbarrier phase.  Gives up (false) when another thread of
 // the CTA has already given up, or after the time limit (then it records the
-// error and tells the CTA).  `cluster` waits acquire at cluster scope.
+// error and tells the CTA).  `cluster` waits acquire at cluster scope; CTA
+// waits poll with test_wait rather than suspend in try_wait, whose wake-up
+// after the phase completes cost ~0.3 us per wait here.
 __device__ __noinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, bool cluster)
 {
-    auto ready = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    auto ready = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_test(bar, parity); };
     if (ready()) return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
@@ -553,17 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                     z_src[mat] = box1 + srow * p.BW + off;
                 }
             }
-            // bf16 constants of the current group, per matrix: (128 + zi) twice,
-            // the scale twice, (zi - z) * scale twice; rows and groups past the
-            // matrix keep (128, 0, 0), which dequantizes any code to 0
-            int cur_gl = -1;
-            uint32_t c2[NMAT], s2[NMAT], d2[NMAT];
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat) {
-                c2[mat] = 0x43004300u;
-                s2[mat] = 0u;
-                d2[mat] = 0u;
-            }
             // KPS K-blocks per step (the whole stage for one matrix, pairs for
             // gate/up, whose tensor-memory ring is shorter): the step's codes
             // are loaded first, its tensor-memory stores are in flight
@@ -591,22 +596,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                                 wv[e][mat] = *reinterpret_cast<const uint4 *>(
                                     stage + mat * p.codes_bytes + r * 128 + (((2 * (jp + e) + h) ^ (r & 7)) << 4));
                         }
+                    // bf16 constants of each K-block's group, per matrix: (128 + zi)
+                    // twice, the scale twice, (zi - z) * scale twice; rows and groups
+                    // past the matrix get (128, 0, 0), which dequantizes any code to
+                    // 0.  All of the step's constants come first (predicated loads,
+                    // no branch between the K-blocks' arithmetic).
+                    uint32_t c2[KPS][NMAT], s2[KPS][NMAT], d2[KPS][NMAT];
+#pragma unroll
+                    for (int e = 0; e < KPS; ++e) {
+                        const int gl = chunk_group(c0 + 2 * (jp + e) + h, p.gmagic) - g0;
+                        const bool valid = row_valid && g0 + gl <= g_last;
+#pragma unroll
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            const float sv = valid ? s_src[mat][gl] : 0.0f;
+                            const float zv = valid ? z_src[mat][gl] : 0.0f;
+                            const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
+                            c2[e][mat] = bf16x2_pack(128.0f + zi, 128.0f + zi);
+                            s2[e][mat] = bf16x2_pack(sv, sv);
+                            const float dzs = (zi - zv) * sv;
+                            d2[e][mat] = bf16x2_pack(dzs, dzs);
+                        }
+                    }
 #pragma unroll
                     for (int e = 0; e < KPS; ++e) {
                         const int ws = (kbg + e) % kNW;
-                        const int gl = chunk_group(c0 + 2 * (jp + e) + h, p.gmagic) - g0;
-                        if (row_valid && gl != cur_gl && g0 + gl <= g_last) {
-                            cur_gl = gl;
-#pragma unroll
-                            for (int mat = 0; mat < NMAT; ++mat) {
-                                const float sv = s_src[mat][gl], zv = z_src[mat][gl];
-                                const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
-                                const float dzs = (zi - zv) * sv;
-                                c2[mat] = bf16x2_pack(128.0f + zi, 128.0f + zi);
-                                s2[mat] = bf16x2_pack(sv, sv);
-                                d2[mat] = bf16x2_pack(dzs, dzs);
-                            }
-                        }
 #pragma unroll
                         for (int mat = 0; mat < NMAT; ++mat) {
                             uint32_t o[16];
@@ -618,10 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_matvec_kernel(const __grid_con
                                 const uint32_t t1 = bf16_code_pair(w >> 4, magic);
                                 const uint32_t t2 = bf16_code_pair(w >> 8, magic);
                                 const uint32_t t3 = bf16_code_pair(w >> 12, magic);
-                                o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(t0, c2[mat]), s2[mat], d2[mat]);
-                                o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(t1, c2[mat]), s2[mat], d2[mat]);
-                                o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(t2, c2[mat]), s2[mat], d2[mat]);
-                                o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(t3, c2[mat]), s2[mat], d2[mat]);
+                                o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(t0, c2[e][mat]), s2[e][mat], d2[e][mat]);
+                                o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(t1, c2[e][mat]), s2[e][mat], d2[e][mat]);
+                                o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(t2, c2[e][mat]), s2[e][mat], d2[e][mat]);
+                                o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(t3, c2[e][mat]), s2[e][mat], d2[e][mat]);
                             }
                             tmem_st16(tmem_base + lane_off + w_col(mat, ws) + 16 * h, o);
                         }
