@@ -52,6 +52,13 @@ constexpr int kThreads = 15 * 32;
 constexpr int kEpBase = kDqWarps * 32;
 constexpr int kTR = 128;       // weight columns per tile
 constexpr int kNW = 8;         // tensor-memory slots of dequantized K-blocks
+// K-blocks per hand-off step between the dequant warps and the MMA thread (a
+// whole stage: one wait, one arrival and one commit per stage, not per
+// K-block, whose barrier round trip cost more than its MMAs), and the steps
+// tensor memory holds
+constexpr int kKPS = 4;
+constexpr int kNS = kNW / kKPS;
+static_assert(kNW % kKPS == 0, "tensor-memory steps");
 constexpr int kStageK = 256;   // codes per weight stage
 constexpr int kBlockK = 64;    // codes per K-block
 constexpr int kMaxStages = 8;  // weight ring
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(&bar.a_full[s], 1);
             mbar_init(&bar.a_empty[s], 1);
         }
-        for (int s = 0; s < kNW; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(&bar.w_full[s], kDqWarps);
             mbar_init(&bar.w_empty[s], 1);
         }
@@ -336,54 +343,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     z_src = reinterpret_cast<const float *>(stage + p.off_sz + (1 * p.P + rho) * p.sz_box_stride) +
                             srow * p.BW + off;
                 }
-                // bf16 constants of the current group: (128 + zi) twice, the
-                // scale twice, (zi - z) * scale twice; rows and groups past the
-                // matrix keep (128, 0, 0), which dequantizes any code to 0
-                int cur_gl = -1;
-                uint32_t c2 = 0x43004300u, s2 = 0u, d2 = 0u;
-                constexpr int KPS = 4;  // K-blocks per stage
+                constexpr int KPS = kKPS;  // K-blocks per stage = per hand-off step
+                static_assert(KPS == kStageK / kBlockK, "one step per stage");
                 uint4 wv[KPS];
 #pragma unroll
                 for (int e = 0; e < KPS; ++e)
                     wv[e] = *reinterpret_cast<const uint4 *>(stage + r * 128 + (((2 * e + h) ^ (r & 7)) << 4));
-                // each K-block goes to the MMA as soon as it is in tensor memory
-                // (its slot freed by the MMA kNW K-blocks earlier)
+                // bf16 constants of each K-block's group: (128 + zi) twice, the
+                // scale twice, (zi - z) * scale twice; rows and groups past the
+                // matrix get (128, 0, 0), which dequantizes any code to 0 (all
+                // of them first: predicated loads, no branch between K-blocks)
+                uint32_t c2[KPS], s2[KPS], d2[KPS];
 #pragma unroll
                 for (int e = 0; e < KPS; ++e) {
-                    const int kb = kbg + e;
-                    const int ws = kb % kNW;
-                    if (!__all_sync(0xffffffffu,
-                                    kb < kNW || gemm_wait(&bar.w_empty[ws], ((kb / kNW) - 1) & 1, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
                     const int gl = chunk_group(c0 + 2 * e + h, p.gmagic) - g0;
-                    if (row_valid && gl != cur_gl && g0 + gl <= g_last) {
-                        cur_gl = gl;
-                        const float sv = s_src[gl], zv = z_src[gl];
-                        const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
-                        const float dzs = (zi - zv) * sv;
-                        c2 = bf16x2_pack(128.0f + zi, 128.0f + zi);
-                        s2 = bf16x2_pack(sv, sv);
-                        d2 = bf16x2_pack(dzs, dzs);
-                    }
+                    const bool valid = row_valid && g0 + gl <= g_last;
+                    const float sv = valid ? s_src[gl] : 0.0f;
+                    const float zv = valid ? z_src[gl] : 0.0f;
+                    const float zi = rintf(fminf(fmaxf(zv, 0.0f), 15.0f));
+                    const float dzs = (zi - zv) * sv;
+                    c2[e] = bf16x2_pack(128.0f + zi, 128.0f + zi);
+                    s2[e] = bf16x2_pack(sv, sv);
+                    d2[e] = bf16x2_pack(dzs, dzs);
+                }
+                // the step's tensor-memory slots (freed by the MMA kNS steps earlier)
+                const int stg = kbg / KPS;
+                if (!__all_sync(0xffffffffu,
+                                stg < kNS || gemm_wait(&bar.w_empty[stg % kNS], ((stg / kNS) - 1) & 1, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int e = 0; e < KPS; ++e) {
+                    const int ws = (kbg + e) % kNW;
                     uint32_t o[16];
                     const uint32_t words[4] = {wv[e].x, wv[e].y, wv[e].z, wv[e].w};
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
                         const uint32_t w = words[wi];
-                        o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w, magic), c2), s2, d2);
-                        o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 4, magic), c2), s2, d2);
-                        o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 8, magic), c2), s2, d2);
-                        o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 12, magic), c2), s2, d2);
+                        o[4 * wi + 0] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w, magic), c2[e]), s2[e], d2[e]);
+                        o[4 * wi + 1] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 4, magic), c2[e]), s2[e], d2[e]);
+                        o[4 * wi + 2] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 8, magic), c2[e]), s2[e], d2[e]);
+                        o[4 * wi + 3] = bf16x2_fma(bf16x2_sub(bf16_code_pair(w >> 12, magic), c2[e]), s2[e], d2[e]);
                     }
                     tmem_st16(tmem_base + lane_off + (uint32_t)(ws * 32) + 16 * h, o);
-                    tmem_wait_st();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar.w_full[ws]);
                 }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.w_full[stg % kNS]);
                 if (!ok) break;
                 // the stage's codes are in registers: its ring slot is free
                 __syncwarp();
@@ -413,23 +422,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     break;
                 }
                 tc_fence_after_sync();
-                for (int kb = 0; kb < KB; ++kb, ++kbg) {
-                    const int ws = kbg % kNW;
-                    const int as = kbg % p.SA;
-                    if (!poll_wait(&bar.w_full[ws], (kbg / kNW) & 1, abort) ||
-                        !poll_wait(&bar.a_full[as], (kbg / p.SA) & 1, abort)) {
+                // one weight step (a stage of kKPS K-blocks; KB is a multiple)
+                // per wait and per commit; activation K-blocks one by one
+                for (int kb0 = 0; kb0 < KB && ok; kb0 += kKPS, kbg += kKPS) {
+                    const int stg = kbg / kKPS;
+                    if (!poll_wait(&bar.w_full[stg % kNS], (stg / kNS) & 1, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t bdesc = smem_desc_sw128(act_s + (uint32_t)as * p.act_bytes, 1024);
-                    const uint32_t a0 = tmem_base + (uint32_t)(ws * 32);
+                    for (int e = 0; e < kKPS; ++e) {
+                        const int kb = kb0 + e;
+                        const int as = (kbg + e) % p.SA;
+                        if (!poll_wait(&bar.a_full[as], ((kbg + e) / p.SA) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint64_t bdesc = smem_desc_sw128(act_s + (uint32_t)as * p.act_bytes, 1024);
+                        const uint32_t a0 = tmem_base + (uint32_t)(((kbg + e) % kNW) * 32);
 #pragma unroll
-                    for (int jj = 0; jj < kBlockK / 16; ++jj)
-                        tc_mma_ts(d, a0 + 8 * jj, bdesc + (uint64_t)(2 * jj), idesc, (kb | jj) != 0 ? 1u : 0u);
-                    any = true;
-                    tc_commit(&bar.w_empty[ws]);
-                    tc_commit(&bar.a_empty[as]);
+                        for (int jj = 0; jj < kBlockK / 16; ++jj)
+                            tc_mma_ts(d, a0 + 8 * jj, bdesc + (uint64_t)(2 * jj), idesc, (kb | jj) != 0 ? 1u : 0u);
+                        any = true;
+                        tc_commit(&bar.a_empty[as]);
+                    }
+                    if (!ok) break;
+                    tc_commit(&bar.w_empty[stg % kNS]);
                 }
                 if (!ok) break;
                 tc_commit(bar.acc_full);
