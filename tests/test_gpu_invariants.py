@@ -199,6 +199,36 @@ def test_nonfinite_activation_propagates(gq4):
     assert np.all(np.isfinite(C[0])) and np.all(np.isnan(C[1]))
 
 
+@pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
+def test_one_lane_nonfinite_activation(gq4, bad):
+    """M = 1 (the integer one-lane path): a non-finite activation makes every
+    output NaN (each column's dot product uses it), nothing is masked."""
+    K, N, gs = 4096, 300, 128
+    w = I.quant_weights(K, N, gs, 971)
+    A = I.activations(1, K, 971)
+    A[0, 777] = bad
+    C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    assert np.all(np.isnan(C))
+
+
+@pytest.mark.parametrize("outlier,scale", [(100.0, 1.0), (1000.0, 1.0), (1.0, 1e-30), (1.0, 1e20)])
+def test_one_lane_activation_dynamic_range(gq4, outlier, scale):
+    """M = 1 holds activations as 24-bit fixed point per 64-code group (a
+    power-of-two scale per group): one outlier of 100x or 1000x the typical
+    magnitude in every group, and vectors scaled to 1e-30 or 1e20, stay
+    within the fp32 tolerance against the oracle."""
+    K, N, gs = 4096, 512, 128
+    w = I.quant_weights(K, N, gs, 972, int(outlier))
+    A = I.activations(1, K, 972, int(outlier)) * np.float32(scale)
+    r = np.random.default_rng(973)
+    pos = np.arange(0, K, 64) + r.integers(0, 64, size=K // 64)
+    A[0, pos] = np.float32(outlier * scale) * np.sign(r.standard_normal(pos.size)).astype(np.float32)
+    A = A.astype(np.float32)
+    C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+    check_close(f"outlier {outlier} scale {scale}", C, ref, tol_fp32(S))
+
+
 def test_stream_argument(gq4):
     """Calls run on the stream they are given and respect its ordering."""
     M, K, N, gs = 1, 1024, 1024, 32
