@@ -81,11 +81,19 @@
  *         gq4_from_mlx do), or the caller puts a non-kernel operation
  *         (an event wait, a copy) or a host synchronisation in between.
  *   - Results are deterministic: the same inputs give the same bits.
- *   - Arithmetic: with M = 1 or 2 <= M <= 15 lanes every product and sum is
- *     f32 (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot
- *     product).  With 16 <= M <= 32 lanes on sm_103 the weights and the
- *     activations are rounded to bf16 and multiplied on the tensor core with
- *     f32 accumulation (|error| <= 2e-2 * sum_k |a_k w_k| + 1e-6); the norm
+ *   - A NaN or infinite activation makes every output whose dot product uses
+ *     it non-finite (NaN at M = 1).
+ *   - Arithmetic: with 2 <= M <= 15 lanes every product and sum is f32
+ *     (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot
+ *     product).  With M = 1 each 64-code group of activations is held as
+ *     24-bit fixed point with a power-of-two scale (each value within
+ *     2^-22 of the group's largest magnitude) and the products are summed
+ *     exactly in integers: the same bound holds unless a group holds an
+ *     activation some 2^12 times larger than the ones that carry the
+ *     result (a huge activation on a near-zero weight).  With
+ *     16 <= M <= 32 lanes on sm_103 the weights and the activations are
+ *     rounded to bf16 and multiplied on the tensor core with f32
+ *     accumulation (|error| <= 2e-2 * sum_k |a_k w_k| + 1e-6); the norm
  *     prologue's side outputs stay f32.
  * ---------------------------------------------------------------------------
  */

@@ -100,13 +100,15 @@ __device__ __forceinline__ void quantize_and_store_i8(const float4 (&x)[NQ], int
     float fac16[NQ];
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
-        // the group's exponent: max |a| < 2^E (a zero, subnormal or
-        // non-finite maximum is clamped; a non-finite activation makes sm
-        // non-finite, and the group's value NaN through dz * asum)
+        // the group's exponent: max |a| < 2^E (zero or subnormal maxima
+        // clamp).  A non-finite activation makes the group's value NaN: an
+        // infinite maximum gives it a NaN scale, and a NaN (which the max
+        // skips) makes sm NaN, which reaches the value through dz * asum.
         int E = (int)(__float_as_uint(mx[i]) >> 23) - 126;
         E = min(max(E, -100), 127);
         const float sc = __uint_as_float((uint32_t)(149 - E) << 23);  // 2^(22 - E)
-        fac16[i] = __uint_as_float((uint32_t)(E + 101) << 23);        // 2^(E - 26)
+        fac16[i] = __float_as_uint(mx[i]) >= 0x7f800000u ? __uint_as_float(0x7fffffffu)
+                                                         : __uint_as_float((uint32_t)(E + 101) << 23);  // 2^(E - 26)
         X[i][0] = __float_as_int(__fmaf_rn(x[i].x, sc, kI8MagicF)) - kI8Magic;
         X[i][1] = __float_as_int(__fmaf_rn(x[i].y, sc, kI8MagicF)) - kI8Magic;
         X[i][2] = __float_as_int(__fmaf_rn(x[i].z, sc, kI8MagicF)) - kI8Magic;

@@ -201,8 +201,8 @@ def test_nonfinite_activation_propagates(gq4):
 
 @pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
 def test_one_lane_nonfinite_activation(gq4, bad):
-    """M = 1 (the integer one-lane path): a non-finite activation makes every
-    output NaN (each column's dot product uses it), nothing is masked."""
+    """M = 1 (the integer one-lane path): a NaN or infinite activation makes
+    every output NaN (each column's dot product uses it), nothing is masked."""
     K, N, gs = 4096, 300, 128
     w = I.quant_weights(K, N, gs, 971)
     A = I.activations(1, K, 971)
