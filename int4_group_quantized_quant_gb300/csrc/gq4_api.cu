@@ -128,12 +128,14 @@ gq4_status check_output(const float *out, size_t elems, RangeSet &rs)
 
 gq4_status run(const gq4::Call &call, cudaStream_t stream)
 {
-    // one lane: the persistent streaming kernel; 16..32 lanes: the bf16
-    // tensor-core kernel; otherwise (and for shapes those do not take) the
-    // fp32 CUDA-core kernel
+    // one lane: the persistent streaming kernel; 2..4 lanes: the persistent
+    // warp-MMA kernel; 16..32 lanes: the bf16 tensor-core kernel; otherwise
+    // (and for shapes those do not take) the fp32 CUDA-core kernel
     cudaError_t err;
     if (gq4::stream_path_supported(call))
         err = gq4::launch_stream(call, stream);
+    else if (gq4::lanes_path_supported(call))
+        err = gq4::launch_lanes(call, stream);
     else if (gq4::tc_path_supported(call))
         err = gq4::launch_tc(call, stream);
     else
@@ -585,6 +587,8 @@ gq4_status gq4_gemm(int M, int K, int N, int group_size, const float *A, const u
             err = gq4::launch_tc(call, stream);
         else if (rows == 1 && gq4::stream_path_supported(call))
             err = gq4::launch_stream(call, stream);
+        else if (gq4::lanes_path_supported(call))
+            err = gq4::launch_lanes(call, stream);
         else
             err = gq4::launch_fp32(call, stream);
         if (err != cudaSuccess) return GQ4_ERR_CUDA;
@@ -666,9 +670,10 @@ gq4_status gq4_device_error(unsigned int *bits, int clear)
     if (gq4::read_seq_device_error(&c, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_quant_device_error(&d, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
     if (gq4::read_embed_device_error(&e, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    unsigned int f = 0;
+    unsigned int f = 0, l = 0;
     if (gq4::read_gemm_device_error(&f, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
-    *bits = a | b | c | d | e | f;
+    if (gq4::read_lanes_device_error(&l, clear != 0) != cudaSuccess) return GQ4_ERR_CUDA;
+    *bits = a | b | c | d | e | f | l;
     return GQ4_OK;
 }
 

@@ -65,6 +65,12 @@ cudaError_t launch_fp32(const Call &call, cudaStream_t stream);
 bool stream_path_supported(const Call &call);
 cudaError_t launch_stream(const Call &call, cudaStream_t stream);
 
+// 2 <= M <= 4 lanes: persistent bulk-copy kernel, exact fp16 products on the
+// warp-level MMA (K a multiple of 128 within the shared-memory plan).
+bool lanes_path_supported(const Call &call);
+cudaError_t launch_lanes(const Call &call, cudaStream_t stream);
+cudaError_t read_lanes_device_error(unsigned int *bits, bool clear);
+
 // bf16 tensor-core path for 16 <= M <= 32 lanes (sm_103).
 bool tc_path_supported(const Call &call);
 cudaError_t launch_tc(const Call &call, cudaStream_t stream);

@@ -1,11 +1,13 @@
 """GPU invariants that hold bit for bit by construction of the kernels.
 
 * quad outputs concatenated == the plain matvec on the same weights;
-* lane m of an M-lane call == lane 0 of a two-lane call on row m for
-  M <= 15 (the multi-lane CUDA-core kernel's per-lane arithmetic does not
-  depend on the lane count; one-lane calls use the streaming kernel and
-  16..32 lanes the tensor-core kernel, whose orders differ, so those are
-  compared within tolerance instead);
+* lane m of an M-lane call == lane 0 of a smaller call on row m, within one
+  kernel: 2..4 lanes (the warp-MMA kernel, gs a multiple of 128: each lane's
+  N columns are computed independently) against a two-lane call, 5..15 lanes
+  (the CUDA-core kernel, whose per-lane arithmetic does not depend on the
+  lane count) against a five-lane call; one-lane calls use the streaming
+  kernel and 16..32 lanes the tensor-core kernel, whose orders differ, so
+  those are compared within tolerance instead;
 * repeated calls give identical bits;
 * codes equal to integer zero points give exactly 0 at K = 11008;
 * a zero gate gives exactly 0 out of the gated call;
@@ -40,9 +42,9 @@ def test_quad_equals_matvec(gq4, M):
         assert np.array_equal(cat.view(np.uint32), C.view(np.uint32)), (M, n0, n1, n2)
 
 
-def _pair(A, m):
-    """Rows (m, m+1 mod M) of A: a two-lane call whose lane 0 is row m."""
-    return np.ascontiguousarray(A[[m, (m + 1) % A.shape[0]]])
+def _pair(A, m, lanes=2):
+    """Rows (m, m+1, ... mod M) of A: a `lanes`-lane call whose lane 0 is row m."""
+    return np.ascontiguousarray(A[[(m + i) % A.shape[0] for i in range(lanes)]])
 
 
 @pytest.mark.parametrize("M", [3, 4, 7, 15])
@@ -51,8 +53,9 @@ def test_lane_equals_solo(gq4, M):
     w = I.quant_weights(K, N, gs, 961, M)
     A = I.activations(M, K, 961, M)
     C = host(gq4.matvec(dev(A), *wdev(w), gs))
+    small = 2 if M <= 4 else 5  # the same kernel as the M-lane call
     for m in range(M):
-        Cm = host(gq4.matvec(dev(_pair(A, m)), *wdev(w), gs))
+        Cm = host(gq4.matvec(dev(_pair(A, m, small)), *wdev(w), gs))
         assert np.array_equal(C[m].view(np.uint32), Cm[0].view(np.uint32)), (M, m)
     # and the one-lane streaming kernel agrees with the oracle on every row
     for m in range(min(M, 3)):
