@@ -14,21 +14,22 @@
 //   * A bit mask moves two codes of a packed word into the two fp16 halves of
 //     a register: bits 0-3 and 16-19 give the fp16 bit patterns q, read as the
 //     subnormal values q * 2^-24 exactly; bits 4-7 and 20-23 give 16 q * 2^-24.
-//     A shift by 8 brings the other four codes of the word to the same places.
-//     The integer part zi of the zero point comes off in fp16 (zi * 2^-24 and
-//     16 zi * 2^-24 are subnormals too, and the differences are exact), so
-//     codes equal to an integer zero contribute exactly nothing.
-//   * Activations are staged per lane and 128-code block, scaled by a power of
-//     two so the block's largest magnitude lies in [2^13, 2^14), as an fp16
-//     high part and an fp16 low part (x' = hi + lo to about 22 bits); the
-//     odd code positions take x' / 16, matching the 16 q of their codes.
+//     A shift by 8 brings the other four codes of the word to the same places:
+//     five integer operations decode a word (8 codes).
+//   * Activations are staged per lane and 128-code block as 22-bit fixed-point
+//     integers X = rint(x 2^k) (the block's largest magnitude in [2^21, 2^22])
+//     split into X = 2048 h + l, both exact in fp16; the odd code positions
+//     take h / 16 and l / 16, matching the 16 q of their codes.
 //   * mma.sync m16n8k16 (fp16 inputs, f32 accumulation): 16 weight columns
-//     (rows of the MMA) times 8 columns of B = {hi, lo} of 4 lanes.  Products
-//     of the fp16 operands are exact; the sums are f32.
-//   * Per block, column and lane: y += s * (2^(24-e) D - (z - zi) X), with D
-//     the MMA sum of (q - zi) x' over the block, e the block's scale exponent
-//     and X the f32 sum of the block's activations (the fractional part of the
-//     zero point comes off through X).
+//     (rows of the MMA) times 8 columns of B = {h, l} of 4 lanes.  Every
+//     product and partial sum is an integer times 2^-24 below 2^24 of them,
+//     so the block's sums of q h and q l are exact; zi (sum h) and zi (sum l)
+//     come off exactly (zi the integer part of the zero point: codes equal to
+//     an integer zero give exactly nothing).
+//   * Per block, column and lane: y += s * (2^(24-k) (2048 H + L) - (z - zi)
+//     S), with H and L the exact sums of (q - zi) h and (q - zi) l and S the
+//     f32 sum of the block's activations (the fractional part of the zero
+//     comes off through S).
 //
 // Decomposition:
 //   * Persistent grid, one CTA per SM, a contiguous range of whole columns per
@@ -45,8 +46,9 @@
 //     out for conflict-free reads, then runs its blocks; its partial sums go
 //     to a per-ring-entry buffer and the last warp to finish the stage (a
 //     shared counter) adds the 8 partials in warp order and writes the
-//     outputs.  A ring entry is released only after that sum, so the next
-//     occupant cannot overwrite the partials early.
+//     outputs.  Each warp releases its ring entry as soon as its blocks are
+//     done; the partial buffers (one more than ring entries) are reused only
+//     after their sum (see the stage loop).
 //   * Programmatic dependent launch as in the one-lane kernel: the producer
 //     streams weights before the dependency wait, the consumers wait before
 //     reading activations; a kernel signals its dependents at its last stage.
@@ -84,7 +86,8 @@ struct LanesParams {
     int KW;          // packed words per column (K / 8)
     int KB;          // 128-code blocks per column
     int G;           // scale groups per column
-    int bpg;         // blocks per scale group (gs / 128)
+    int bpg;         // blocks per scale group (gs / 128, a power of two)
+    int bpg_shift;   // log2(bpg)
     int S;           // ring depth
     int unit;        // column granularity of the balanced split
     int n_units;
@@ -145,6 +148,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Bulk prefetch of global memory into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2^k as an f32 for -126 <= k <= 127 (exact).
 __device__ __forceinline__ float pow2i(int k)
 {
@@ -158,91 +167,90 @@ __device__ __forceinline__ float mul_pow2(float x, int k)
     return (x * pow2i(k1)) * pow2i(k - k1);
 }
 
-// a - b on two fp16 halves (round to nearest, subnormals kept: the operands
-// here are subnormal integers times 2^-24 and the difference is exact).
-__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t h2_bits(__half2 h)
 {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// fp16 high and low parts of two values (low halves: a, high halves: b).
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo)
+// Reduce-scatter of U values per lane (U = 8 or 16) over the 32 lanes of a
+// warp: afterwards lane l holds the reduction of unit unit_of(l) over all 32
+// lanes (U = 16: unit (l >> 1) & 15, held by lanes 2u and 2u + 1; U = 8: unit
+// (l >> 2) & 7, held by lanes 4u .. 4u + 3).  A fixed order of operations, so
+// the result is the same whatever the units hold.
+template <int U>
+__device__ __forceinline__ int rs_unit(int lane)
 {
-    const __half2 h = __floats2half2_rn(a, b);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-    hi = h2_bits(h);
-    lo = h2_bits(l);
+    return U == 16 ? (lane >> 1) & 15 : (lane >> 2) & 7;
 }
 
-// One packed word w of lane m in the prologue: its 8 activations x (zero
-// for a word past K or a lane past M), the block's largest magnitude and sum
-// over the 16 lanes holding the block (all 32 lanes of the warp call this
-// together), the power-of-two scale, and the fp16 high/low parts stored in
-// the MMA's B layout [block][pair][n = 2m + part][t][8 halves]; the block's
-// {f1, f2, X} (f1 f2 = 2^(24 - k), X = sum of x) by its first lane.
-template <int NP>
-__device__ __forceinline__ void stage_word(const float (&x)[8], int m, int w, bool ok, int lane,
-                                           unsigned char *s_act, unsigned char *s_fx)
+template <int U>
+__device__ __forceinline__ int rs_owner(int u)
 {
-    float mx = 0.0f, sm = 0.0f;
-    bool bad = false;  // inf or NaN (fmaxf would drop a NaN)
+    return U == 16 ? 2 * u : 4 * u;
+}
+
+template <int U, class T, class Op>
+__device__ __forceinline__ T reduce_scatter(const T (&v)[U], int lane, Op op)
+{
+    static_assert(U == 8 || U == 16, "units per warp");
+    T a[U];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        mx = fmaxf(mx, fabsf(x[j]));
-        sm += x[j];
-        bad |= !(fabsf(x[j]) <= 3.402823466e38f);
+    for (int i = 0; i < U; ++i) a[i] = v[i];
+    int n = U;
+#pragma unroll
+    for (int off = 16; off >= (U == 16 ? 2 : 4); off >>= 1) {
+        n >>= 1;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < U / 2; ++i) {
+            if (i >= n) break;
+            const T keep = up ? a[i + n] : a[i];
+            const T send = up ? a[i] : a[i + n];
+            a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+        }
     }
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        sm += __shfl_xor_sync(0xffffffffu, sm, off);
-        bad |= __shfl_xor_sync(0xffffffffu, (int)bad, off) != 0;
+    for (int off = (U == 16 ? 1 : 2); off >= 1; off >>= 1) a[0] = op(a[0], __shfl_xor_sync(0xffffffffu, a[0], off));
+    return a[0];
+}
+
+struct OpAdd {
+    template <class T>
+    __device__ __forceinline__ T operator()(T x, T y) const { return x + y; }
+};
+struct OpMax {
+    __device__ __forceinline__ uint32_t operator()(uint32_t x, uint32_t y) const { return max(x, y); }
+};
+
+constexpr int kBadScale = 1 << 20;  // the scale exponent of a block holding an inf or NaN
+
+// Scale of a block from its largest magnitude as bits (an inf or NaN compares
+// above any finite): X = rint(x 2^k) puts the largest magnitude in
+// [2^21, 2^22]; f = 2^(24 - k) turns the MMA's sums (units of 2^-24) back
+// into activation units.  A non-finite block gives k = kBadScale and f = NaN.
+__device__ __forceinline__ void block_scale(uint32_t mb, int &k, float &f)
+{
+    k = 0;
+    f = 0.0f;
+    if (mb >= 0x7f800000u) {
+        k = kBadScale;
+    } else if (mb != 0u) {
+        int E = ilogbf(__uint_as_float(mb));  // the largest magnitude in [2^E, 2^(E+1))
+        if (E > 124) {
+            k = kBadScale;  // 2^(24-k) would leave the f32 range
+        } else {
+            E = E < -129 ? -129 : E;  // subnormal activations: a smaller scale
+            k = 21 - E;
+            f = pow2i(3 + E);
+        }
     }
-    float f1, f2;
-    int k;  // x' = x 2^k
-    if (bad) {
-        f1 = __int_as_float(0x7fffffff);  // the block's lane results become NaN
-        f2 = 1.0f;
-        k = 0;
-    } else if (mx == 0.0f) {
-        f1 = 0.0f;
-        f2 = 0.0f;
-        k = 0;
-    } else {
-        const int E = ilogbf(mx);  // mx in [2^E, 2^(E+1))
-        k = 13 - E;
-        const int j = 11 + E;      // 2^(24 - k)
-        const int j1 = j / 2;
-        f1 = pow2i(j1);
-        f2 = pow2i(j - j1);
-    }
-    float xs[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float v = bad ? 0.0f : mul_pow2(x[j], k);
-        xs[j] = (j & 1) ? v * 0.0625f : v;
-    }
-    if (!ok) return;
-    uint4 hi, lo;
-    split_pair(xs[0], xs[4], hi.x, lo.x);
-    split_pair(xs[1], xs[5], hi.y, lo.y);
-    split_pair(xs[2], xs[6], hi.z, lo.z);
-    split_pair(xs[3], xs[7], hi.w, lo.w);
-    const int b = w >> 4, wi = w & 15;
-    const int t = wi >> 2, pr = wi & 3;
-    uint4 *dst = reinterpret_cast<uint4 *>(s_act + ((size_t)(b * 4 + pr) * (2 * NP) + 2 * m) * 64 + t * 16);
-    dst[0] = hi;
-    dst[4] = lo;  // n = 2m + 1: 64 bytes on
-    if ((lane & 15) == 0)
-        *reinterpret_cast<float4 *>(s_fx + ((size_t)b * 4 + m) * 16) = make_float4(f1, f2, sm, 0.0f);
+    if (k == kBadScale) f = __int_as_float(0x7fffffff);  // the block's lane results become NaN
+}
+
+// Two integers as fp16 halves: a, and b / 16 (exact).
+__device__ __forceinline__ uint32_t piece_pair(int a, int b)
+{
+    return h2_bits(__floats2half2_rn((float)a, (float)b * 0.0625f));
 }
 
 // NP: lanes per MMA (2 or 4; the N columns are {hi, lo} of each lane).
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     uint64_t *srows = empty + kMaxStages;  // scale/zero rows landed
     uint64_t *ready = srows + 1;           // consumers' prologue done
     int *s_seq = reinterpret_cast<int *>(ready + 1);  // stage a ring entry holds
-    int *s_cnt = s_seq + kMaxStages;                  // warps done with a ring entry
+    int *s_cnt = s_seq + kMaxStages;                  // warps done with a partial buffer
     float *s_inv = reinterpret_cast<float *>(smem + p.off_misc);        // [4] inverse RMS per lane
     float *s_sq = s_inv + 4;                                            // [8 warps][4] square sums
     unsigned char *s_act = smem + p.off_act;
@@ -283,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
                 s_seq[s] = -1;
-                s_cnt[s] = 0;
             }
+            for (int s = 0; s <= p.S; ++s) s_cnt[s] = 0;  // S + 1 partial buffers
             mbar_init(srows, 1);
             mbar_init(ready, 1);
             mbar_fence_init();
@@ -305,6 +313,25 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     bulk_g2s(smem + p.off_z[m], p.zeros[m] + (size_t)col_begin * p.G, bytes, srows);
                 }
             }
+            // the codes of stage i as (first column, count) per region
+            auto stage_regions = [&](int i, int (&rc)[2], int (&rn)[2]) {
+                const int c0 = col_begin + i * TCOLS;
+                const int nc = min(TCOLS, col_end - c0);
+                if constexpr (NMAT == 2) {
+                    rc[0] = rc[1] = c0;
+                    rn[0] = rn[1] = nc;
+                } else {
+                    rc[0] = c0;
+                    rn[0] = min(8, nc);
+                    rc[1] = c0 + 8;
+                    rn[1] = nc - rn[0];
+                }
+            };
+            // Stages beyond the ring are prefetched into L2 (up to S ahead of
+            // the stage being copied), so that a ring entry's refill reads L2:
+            // more bytes in flight than the ring holds.  Not before the
+            // consumers' prologue, whose activation loads go first.
+            int pf = p.S;  // next stage to prefetch
             for (int i = 0; ok && i < n_stages; ++i) {
                 const int slot = i % p.S;
                 // two stages go out at once, the rest after the consumers'
@@ -320,18 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     ok = false;
                     break;
                 }
-                const int c0 = col_begin + i * TCOLS;
-                const int nc = min(TCOLS, col_end - c0);
                 int rc[2], rn[2];  // first column and count of each region
-                if constexpr (NMAT == 2) {
-                    rc[0] = rc[1] = c0;
-                    rn[0] = rn[1] = nc;
-                } else {
-                    rc[0] = c0;
-                    rn[0] = min(8, nc);
-                    rc[1] = c0 + 8;
-                    rn[1] = nc - rn[0];
-                }
+                stage_regions(i, rc, rn);
                 unsigned char *dst = smem + (size_t)slot * p.stage_bytes;
                 s_seq[slot] = i;  // published by the release of the arrive below
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)(rn[0] + rn[1]) * p.col_bytes);
@@ -343,6 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                              (uint32_t)rn[r] * p.col_bytes, &full[slot]);
                 }
                 issued = i + 1;
+                if (i >= 2) {
+                    for (; pf < n_stages && pf <= i + p.S; ++pf) {
+                        int pc[2], pn[2];
+                        stage_regions(pf, pc, pn);
+                        if constexpr (NMAT == 2) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r)
+                                prefetch_l2(p.Bq[r] + (size_t)pc[r] * (p.KW / 4), (uint32_t)pn[r] * p.col_bytes);
+                        } else {
+                            // the two regions are one contiguous run of columns
+                            prefetch_l2(p.Bq[0] + (size_t)pc[0] * (p.KW / 4),
+                                        (uint32_t)(pn[0] + pn[1]) * p.col_bytes);
+                        }
+                    }
+                }
             }
             if (!ok) {
                 // leave no copy in flight into this CTA's shared memory
@@ -355,13 +387,22 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     }
 
     // =====================================================================
-    // Consumer warps: prologue.  A thread takes the packed words w = base +
-    // lane (+ kCT ...) of every lane m: their 8 activations, the block's scale
-    // exponent and sum by shuffles over the 16 threads holding the block's 16
-    // words, the fp16 high/low parts into the MMA's B layout.  All loads of a
-    // batch of words are issued before any is used (one round trip per batch
-    // under the weight stream); the loop bounds are uniform per warp, so the
-    // shuffles always see all 32 lanes.
+    // Consumer warps: prologue.  One warp load instruction reads one 128-
+    // activation block of one lane (lane l: activations 4l .. 4l + 3), so the
+    // loads are fully coalesced.  A warp takes 4 k-blocks of every lane per
+    // pass (U = 4 NP units), all its loads issued before any is used (one
+    // round trip under the weight stream); the loop bounds are uniform per
+    // warp.  Per unit: the block's largest magnitude and sums are reduce-
+    // scattered over the warp, the scales gathered back from the unit's owner
+    // lane; X = rint(x 2^k) = 2048 h + l with l in [-1024, 1023] (both exact
+    // in fp16: every MMA product and partial sum is an integer times 2^-24
+    // below 2^24 of them, so a block's dot products are exact and the integer
+    // part of the zero point comes off exactly through the piece sums).  Codes
+    // j and j + 4 of a word (lanes 2w and 2w + 1) meet in one xor-1 shuffle
+    // per piece; the odd code positions take h / 16 and l / 16 (their codes
+    // are 16 q).  Stored: the pieces in the MMA's B layout [block][pair]
+    // [n = 2m + part][t][8 halves], and per unit {2^(24-k), sum h 2^-24,
+    // sum l 2^-24, sum x}.
     // =====================================================================
     const int ctid = threadIdx.x;
     lanes_dependency_wait();
@@ -369,68 +410,106 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
 #pragma unroll
     for (int m = 0; m < NP; ++m) sq[m] = 0.0f;
     const bool cta0 = blockIdx.x == 0;
-    constexpr int WB = 2;                          // words per thread per batch
-    constexpr bool TWO = PRO != kProNone;          // A_b (norm) or the gate vector
+    constexpr bool TWO = PRO != kProNone;  // A_b (norm) or the gate vector
+    constexpr int U = 4 * NP;
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int base = warp * 32; base < p.KW; base += kCT * WB) {
-        float4 va[WB][NP][2], vb[WB][NP][2], vg[WB][2];
+    const int par = lane & 1;  // codes 0-3 (0) or 4-7 (1) of word lane >> 1
+    const int wsl = lane >> 1;
+    // this lane's 8 bytes within a block's B area, lane 0 of the MMA's N
+    const uint32_t act_lane = (uint32_t)(wsl & 3) * (2 * NP) * 64u + (uint32_t)(wsl >> 2) * 16u + 8u * par;
+    for (int kb0 = 4 * warp; kb0 < p.KB; kb0 += 4 * kConsumerWarps) {
+        float4 va[U], vb[U], vg[4];
 #pragma unroll
-        for (int j = 0; j < WB; ++j) {
-            const int w = base + lane + j * kCT;
-            const bool ok = w < p.KW;
+        for (int i = 0; i < 4; ++i) {
+            const bool okb = kb0 + i < p.KB;
+            const size_t k0 = (size_t)(kb0 + i) * kBlock + 4 * lane;
 #pragma unroll
             for (int m = 0; m < NP; ++m) {
-                const bool on = ok && m < p.M;
-                const float4 *a4 = reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + (size_t)w * 8);
-                va[j][m][0] = on ? __ldg(a4) : z4;
-                va[j][m][1] = on ? __ldg(a4 + 1) : z4;
-                if constexpr (TWO) {
-                    const bool onb = on && p.A_b != nullptr;
-                    const float4 *b4 = reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + (size_t)w * 8);
-                    vb[j][m][0] = onb ? __ldg(b4) : z4;
-                    vb[j][m][1] = onb ? __ldg(b4 + 1) : z4;
-                }
+                const bool on = okb && m < p.M;
+                va[i * NP + m] = on ? __ldg(reinterpret_cast<const float4 *>(p.A + (size_t)m * p.K + k0)) : z4;
+                if constexpr (TWO)
+                    vb[i * NP + m] = (on && p.A_b != nullptr)
+                                         ? __ldg(reinterpret_cast<const float4 *>(p.A_b + (size_t)m * p.K + k0))
+                                         : z4;
             }
+            if constexpr (NORM) vg[i] = okb ? __ldg(reinterpret_cast<const float4 *>(p.W_norm + k0)) : z4;
+        }
+        uint32_t mb[U];
+        float smv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = u / NP, m = u % NP;
+            float4 v = va[u];
             if constexpr (NORM) {
-                const float4 *g4 = reinterpret_cast<const float4 *>(p.W_norm + (size_t)w * 8);
-                vg[j][0] = ok ? __ldg(g4) : z4;
-                vg[j][1] = ok ? __ldg(g4 + 1) : z4;
+                const float4 a = vb[u];
+                v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+                if (cta0 && kb0 + i < p.KB && m < p.M && p.residual_out)
+                    *reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + (size_t)(kb0 + i) * kBlock +
+                                                4 * lane) = v;
+                float s2 = v.x * v.x;
+                s2 = fmaf(v.y, v.y, s2); s2 = fmaf(v.z, v.z, s2); s2 = fmaf(v.w, v.w, s2);
+                sq[m] += s2;
+                const float4 gg = vg[i];
+                v.x *= gg.x; v.y *= gg.y; v.z *= gg.z; v.w *= gg.w;
+            } else if constexpr (TWO) {
+                const float4 gg = vb[u];
+                v.x = gate_input<PRO>(v.x, gg.x); v.y = gate_input<PRO>(v.y, gg.y);
+                v.z = gate_input<PRO>(v.z, gg.z); v.w = gate_input<PRO>(v.w, gg.w);
+            }
+            va[u] = v;
+            mb[u] = max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                        max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu));
+            smv[u] = (v.x + v.y) + (v.z + v.w);
+        }
+        // the scale of the lane's own unit, then of every unit from its owner
+        const uint32_t mown = reduce_scatter<U>(mb, lane, OpMax());
+        const float sown = reduce_scatter<U>(smv, lane, OpAdd());
+        int kown;
+        float fown;
+        block_scale(mown, kown, fown);
+        int shv[U], slv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = u / NP, m = u % NP;
+            const int k = __shfl_sync(0xffffffffu, kown, rs_owner<U>(u));
+            const bool bad = k == kBadScale;
+            const float xv[4] = {va[u].x, va[u].y, va[u].z, va[u].w};
+            int h[4], l[4];
+            int sh = 0, sl = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int X = bad ? 0 : __float2int_rn(mul_pow2(xv[j], k));
+                h[j] = (X + 1024) >> 11;
+                l[j] = X - (h[j] << 11);
+                sh += h[j];
+                sl += l[j];
+            }
+            shv[u] = sh;
+            slv[u] = sl;
+            // own halves and the other lane's: (piece of code a, piece of code b / 16)
+            const uint32_t hown = par ? piece_pair(h[2], h[3]) : piece_pair(h[0], h[1]);
+            const uint32_t hsnd = par ? piece_pair(h[0], h[1]) : piece_pair(h[2], h[3]);
+            const uint32_t lown = par ? piece_pair(l[2], l[3]) : piece_pair(l[0], l[1]);
+            const uint32_t lsnd = par ? piece_pair(l[0], l[1]) : piece_pair(l[2], l[3]);
+            const uint32_t hrcv = __shfl_xor_sync(0xffffffffu, hsnd, 1);
+            const uint32_t lrcv = __shfl_xor_sync(0xffffffffu, lsnd, 1);
+            // even lane: (code 0, code 4), (code 1, code 5); odd: (2, 6), (3, 7)
+            const uint32_t ha = par ? hrcv : hown, hb = par ? hown : hrcv;
+            const uint32_t la = par ? lrcv : lown, lb = par ? lown : lrcv;
+            if (kb0 + i < p.KB) {
+                unsigned char *d = s_act + (size_t)(kb0 + i) * 4 * (2 * NP) * 64 + (size_t)(2 * m) * 64 + act_lane;
+                *reinterpret_cast<uint2 *>(d) = make_uint2(__byte_perm(ha, hb, 0x5410), __byte_perm(ha, hb, 0x7632));
+                *reinterpret_cast<uint2 *>(d + 64) =
+                    make_uint2(__byte_perm(la, lb, 0x5410), __byte_perm(la, lb, 0x7632));
             }
         }
-#pragma unroll
-        for (int j = 0; j < WB; ++j) {
-            const int w = base + lane + j * kCT;
-            const bool ok = w < p.KW;
-#pragma unroll
-            for (int m = 0; m < NP; ++m) {
-                float4 v0 = va[j][m][0], v1 = va[j][m][1];
-                if constexpr (NORM) {
-                    const float4 b0 = vb[j][m][0], b1 = vb[j][m][1];
-                    v0.x += b0.x; v0.y += b0.y; v0.z += b0.z; v0.w += b0.w;
-                    v1.x += b1.x; v1.y += b1.y; v1.z += b1.z; v1.w += b1.w;
-                    if (cta0 && ok && m < p.M && p.residual_out) {
-                        float4 *r4 = reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + (size_t)w * 8);
-                        r4[0] = v0;
-                        r4[1] = v1;
-                    }
-                    float s2 = v0.x * v0.x;
-                    s2 = fmaf(v0.y, v0.y, s2); s2 = fmaf(v0.z, v0.z, s2); s2 = fmaf(v0.w, v0.w, s2);
-                    s2 = fmaf(v1.x, v1.x, s2); s2 = fmaf(v1.y, v1.y, s2);
-                    s2 = fmaf(v1.z, v1.z, s2); s2 = fmaf(v1.w, v1.w, s2);
-                    sq[m] += s2;
-                    const float4 g0 = vg[j][0], g1 = vg[j][1];
-                    v0.x *= g0.x; v0.y *= g0.y; v0.z *= g0.z; v0.w *= g0.w;
-                    v1.x *= g1.x; v1.y *= g1.y; v1.z *= g1.z; v1.w *= g1.w;
-                } else if constexpr (TWO) {
-                    const float4 g0 = vb[j][m][0], g1 = vb[j][m][1];
-                    v0.x = gate_input<PRO>(v0.x, g0.x); v0.y = gate_input<PRO>(v0.y, g0.y);
-                    v0.z = gate_input<PRO>(v0.z, g0.z); v0.w = gate_input<PRO>(v0.w, g0.w);
-                    v1.x = gate_input<PRO>(v1.x, g1.x); v1.y = gate_input<PRO>(v1.y, g1.y);
-                    v1.z = gate_input<PRO>(v1.z, g1.z); v1.w = gate_input<PRO>(v1.w, g1.w);
-                }
-                const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                stage_word<NP>(x, m, w, ok, lane, s_act, smem + p.off_fx);
-            }
+        const int shown = reduce_scatter<U>(shv, lane, OpAdd());
+        const int slown = reduce_scatter<U>(slv, lane, OpAdd());
+        const int uo = rs_unit<U>(lane);
+        if (lane == rs_owner<U>(uo) && kb0 + uo / NP < p.KB) {
+            const float e24 = 5.9604644775390625e-8f;  // 2^-24
+            *reinterpret_cast<float4 *>(smem + p.off_fx + ((size_t)(kb0 + uo / NP) * 4 + uo % NP) * 16) =
+                make_float4(fown, (float)shown * e24, (float)slown * e24, sown);
         }
     }
     if constexpr (NORM) {
@@ -464,6 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int gw0 = bw0 / p.bpg;
     const int ngw = bw1 > bw0 ? (bw1 - 1) / p.bpg - gw0 + 1 : 0;
     float4 *scr = reinterpret_cast<float4 *>(smem + p.off_scr) + (size_t)warp * p.max_groups * 16;
+    // scratch fill: lane -> (row fr, group fj), rpp rows per pass (ngw <= 32)
+    const int rpp = ngw > 0 ? 32 / ngw : 1;
+    const int fr = ngw > 0 ? lane / ngw : 0;
+    const int fj = (ngw > 0 && fr < rpp) ? lane - fr * ngw : -1;
     float2 *part = reinterpret_cast<float2 *>(smem + p.off_part);  // [S][warps][32]
     const float inv_t = NORM ? s_inv[t] : 1.0f;
     // MMA rows g and g + 8: region g & 1, columns (g >> 1) and (g >> 1) + 4 of it
@@ -484,9 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         }
         const unsigned char *st = smem + (size_t)ring * p.stage_bytes;
 
-        // scale and zero of this warp's groups for the tile's 16 MMA rows
-        for (int idx = lane; idx < ngw * 16; idx += 32) {
-            const int j = idx % ngw, r = idx / ngw;
+        // scale and zero of this warp's groups for the tile's 16 MMA rows:
+        // {s, z - zi, zi, 0}, lanes (row, group) = (fr + rpp i, fj)
+        for (int r = fr; fj >= 0 && r < 16; r += rpp) {
             int m, lc;
             if constexpr (NMAT == 2) {
                 m = r & 1;
@@ -496,62 +579,87 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 lc = lc0 + 8 * (r & 1) + (r >> 1);
             }
             lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
-            const size_t si = (size_t)lc * p.G + gw0 + j;
-            const float* sr = reinterpret_cast<const float *>(smem + p.off_s[m]);
-            const float* zr = reinterpret_cast<const float *>(smem + p.off_z[m]);
-            // scale, fractional part of the zero, integer part as two fp16
-            // subnormal halves (zi * 2^-24: the bit pattern zi)
-            const float z = zr[si];
-            const float zf = rintf(fminf(fmaxf(z, 0.0f), 15.0f));
-            const uint32_t zbits = (uint32_t)(int)zf * 0x00010001u;
-            scr[j * 16 + r] = make_float4(sr[si], z - zf, __uint_as_float(zbits), 0.0f);
+            const size_t si = (size_t)lc * p.G + gw0 + fj;
+            const float sv = reinterpret_cast<const float *>(smem + p.off_s[m])[si];
+            const float z = reinterpret_cast<const float *>(smem + p.off_z[m])[si];
+            const float zi = rintf(fminf(fmaxf(z, 0.0f), 15.0f));
+            scr[fj * 16 + r] = make_float4(sv, z - zi, zi, 0.0f);
         }
         __syncwarp();
 
         float y0 = 0.0f, y8 = 0.0f;
         if (!failed) {
             const unsigned char *ra = st + row_off;
-            for (int b = bw0; b < bw1; ++b) {
-                const uint4 wa = *reinterpret_cast<const uint4 *>(ra + b * 64 + t * 16);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(ra + row8_delta + b * 64 + t * 16);
-                const int j = b / p.bpg - gw0;
-                const float4 sz0 = scr[j * 16 + g];
-                const float4 sz8 = scr[j * 16 + g + 8];
-                // the integer zero, subtracted from the codes exactly: zi and
-                // 16 zi as fp16 subnormals in both halves
-                const uint32_t z0 = __float_as_uint(sz0.z), z8 = __float_as_uint(sz8.z);
-                const uint32_t z0h = z0 << 4, z8h = z8 << 4;
-                float d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                float d2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                const unsigned char *bb = s_act + (size_t)b * 4 * (2 * NP * 64) + b_lane_off;
+            // two blocks at a time: all their shared-memory loads first, then
+            // four independent MMA chains (a repeated last block is discarded)
+            for (int b = bw0; b < bw1; b += 2) {
+                const bool two = b + 1 < bw1;
+                const int bb[2] = {b, two ? b + 1 : b};
+                uint4 wa[2], wb[2], bq[2][4];
+                float4 fx[2], sz0[2], sz8[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    wa[u] = *reinterpret_cast<const uint4 *>(ra + bb[u] * 64 + t * 16);
+                    wb[u] = *reinterpret_cast<const uint4 *>(ra + row8_delta + bb[u] * 64 + t * 16);
+                    const unsigned char *bp = s_act + (size_t)bb[u] * 4 * (2 * NP * 64) + b_lane_off;
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr)
+                        bq[u][pr] = b_active ? *reinterpret_cast<const uint4 *>(bp + pr * (2 * NP * 64))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                    // {2^(24-k), sum h 2^-24, sum l 2^-24, sum x} of lane t's block
+                    fx[u] = s_fx[bb[u] * 4 + t];
+                    const int j = (bb[u] >> p.bpg_shift) - gw0;
+                    sz0[u] = scr[j * 16 + g];  // {s, z - zi, zi, 0} of row g
+                    sz8[u] = scr[j * 16 + g + 8];
+                }
+                float d1[2][4], d2[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d1[u][i] = d2[u][i] = 0.0f;
 #pragma unroll
                 for (int pr = 0; pr < 4; ++pr) {
-                    uint4 bq = make_uint4(0u, 0u, 0u, 0u);
-                    if (b_active) bq = *reinterpret_cast<const uint4 *>(bb + pr * (2 * NP * 64));
-                    const uint32_t w0 = pr == 0 ? wa.x : pr == 1 ? wa.y : pr == 2 ? wa.z : wa.w;
-                    const uint32_t w8 = pr == 0 ? wb.x : pr == 1 ? wb.y : pr == 2 ? wb.z : wb.w;
-                    mma_f16(d1, hsub2_bits(w0 & 0x000F000Fu, z0), hsub2_bits(w8 & 0x000F000Fu, z8),
-                            hsub2_bits(w0 & 0x00F000F0u, z0h), hsub2_bits(w8 & 0x00F000F0u, z8h), bq.x, bq.y);
-                    const uint32_t v0 = w0 >> 8, v8 = w8 >> 8;
-                    mma_f16(d2, hsub2_bits(v0 & 0x000F000Fu, z0), hsub2_bits(v8 & 0x000F000Fu, z8),
-                            hsub2_bits(v0 & 0x00F000F0u, z0h), hsub2_bits(v8 & 0x00F000F0u, z8h), bq.z, bq.w);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t w0 = pr == 0 ? wa[u].x : pr == 1 ? wa[u].y : pr == 2 ? wa[u].z : wa[u].w;
+                        const uint32_t w8 = pr == 0 ? wb[u].x : pr == 1 ? wb[u].y : pr == 2 ? wb[u].z : wb[u].w;
+                        mma_f16(d1[u], w0 & 0x000F000Fu, w8 & 0x000F000Fu, w0 & 0x00F000F0u, w8 & 0x00F000F0u,
+                                bq[u][pr].x, bq[u][pr].y);
+                        const uint32_t v0 = w0 >> 8, v8 = w8 >> 8;
+                        mma_f16(d2[u], v0 & 0x000F000Fu, v8 & 0x000F000Fu, v0 & 0x00F000F0u, v8 & 0x00F000F0u,
+                                bq[u][pr].z, bq[u][pr].w);
+                    }
                 }
-                const float4 fx = s_fx[b * 4 + t];
-                const float e0 = (d1[0] + d1[1]) + (d2[0] + d2[1]);
-                const float e8 = (d1[2] + d1[3]) + (d2[2] + d2[3]);
-                // y += s * (sum (q - zi) x - (z - zi) X)
-                y0 = fmaf(sz0.x, fmaf(-sz0.y, fx.z, (e0 * fx.x) * fx.y), y0);
-                y8 = fmaf(sz8.x, fmaf(-sz8.y, fx.z, (e8 * fx.x) * fx.y), y8);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (u == 1 && !two) break;
+                    // exact: sum (q - zi) h and sum (q - zi) l, times 2^-24
+                    const float h0 = fmaf(-sz0[u].z, fx[u].y, d1[u][0] + d2[u][0]);
+                    const float l0 = fmaf(-sz0[u].z, fx[u].z, d1[u][1] + d2[u][1]);
+                    const float h8 = fmaf(-sz8[u].z, fx[u].y, d1[u][2] + d2[u][2]);
+                    const float l8 = fmaf(-sz8[u].z, fx[u].z, d1[u][3] + d2[u][3]);
+                    // y += s * (sum (q - zi) x - (z - zi) X)
+                    y0 = fmaf(sz0[u].x, fmaf(-sz0[u].y, fx[u].w, fmaf(h0, 2048.0f, l0) * fx[u].x), y0);
+                    y8 = fmaf(sz8[u].x, fmaf(-sz8[u].y, fx[u].w, fmaf(h8, 2048.0f, l8) * fx[u].x), y8);
+                }
             }
         }
 
-        // ---- cross-warp sum: partials per ring entry, the last warp adds ----
-        part[((size_t)ring * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
+        // this warp is done with the stage's codes
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[ring]);
+
+        // ---- cross-warp sum: S + 1 partial buffers, the last warp adds ----
+        // A warp reaches stage i + S + 1 (the next user of buffer i mod
+        // (S + 1)) only after every warp released stage i + 1, and the last
+        // warp of stage i releases stage i + 1 only after its sum of stage i.
+        const int ps = i % (p.S + 1);
+        part[((size_t)ps * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = atomicAdd(&s_cnt[ring], 1) == kConsumerWarps - 1;
+            last = atomicAdd(&s_cnt[ps], 1) == kConsumerWarps - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
@@ -559,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             float a0 = 0.0f, a8 = 0.0f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float2 v = part[((size_t)ring * kConsumerWarps + w) * 32 + lane];
+                const float2 v = part[((size_t)ps * kConsumerWarps + w) * 32 + lane];
                 a0 += v.x;
                 a8 += v.y;
             }
@@ -602,10 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 }
             }
             __syncwarp();
-            if (lane == 0) s_cnt[ring] = 0;
+            if (lane == 0) s_cnt[ps] = 0;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[ring]);  // after the sum: the partials stay until then
     }
 
     if constexpr (NORM) {
@@ -693,6 +800,9 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     prm.G = call.K / call.gs;
     if (prm.G % 4 != 0) return false;  // every region's scale rows 16-byte aligned
     prm.bpg = call.gs / kBlock;
+    if ((prm.bpg & (prm.bpg - 1)) != 0) return false;  // group of a block by a shift
+    prm.bpg_shift = 0;
+    while ((1 << prm.bpg_shift) < prm.bpg) ++prm.bpg_shift;
     prm.unit = 1;
     prm.n_units = call.N;
     if (grid > prm.n_units) grid = prm.n_units;
@@ -706,6 +816,7 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
         const int n = (b1 - 1) / prm.bpg - b0 / prm.bpg + 1;
         if (b1 > b0 && n > mg) mg = n;
     }
+    if (mg > 32) return false;  // the scratch fill maps a warp's groups onto its lanes
     prm.max_groups = mg > 0 ? mg : 1;
     prm.col_bytes = (uint32_t)call.K / 2u;
     const uint32_t reg_bytes = 8u * prm.col_bytes;  // a multiple of 512
@@ -719,9 +830,10 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     const uint32_t bar_bytes = (2 * kMaxStages + 2) * 8u + 2 * kMaxStages * 4u;
     const uint32_t part_per_stage = (uint32_t)kConsumerWarps * 32u * 8u;
     const uint32_t fixed = act_bytes + fx_bytes + 2u * call.nmat * rows_bytes + scr_bytes + misc_bytes + bar_bytes;
-    if (fixed + 2u * (stage + part_per_stage) > kSmemLimit) return false;
-    int S = (int)((kSmemLimit - fixed) / (stage + part_per_stage));
-    if (S > kMaxStages) S = kMaxStages;
+    // S ring entries and S + 1 partial buffers
+    if (fixed + part_per_stage + 2u * (stage + part_per_stage) > kSmemLimit) return false;
+    int S = (int)((kSmemLimit - fixed - part_per_stage) / (stage + part_per_stage));
+    if (S > kMaxStages - 1) S = kMaxStages - 1;
     prm.S = S;
     prm.stage_bytes = stage;
     uint32_t off = round_up((uint32_t)S * stage, 128u);
@@ -741,7 +853,7 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     prm.off_fx = off;
     off += fx_bytes;
     prm.off_part = off;
-    off += round_up((uint32_t)S * part_per_stage, 128u);
+    off += round_up((uint32_t)(S + 1) * part_per_stage, 128u);
     prm.off_scr = off;
     off += scr_bytes;
     prm.off_misc = off;
