@@ -33,25 +33,26 @@
 //
 // Decomposition:
 //   * Persistent grid, one CTA per SM, a contiguous range of whole columns per
-//     CTA (balanced in units whose scale/zero rows start 16-byte aligned).
-//   * One producer warp streams the CTA's scale/zero rows once, then the codes
-//     through a ring of stages.  A stage is one MMA tile: 16 columns (8 gate
-//     and 8 up columns for gate/up, 8 and 8 of the two matrices for dual),
-//     fetched as two bulk copies of 8 whole columns into two regions whose
-//     bases differ by 64 bytes mod 128, so that MMA rows g and g + 1 (lanes
-//     4g.. and 4g+4..) read disjoint bank halves.
-//   * The 8 consumer warps split each stage's K into 8 slices of whole
-//     128-code blocks.  Per stage a warp first copies the scale and zero of
-//     its groups for the tile's 16 columns into a private scratch area laid
-//     out for conflict-free reads, then runs its blocks; its partial sums go
-//     to a per-ring-entry buffer and the last warp to finish the stage (a
-//     shared counter) adds the 8 partials in warp order and writes the
-//     outputs.  Each warp releases its ring entry as soon as its blocks are
-//     done; the partial buffers (one more than ring entries) are reused only
-//     after their sum (see the stage loop).
+//     CTA; 8 consumer warps, a producer warp and a helper warp.
+//   * The producer streams the codes through a ring of S stages.  A stage is
+//     one MMA tile: 16 columns (8 gate and 8 up columns for gate/up, 8 and 8
+//     of the two matrices for dual), fetched as two bulk copies of 8 whole
+//     columns into two regions whose bases differ by 64 bytes mod 128, so
+//     that MMA rows g and g + 1 (lanes 4g.. and 4g+4..) read disjoint bank
+//     halves.  Stages beyond the ring are prefetched into L2.
+//   * The helper warp writes each stage's scale scratch ({s, z} per
+//     group and MMA row, read from global memory, laid out for conflict-free
+//     reads) and adds each stage's 8 partial sums in warp order, applies the
+//     norm's inverse RMS and the epilogue, and writes the outputs.
+//   * The consumer warps split each stage's K into 8 slices of whole 128-code
+//     blocks; per stage a warp waits for the codes and the scratch, runs its
+//     blocks, releases the ring entry and posts its partials to the ring
+//     entry's buffer.  A ring entry's scratch and partial buffer are rewritten
+//     for stage i only after the helper has summed stage i - S.
 //   * Programmatic dependent launch as in the one-lane kernel: the producer
-//     streams weights before the dependency wait, the consumers wait before
-//     reading activations; a kernel signals its dependents at its last stage.
+//     and the helper read weights before the dependency wait, the consumers
+//     wait before reading activations; a kernel signals its dependents at its
+//     last stage.
 //   * Every mbarrier wait is bounded in time; on expiry the kernel records an
 //     error in a device word (gq4_device_error), writes NaN and releases its
 //     stages.
@@ -75,11 +76,16 @@ __device__ unsigned int g_lanes_error = 0;
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;      // bulk copies of the codes
+constexpr int kHelperWarp = kConsumerWarps + 1;    // scale scratch, cross-warp sums, outputs
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kBar2Threads = (kConsumerWarps + 1) * 32;  // consumers + producer
 constexpr int kCT = kConsumerWarps * 32;
 constexpr int kMaxStages = 16;
 constexpr int kBlock = 128;  // codes per activation block (one scale exponent, one MMA run)
-constexpr uint32_t kSmemLimit = 220u * 1024u;
+constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
+constexpr int kMaxWarpBlocks = 4;   // 128-code blocks per consumer warp (K <= 4096)
+constexpr uint32_t kSmemLimit = 226u * 1024u;  // of the 227 KB a block may opt in to
 
 struct LanesParams {
     int M, K, N, gs;
@@ -91,11 +97,9 @@ struct LanesParams {
     int S;           // ring depth
     int unit;        // column granularity of the balanced split
     int n_units;
-    int max_groups;  // most groups any warp's K slice touches (scratch rows)
     uint32_t col_bytes;    // bytes of one column's codes (K / 2)
     uint32_t stage_bytes;
     uint32_t off_reg1;     // second region of a stage (64 mod 128)
-    uint32_t off_s[2], off_z[2];  // scale/zero rows of the CTA's range (per matrix)
     uint32_t off_act, off_fx, off_part, off_scr, off_misc, off_bar;
     const float *A;
     const float *A_b;
@@ -258,12 +262,12 @@ template <int NMAT, int PRO, int EPI, int NP>
 __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_constant__ LanesParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);
-    uint64_t *empty = full + kMaxStages;
-    uint64_t *srows = empty + kMaxStages;  // scale/zero rows landed
-    uint64_t *ready = srows + 1;           // consumers' prologue done
-    int *s_seq = reinterpret_cast<int *>(ready + 1);  // stage a ring entry holds
-    int *s_cnt = s_seq + kMaxStages;                  // warps done with a partial buffer
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // codes of a stage landed
+    uint64_t *empty = full + kMaxStages;   // the consumer warps are done with a ring entry
+    uint64_t *sfull = empty + kMaxStages;  // the helper wrote a ring entry's scale scratch
+    uint64_t *pbar = sfull + kMaxStages;   // the consumer warps wrote a ring entry's partials
+    uint64_t *aload = pbar + kMaxStages;   // the consumer warps' activation loads returned
+    int *s_seq = reinterpret_cast<int *>(aload + 1);  // stage a ring entry holds
     float *s_inv = reinterpret_cast<float *>(smem + p.off_misc);        // [4] inverse RMS per lane
     float *s_sq = s_inv + 4;                                            // [8 warps][4] square sums
     unsigned char *s_act = smem + p.off_act;
@@ -285,34 +289,25 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // =====================================================================
     // Producer warp.
     // =====================================================================
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             for (int s = 0; s < p.S; ++s) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
+                mbar_init(&sfull[s], 1);
+                mbar_init(&pbar[s], kConsumerWarps);
                 s_seq[s] = -1;
             }
-            for (int s = 0; s <= p.S; ++s) s_cnt[s] = 0;  // S + 1 partial buffers
-            mbar_init(srows, 1);
-            mbar_init(ready, 1);
+            mbar_init(aload, kConsumerWarps);
             mbar_fence_init();
         }
         __syncwarp();
-        lanes_bar_arrive(2, kThreads);
+        lanes_bar_arrive(4, kBar2Threads);  // the consumers' first mbarrier use (aload)
+        lanes_bar_arrive(2, kBar2Threads);  // the consumers' barrier after their prologue
+        lanes_bar_arrive(3, 64);            // the helper's
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
-            {
-                // the CTA's scale and zero rows, one copy per array (the
-                // range starts 16-byte aligned and G is a multiple of 4)
-                const uint32_t bytes = (uint32_t)ncols * (uint32_t)p.G * 4u;
-                mbar_arrive_expect_tx(srows, (uint32_t)NMAT * 2u * bytes);
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    bulk_g2s(smem + p.off_s[m], p.scales[m] + (size_t)col_begin * p.G, bytes, srows);
-                    bulk_g2s(smem + p.off_z[m], p.zeros[m] + (size_t)col_begin * p.G, bytes, srows);
-                }
-            }
             // the codes of stage i as (first column, count) per region
             auto stage_regions = [&](int i, int (&rc)[2], int (&rn)[2]) {
                 const int c0 = col_begin + i * TCOLS;
@@ -327,17 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     rn[1] = nc - rn[0];
                 }
             };
-            // Stages beyond the ring are prefetched into L2 (up to S ahead of
-            // the stage being copied), so that a ring entry's refill reads L2:
-            // more bytes in flight than the ring holds.  Not before the
-            // consumers' prologue, whose activation loads go first.
-            int pf = p.S;  // next stage to prefetch
+            // Two stages go out at once; the rest once the consumers'
+            // activation loads have returned (they are not queued behind the
+            // weight stream), while the consumers still stage activations.
+            // From then on stages up to kPrefetchAhead ahead are prefetched
+            // into L2, so a ring entry's refill reads L2 and the weight
+            // stream runs through the prologue: more bytes in flight than
+            // the ring holds.
+            int pf = 3;  // next stage to prefetch
             for (int i = 0; ok && i < n_stages; ++i) {
                 const int slot = i % p.S;
-                // two stages go out at once, the rest after the consumers'
-                // prologue (its activation loads are not queued behind the
-                // whole ring's weight copies)
-                if (i == 2 && !mbar_wait(ready, 0)) {
+                if (i == 2 && !mbar_wait(aload, 0)) {
                     lanes_error();
                     ok = false;
                     break;
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 }
                 issued = i + 1;
                 if (i >= 2) {
-                    for (; pf < n_stages && pf <= i + p.S; ++pf) {
+                    for (; pf < n_stages && pf <= i + kPrefetchAhead; ++pf) {
                         int pc[2], pn[2];
                         stage_regions(pf, pc, pn);
                         if constexpr (NMAT == 2) {
@@ -378,10 +373,127 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             }
             if (!ok) {
                 // leave no copy in flight into this CTA's shared memory
-                (void)mbar_wait(srows, 0);
                 for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
                     (void)mbar_wait(&full[i % p.S], (i / p.S) & 1);
             }
+        }
+        return;
+    }
+
+    // =====================================================================
+    // Helper warp.  Per stage i, after the sum of stage i - S (whose scratch
+    // and partial buffer share ring entry i mod S): the scale scratch of stage
+    // i, {s, z} per [group][MMA row], read from global memory
+    // (the scales are weights: no dependency wait).  The sum of a stage adds
+    // the 8 consumer warps' partials in warp order, applies the norm's
+    // inverse RMS and writes the outputs (its lane l mirrors consumer lane l:
+    // MMA rows g and g + 8, decode lane t).  The consumers of stage i wait for
+    // its scratch, so they write stage i's partials only after the sum of
+    // stage i - S has read the buffer.
+    // =====================================================================
+    if (warp == kHelperWarp) {
+        lanes_bar(3, 64);  // the producer has initialised the mbarriers
+        const int g = lane >> 2, t = lane & 3;
+        const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
+        const bool lane_ok = t < p.M;
+        const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [S][warps][32]
+        bool hfail = false;
+        // the scale and zero of stage i's 16 MMA rows, lane = group (G <= 32)
+        auto load_scales = [&](int i, float (&sv)[16], float (&zv)[16]) {
+            const int lc0 = i * TCOLS;
+            const bool ok = lane < p.G;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                int m, lc;
+                if constexpr (NMAT == 2) {
+                    m = r & 1;
+                    lc = lc0 + (r >> 1);
+                } else {
+                    m = 0;
+                    lc = lc0 + 8 * (r & 1) + (r >> 1);
+                }
+                lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
+                const size_t si = (size_t)(col_begin + lc) * p.G + lane;
+                sv[r] = ok ? __ldg(p.scales[m] + si) : 0.0f;
+                zv[r] = ok ? __ldg(p.zeros[m] + si) : 0.0f;
+            }
+        };
+        // the sum of stage j's partials and its outputs
+        auto reduce_stage = [&](int j) {
+            const int slot = j % p.S;
+            if (!hfail && !__all_sync(0xffffffffu, mbar_wait(&pbar[slot], (j / p.S) & 1))) {
+                lanes_error();
+                hfail = true;
+            }
+            float a0 = 0.0f, a8 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float2 v = part[((size_t)slot * kConsumerWarps + w) * 32 + lane];
+                a0 += v.x;
+                a8 += v.y;
+            }
+            if constexpr (NORM) {
+                const float inv = s_inv[t];
+                a0 *= inv;
+                a8 *= inv;
+            }
+            if (hfail) a0 = a8 = __int_as_float(0x7fffffff);
+            const int c0 = col_begin + j * TCOLS;
+            if constexpr (EPI == kEpiGated) {
+                // even g: gate rows; g + 1 (4 lanes on): the up rows of the same columns
+                const float u0 = __shfl_down_sync(0xffffffffu, a0, 4);
+                const float u8 = __shfl_down_sync(0xffffffffu, a8, 4);
+                if ((g & 1) == 0 && lane_ok) {
+                    const int ca = c0 + ci, cb = c0 + ci + 4;
+                    if (ca < col_end) p.out[0][(size_t)t * p.N + ca] = a0 / (1.0f + expf(-a0)) * u0;
+                    if (cb < col_end) p.out[0][(size_t)t * p.N + cb] = a8 / (1.0f + expf(-a8)) * u8;
+                }
+            } else if constexpr (EPI == kEpiDual) {
+                if (lane_ok) {
+                    float *o = p.out[g & 1];
+                    const int ca = c0 + ci, cb = c0 + ci + 4;
+                    if (ca < col_end) o[(size_t)t * p.N + ca] = a0;
+                    if (cb < col_end) o[(size_t)t * p.N + cb] = a8;
+                }
+            } else {
+                if (lane_ok) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = c0 + 8 * (g & 1) + ci + 4 * h;
+                        if (col >= col_end) continue;
+                        const float v = h ? a8 : a0;
+                        if constexpr (EPI == kEpiQuad) {
+                            const int seg = col < p.seg_start[1] ? 0 : col < p.seg_start[2] ? 1
+                                          : col < p.seg_start[3] ? 2 : 3;
+                            p.out[seg][(size_t)t * p.seg_len[seg] + (col - p.seg_start[seg])] = v;
+                        } else {
+                            p.out[0][(size_t)t * p.N + col] = v;
+                        }
+                    }
+                }
+            }
+        };
+        // one step: the loads of stage i + 1 go out first, then the sum of
+        // stage i - S (freeing ring entry i mod S), then stage i's scratch
+        auto step = [&](int i, float (&sv)[16], float (&zv)[16], float (&sn)[16], float (&zn)[16]) {
+            if (i + 1 < n_stages) load_scales(i + 1, sn, zn);
+            if (i >= p.S) reduce_stage(i - p.S);
+            if (i < n_stages) {
+                const int slot = i % p.S;
+                float2 *scr = reinterpret_cast<float2 *>(smem + p.off_scr) + (size_t)slot * p.G * 16;
+                if (lane < p.G) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) scr[lane * 16 + r] = make_float2(sv[r], zv[r]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfull[slot]);
+            }
+        };
+        float s0[16], z0[16], s1[16], z1[16];
+        if (n_stages > 0) load_scales(0, s0, z0);
+        for (int i = 0; i < n_stages + p.S; i += 2) {
+            step(i, s0, z0, s1, z1);
+            if (i + 1 < n_stages + p.S) step(i + 1, s1, z1, s0, z0);
         }
         return;
     }
@@ -417,6 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int wsl = lane >> 1;
     // this lane's 8 bytes within a block's B area, lane 0 of the MMA's N
     const uint32_t act_lane = (uint32_t)(wsl & 3) * (2 * NP) * 64u + (uint32_t)(wsl >> 2) * 16u + 8u * par;
+    // every consumer thread passes named barrier 4 once, before any mbarrier
+    // use: the producer arrives there after initialising the mbarriers
+    lanes_bar(4, kBar2Threads);
+    bool arrived = 4 * warp >= p.KB;  // a warp without k-blocks signals at once
+    if (arrived && lane == 0) mbar_arrive(aload);
     for (int kb0 = 4 * warp; kb0 < p.KB; kb0 += 4 * kConsumerWarps) {
         float4 va[U], vb[U], vg[4];
 #pragma unroll
@@ -460,6 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             mb[u] = max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
                         max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu));
             smv[u] = (v.x + v.y) + (v.z + v.w);
+        }
+        if (!arrived) {  // this warp's first activation loads have returned
+            arrived = true;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(aload);
         }
         // the scale of the lane's own unit, then of every unit from its owner
         const uint32_t mown = reduce_scatter<U>(mb, lane, OpMax());
@@ -527,192 +649,119 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
         }
     }
-    lanes_bar(2, kThreads);  // activations staged; the producer has initialised the mbarriers
-    if (ctid == 0) mbar_arrive(ready);
+    lanes_bar(2, kBar2Threads);  // activations staged; the producer has initialised the mbarriers
 
     // =====================================================================
     // Consumer warps: stages.
     // =====================================================================
     // `failed` stays uniform across each warp: the MMAs need every lane
-    bool failed = !__all_sync(0xffffffffu, mbar_wait(srows, 0));
-    if (failed) lanes_error();
+    bool failed = false;
     const int g = lane >> 2, t = lane & 3;
-    // this warp's K slice: blocks [bw0, bw1), groups [gw0, gw1)
+    // this warp's K slice: blocks [bw0, bw1)
     const int bw0 = (int)((long long)p.KB * warp / kConsumerWarps);
     const int bw1 = (int)((long long)p.KB * (warp + 1) / kConsumerWarps);
-    const int gw0 = bw0 / p.bpg;
-    const int ngw = bw1 > bw0 ? (bw1 - 1) / p.bpg - gw0 + 1 : 0;
-    float4 *scr = reinterpret_cast<float4 *>(smem + p.off_scr) + (size_t)warp * p.max_groups * 16;
-    // scratch fill: lane -> (row fr, group fj), rpp rows per pass (ngw <= 32)
-    const int rpp = ngw > 0 ? 32 / ngw : 1;
-    const int fr = ngw > 0 ? lane / ngw : 0;
-    const int fj = (ngw > 0 && fr < rpp) ? lane - fr * ngw : -1;
     float2 *part = reinterpret_cast<float2 *>(smem + p.off_part);  // [S][warps][32]
-    const float inv_t = NORM ? s_inv[t] : 1.0f;
     // MMA rows g and g + 8: region g & 1, columns (g >> 1) and (g >> 1) + 4 of it
     const uint32_t row_off = ((g & 1) ? p.off_reg1 : 0u) + (uint32_t)(g >> 1) * p.col_bytes;
     const uint32_t row8_delta = 4u * p.col_bytes;
     const uint32_t b_lane_off = (uint32_t)(g * 4 + t) * 16u;
     const bool b_active = g < 2 * NP;
+    // The warp's K slice is the same in every stage: its B fragments and
+    // block factors stay in registers (at most kMaxWarpBlocks blocks).
+    const int nb = bw1 - bw0;
+    uint4 bqc[kMaxWarpBlocks][4];
+    float4 fxc[kMaxWarpBlocks];
+#pragma unroll
+    for (int u = 0; u < kMaxWarpBlocks; ++u) {
+        const int b = bw0 + (u < nb ? u : 0);
+        const unsigned char *bp = s_act + (size_t)b * 4 * (2 * NP * 64) + b_lane_off;
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr)
+            bqc[u][pr] = (b_active && u < nb) ? *reinterpret_cast<const uint4 *>(bp + pr * (2 * NP * 64))
+                                              : make_uint4(0u, 0u, 0u, 0u);
+        // {2^(24-k), sum h 2^-24, sum l 2^-24, sum x} of lane t's block
+        fxc[u] = u < nb ? s_fx[b * 4 + t] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
 
     for (int i = 0; i < n_stages; ++i) {
         if (i == n_stages - 1 && lane == 0) lanes_dependents_launch();
         const int ring = i % p.S;
-        const int c0 = col_begin + i * TCOLS;
-        const int lc0 = i * TCOLS;  // CTA-relative first column of the stage
-        if (!failed && !__all_sync(0xffffffffu, wait_shared_eq(&s_seq[ring], i) &&
-                                                    mbar_wait(&full[ring], (i / p.S) & 1))) {
+        const uint32_t ph = (uint32_t)(i / p.S) & 1u;
+        if (!failed && !__all_sync(0xffffffffu, wait_shared_eq(&s_seq[ring], i) && mbar_wait(&full[ring], ph) &&
+                                                    mbar_wait(&sfull[ring], ph))) {
             lanes_error();
             failed = true;
         }
         const unsigned char *st = smem + (size_t)ring * p.stage_bytes;
-
-        // scale and zero of this warp's groups for the tile's 16 MMA rows:
-        // {s, z - zi, zi, 0}, lanes (row, group) = (fr + rpp i, fj)
-        for (int r = fr; fj >= 0 && r < 16; r += rpp) {
-            int m, lc;
-            if constexpr (NMAT == 2) {
-                m = r & 1;
-                lc = lc0 + (r >> 1);
-            } else {
-                m = 0;
-                lc = lc0 + 8 * (r & 1) + (r >> 1);
-            }
-            lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
-            const size_t si = (size_t)lc * p.G + gw0 + fj;
-            const float sv = reinterpret_cast<const float *>(smem + p.off_s[m])[si];
-            const float z = reinterpret_cast<const float *>(smem + p.off_z[m])[si];
-            const float zi = rintf(fminf(fmaxf(z, 0.0f), 15.0f));
-            scr[fj * 16 + r] = make_float4(sv, z - zi, zi, 0.0f);
-        }
-        __syncwarp();
+        // {s, z} per [group][MMA row] of this stage
+        const float2 *scr = reinterpret_cast<const float2 *>(smem + p.off_scr) + (size_t)ring * p.G * 16;
 
         float y0 = 0.0f, y8 = 0.0f;
         if (!failed) {
             const unsigned char *ra = st + row_off;
-            // two blocks at a time: all their shared-memory loads first, then
-            // four independent MMA chains (a repeated last block is discarded)
-            for (int b = bw0; b < bw1; b += 2) {
-                const bool two = b + 1 < bw1;
-                const int bb[2] = {b, two ? b + 1 : b};
-                uint4 wa[2], wb[2], bq[2][4];
-                float4 fx[2], sz0[2], sz8[2];
+            // two blocks at a time: their codes and scales first, then four
+            // independent MMA chains (a repeated last block is discarded)
+#pragma unroll
+            for (int u0 = 0; u0 < kMaxWarpBlocks; u0 += 2) {
+                if (u0 >= nb) break;
+                const bool two = u0 + 1 < nb;
+                const int bb[2] = {bw0 + u0, bw0 + (two ? u0 + 1 : u0)};
+                uint4 wa[2], wb[2];
+                float2 sz0[2], sz8[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     wa[u] = *reinterpret_cast<const uint4 *>(ra + bb[u] * 64 + t * 16);
                     wb[u] = *reinterpret_cast<const uint4 *>(ra + row8_delta + bb[u] * 64 + t * 16);
-                    const unsigned char *bp = s_act + (size_t)bb[u] * 4 * (2 * NP * 64) + b_lane_off;
-#pragma unroll
-                    for (int pr = 0; pr < 4; ++pr)
-                        bq[u][pr] = b_active ? *reinterpret_cast<const uint4 *>(bp + pr * (2 * NP * 64))
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                    // {2^(24-k), sum h 2^-24, sum l 2^-24, sum x} of lane t's block
-                    fx[u] = s_fx[bb[u] * 4 + t];
-                    const int j = (bb[u] >> p.bpg_shift) - gw0;
-                    sz0[u] = scr[j * 16 + g];  // {s, z - zi, zi, 0} of row g
+                    const int j = bb[u] >> p.bpg_shift;
+                    sz0[u] = scr[j * 16 + g];  // {s, z} of row g
                     sz8[u] = scr[j * 16 + g + 8];
                 }
                 float d1[2][4], d2[2][4];
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d1[u][i] = d2[u][i] = 0.0f;
+                    for (int k = 0; k < 4; ++k) d1[u][k] = d2[u][k] = 0.0f;
 #pragma unroll
                 for (int pr = 0; pr < 4; ++pr) {
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
+                        const uint4 bq = bqc[u0 + u][pr];
                         const uint32_t w0 = pr == 0 ? wa[u].x : pr == 1 ? wa[u].y : pr == 2 ? wa[u].z : wa[u].w;
                         const uint32_t w8 = pr == 0 ? wb[u].x : pr == 1 ? wb[u].y : pr == 2 ? wb[u].z : wb[u].w;
                         mma_f16(d1[u], w0 & 0x000F000Fu, w8 & 0x000F000Fu, w0 & 0x00F000F0u, w8 & 0x00F000F0u,
-                                bq[u][pr].x, bq[u][pr].y);
+                                bq.x, bq.y);
                         const uint32_t v0 = w0 >> 8, v8 = w8 >> 8;
                         mma_f16(d2[u], v0 & 0x000F000Fu, v8 & 0x000F000Fu, v0 & 0x00F000F0u, v8 & 0x00F000F0u,
-                                bq[u][pr].z, bq[u][pr].w);
+                                bq.z, bq.w);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     if (u == 1 && !two) break;
+                    const float4 fx = fxc[u0 + u];
+                    // zi: the zero's integer part (clamped to the code range)
+                    const float zi0 = rintf(fminf(fmaxf(sz0[u].y, 0.0f), 15.0f));
+                    const float zi8 = rintf(fminf(fmaxf(sz8[u].y, 0.0f), 15.0f));
                     // exact: sum (q - zi) h and sum (q - zi) l, times 2^-24
-                    const float h0 = fmaf(-sz0[u].z, fx[u].y, d1[u][0] + d2[u][0]);
-                    const float l0 = fmaf(-sz0[u].z, fx[u].z, d1[u][1] + d2[u][1]);
-                    const float h8 = fmaf(-sz8[u].z, fx[u].y, d1[u][2] + d2[u][2]);
-                    const float l8 = fmaf(-sz8[u].z, fx[u].z, d1[u][3] + d2[u][3]);
+                    const float h0 = fmaf(-zi0, fx.y, d1[u][0] + d2[u][0]);
+                    const float l0 = fmaf(-zi0, fx.z, d1[u][1] + d2[u][1]);
+                    const float h8 = fmaf(-zi8, fx.y, d1[u][2] + d2[u][2]);
+                    const float l8 = fmaf(-zi8, fx.z, d1[u][3] + d2[u][3]);
                     // y += s * (sum (q - zi) x - (z - zi) X)
-                    y0 = fmaf(sz0[u].x, fmaf(-sz0[u].y, fx[u].w, fmaf(h0, 2048.0f, l0) * fx[u].x), y0);
-                    y8 = fmaf(sz8[u].x, fmaf(-sz8[u].y, fx[u].w, fmaf(h8, 2048.0f, l8) * fx[u].x), y8);
+                    y0 = fmaf(sz0[u].x, fmaf(zi0 - sz0[u].y, fx.w, fmaf(h0, 2048.0f, l0) * fx.x), y0);
+                    y8 = fmaf(sz8[u].x, fmaf(zi8 - sz8[u].y, fx.w, fmaf(h8, 2048.0f, l8) * fx.x), y8);
                 }
             }
         }
 
-        // this warp is done with the stage's codes
+        // this warp is done with the stage's codes and scratch
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[ring]);
-
-        // ---- cross-warp sum: S + 1 partial buffers, the last warp adds ----
-        // A warp reaches stage i + S + 1 (the next user of buffer i mod
-        // (S + 1)) only after every warp released stage i + 1, and the last
-        // warp of stage i releases stage i + 1 only after its sum of stage i.
-        const int ps = i % (p.S + 1);
-        part[((size_t)ps * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
+        // its partial sums go to the helper warp (buffer of this ring entry)
+        if (failed) y0 = y8 = __int_as_float(0x7fffffff);
+        part[((size_t)ring * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
         __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(&s_cnt[ps], 1) == kConsumerWarps - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence_block();
-            float a0 = 0.0f, a8 = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float2 v = part[((size_t)ps * kConsumerWarps + w) * 32 + lane];
-                a0 += v.x;
-                a8 += v.y;
-            }
-            a0 *= inv_t;
-            a8 *= inv_t;
-            if (failed) a0 = a8 = __int_as_float(0x7fffffff);
-            const bool lane_ok = t < p.M;
-            const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
-            if constexpr (EPI == kEpiGated) {
-                // even g: gate rows; g + 1 (4 lanes on): the up rows of the same columns
-                const float u0 = __shfl_down_sync(0xffffffffu, a0, 4);
-                const float u8 = __shfl_down_sync(0xffffffffu, a8, 4);
-                if ((g & 1) == 0 && lane_ok) {
-                    const int ca = c0 + ci, cb = c0 + ci + 4;
-                    if (ca < col_end) p.out[0][(size_t)t * p.N + ca] = a0 / (1.0f + expf(-a0)) * u0;
-                    if (cb < col_end) p.out[0][(size_t)t * p.N + cb] = a8 / (1.0f + expf(-a8)) * u8;
-                }
-            } else if constexpr (EPI == kEpiDual) {
-                if (lane_ok) {
-                    float *o = p.out[g & 1];
-                    const int ca = c0 + ci, cb = c0 + ci + 4;
-                    if (ca < col_end) o[(size_t)t * p.N + ca] = a0;
-                    if (cb < col_end) o[(size_t)t * p.N + cb] = a8;
-                }
-            } else {
-                if (lane_ok) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int col = c0 + 8 * (g & 1) + ci + 4 * h;
-                        if (col >= col_end) continue;
-                        const float v = h ? a8 : a0;
-                        if constexpr (EPI == kEpiQuad) {
-                            const int seg = col < p.seg_start[1] ? 0 : col < p.seg_start[2] ? 1
-                                          : col < p.seg_start[3] ? 2 : 3;
-                            p.out[seg][(size_t)t * p.seg_len[seg] + (col - p.seg_start[seg])] = v;
-                        } else {
-                            p.out[0][(size_t)t * p.N + col] = v;
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) s_cnt[ps] = 0;
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(&pbar[ring]);
     }
 
     if constexpr (NORM) {
@@ -748,7 +797,7 @@ cudaError_t launch_lanes_variant(const LanesParams &prm, size_t smem, cudaStream
     constexpr int kMaxDevices = 64;
     static std::atomic<unsigned char> smem_ready[kMaxDevices];
     if (dev < 0 || dev >= kMaxDevices || !smem_ready[dev].load(std::memory_order_acquire)) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kSmemLimit + 4096u));
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
         if (err != cudaSuccess) return err;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                    (int)cudaSharedmemCarveoutMaxShared);
@@ -798,70 +847,50 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     prm.KW = call.K / 8;
     prm.KB = call.K / kBlock;
     prm.G = call.K / call.gs;
-    if (prm.G % 4 != 0) return false;  // every region's scale rows 16-byte aligned
     prm.bpg = call.gs / kBlock;
     if ((prm.bpg & (prm.bpg - 1)) != 0) return false;  // group of a block by a shift
     prm.bpg_shift = 0;
     while ((1 << prm.bpg_shift) < prm.bpg) ++prm.bpg_shift;
+    if (prm.G > 32) return false;  // the helper holds a stage's scales as one group per lane
+    // each consumer warp keeps its slice's activations in registers
+    if ((prm.KB + kConsumerWarps - 1) / kConsumerWarps > kMaxWarpBlocks) return false;
     prm.unit = 1;
     prm.n_units = call.N;
-    if (grid > prm.n_units) grid = prm.n_units;
-    const int max_cols = (prm.n_units + grid - 1) / grid;
     const int NP = call.M <= 2 ? 2 : 4;
-    // the most groups a warp's slice of whole blocks touches
-    int mg = 0;
-    for (int w = 0; w < kConsumerWarps; ++w) {
-        const int b0 = (int)((long long)prm.KB * w / kConsumerWarps);
-        const int b1 = (int)((long long)prm.KB * (w + 1) / kConsumerWarps);
-        const int n = (b1 - 1) / prm.bpg - b0 / prm.bpg + 1;
-        if (b1 > b0 && n > mg) mg = n;
-    }
-    if (mg > 32) return false;  // the scratch fill maps a warp's groups onto its lanes
-    prm.max_groups = mg > 0 ? mg : 1;
     prm.col_bytes = (uint32_t)call.K / 2u;
     const uint32_t reg_bytes = 8u * prm.col_bytes;  // a multiple of 512
     prm.off_reg1 = reg_bytes + 64u;
     const uint32_t stage = round_up(prm.off_reg1 + reg_bytes, 128u);
     const uint32_t act_bytes = (uint32_t)prm.KB * 4u * (uint32_t)(2 * NP) * 64u;
     const uint32_t fx_bytes = (uint32_t)prm.KB * 4u * 16u;
-    const uint32_t rows_bytes = round_up((uint32_t)max_cols * (uint32_t)prm.G * 4u, 128u);
-    const uint32_t scr_bytes = round_up((uint32_t)kConsumerWarps * prm.max_groups * 16u * 16u, 128u);
     const uint32_t misc_bytes = 256u;
-    const uint32_t bar_bytes = (2 * kMaxStages + 2) * 8u + 2 * kMaxStages * 4u;
+    const uint32_t bar_bytes = (4 * kMaxStages + 1) * 8u + kMaxStages * 4u;
+    // per ring entry: the codes, the scale scratch [G][16 rows] {s, z}
+    // and the consumer warps' partial sums
+    const uint32_t scr_per_stage = (uint32_t)prm.G * 16u * 8u;
     const uint32_t part_per_stage = (uint32_t)kConsumerWarps * 32u * 8u;
-    const uint32_t fixed = act_bytes + fx_bytes + 2u * call.nmat * rows_bytes + scr_bytes + misc_bytes + bar_bytes;
-    // S ring entries and S + 1 partial buffers
-    if (fixed + part_per_stage + 2u * (stage + part_per_stage) > kSmemLimit) return false;
-    int S = (int)((kSmemLimit - fixed - part_per_stage) / (stage + part_per_stage));
-    if (S > kMaxStages - 1) S = kMaxStages - 1;
+    const uint32_t per_stage = stage + scr_per_stage + part_per_stage;
+    const uint32_t fixed = act_bytes + fx_bytes + misc_bytes + bar_bytes + 3u * 128u;
+    if (fixed + 2u * per_stage > kSmemLimit) return false;
+    int S = (int)((kSmemLimit - fixed) / per_stage);
+    if (S > kMaxStages) S = kMaxStages;
     prm.S = S;
     prm.stage_bytes = stage;
     uint32_t off = round_up((uint32_t)S * stage, 128u);
-    for (int m = 0; m < 2; ++m) {
-        if (m < call.nmat) {
-            prm.off_s[m] = off;
-            off += rows_bytes;
-            prm.off_z[m] = off;
-            off += rows_bytes;
-        } else {
-            prm.off_s[m] = prm.off_s[0];
-            prm.off_z[m] = prm.off_z[0];
-        }
-    }
     prm.off_act = off;
     off += act_bytes;
     prm.off_fx = off;
-    off += fx_bytes;
+    off += round_up(fx_bytes, 128u);
     prm.off_part = off;
-    off += round_up((uint32_t)(S + 1) * part_per_stage, 128u);
+    off += round_up((uint32_t)S * part_per_stage, 128u);
     prm.off_scr = off;
-    off += scr_bytes;
+    off += round_up((uint32_t)S * scr_per_stage, 128u);
     prm.off_misc = off;
     off += misc_bytes;
     prm.off_bar = off;
     off += bar_bytes;
     smem = off;
-    return smem <= kSmemLimit + 4096u;
+    return smem <= kSmemLimit;
 }
 
 }  // namespace
@@ -869,10 +898,6 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
 bool lanes_path_supported(const Call &call)
 {
     if (call.M < 2 || call.M > 4) return false;
-    for (int m = 0; m < call.nmat; ++m) {
-        if ((reinterpret_cast<uintptr_t>(call.scales[m]) & 15u) != 0) return false;
-        if ((reinterpret_cast<uintptr_t>(call.zeros[m]) & 15u) != 0) return false;
-    }
     // the variants launch_lanes instantiates
     const int pro = prologue_of(call);
     const bool variant = call.epi == kEpiStore ||

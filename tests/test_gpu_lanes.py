@@ -37,7 +37,7 @@ MATVEC_CASES = [
     (2, 256, 16, 128),       # one full tile
     (3, 1152, 17, 128),      # K not a multiple of 256, a ragged second tile
     (4, 4096, 4096, 128),    # the stack's O projection at M = 4
-    (2, 6144, 300, 256),     # two blocks per group
+    (2, 4096, 300, 256),     # two blocks per group
     (4, 2048, 33, 512),      # a warp's two blocks inside one group
     (3, 512, 7, 128),        # fewer columns than SMs
     (4, 1024, 152 * 16 + 5, 128),  # every CTA with a ragged range
