@@ -67,8 +67,8 @@
  *   - Outputs must not overlap each other or any input (GQ4_ERR_ALIAS).
  *   - Launches are asynchronous on `stream` (0 = the legacy default stream).
  *     Stream order holds for activations, norm inputs and outputs.  One
- *     exception for weights: calls with M = 1 or 16 <= M <= 32 are launched
- *     with programmatic dependent launch, so such a call may start reading
+ *     exception for weights: calls with M <= 4 or 16 <= M <= 32 may be
+ *     launched with programmatic dependent launch, so such a call may start reading
  *     its Bq, scales and zeros before the kernel just before it on the same
  *     stream has completed: while it runs, if it is one of these matvecs
  *     (which signal early), else once its blocks have exited.  Hence:
@@ -82,8 +82,17 @@
  *         (an event wait, a copy) or a host synchronisation in between.
  *   - Results are deterministic: the same inputs give the same bits.
  *   - A NaN or infinite activation makes every output whose dot product uses
- *     it non-finite (NaN at M = 1).
- *   - Arithmetic: with 2 <= M <= 15 lanes every product and sum is f32
+ *     it non-finite (NaN at M = 1 and on the 2..4-lane kernel below).
+ *   - Arithmetic: with 2 <= M <= 4 lanes, a group size that is a power-of-
+ *     two multiple of 128, K a multiple of 128 up to 4096 and at most 32
+ *     groups per column, each 128-code block of a lane's activations is held
+ *     as 22-bit fixed point with a power-of-two scale (each value within
+ *     2^-22 of the block's largest magnitude), split into two pieces exact
+ *     in fp16, and the tensor core's warp-level MMA sums the products
+ *     exactly (every partial sum an integer times 2^-24 below 2^24 of them);
+ *     the bound below holds unless a block holds an activation some 2^10
+ *     times larger than the ones that carry the result.  Other 2 <= M <= 15
+ *     calls: every product and sum is f32
  *     (|error| <= 1e-4 * sum_k |a_k w_k| + 1e-6 against the exact dot
  *     product).  With M = 1 each 64-code group of activations is held as
  *     24-bit fixed point with a power-of-two scale (each value within
@@ -388,7 +397,9 @@ GQ4_API gq4_status gq4_dequant(int K, int N, int group_size, const uint32_t *Bq,
  * inside the kernels is bounded in time, so a broken copy cannot hang the
  * GPU; the outputs of that call are then invalid), bit 3 when gq4_quantize
  * met a group with a non-finite value or range, bit 4 when gq4_embedding met
- * an id outside its table; bit 1 also covers the GEMM kernel of gq4_gemm.  Copies the word to
+ * an id outside its table, bit 5 when the 2..4-lane kernel gave up waiting
+ * for a copy, its scale scratch or its warps' partial sums; bit 1 also
+ * covers the GEMM kernel of gq4_gemm.  Copies the word to
  * *bits (synchronous, device-wide) and clears it when clear != 0.  Not for
  * the hot path: a diagnostic to call after a suspicious result. */
 GQ4_API gq4_status gq4_device_error(unsigned int *bits, int clear);
