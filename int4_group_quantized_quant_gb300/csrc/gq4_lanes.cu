@@ -75,7 +75,7 @@ __device__ unsigned int g_lanes_error = 0;
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;
 constexpr int kProducerWarp = kConsumerWarps;      // bulk copies of the codes
 constexpr int kHelperWarp = kConsumerWarps + 1;    // scale scratch, cross-warp sums, outputs
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
@@ -84,7 +84,8 @@ constexpr int kCT = kConsumerWarps * 32;
 constexpr int kMaxStages = 16;
 constexpr int kBlock = 128;  // codes per activation block (one scale exponent, one MMA run)
 constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
-constexpr int kMaxWarpBlocks = 4;   // 128-code blocks per consumer warp (K <= 4096)
+constexpr int kMaxWarpBlocks = 3;   // 128-code blocks per consumer warp (K <= 4608)
+constexpr int kPrologueBlocks = 2;  // k-blocks per warp per prologue pass
 constexpr uint32_t kSmemLimit = 226u * 1024u;  // of the 227 KB a block may opt in to
 
 struct LanesParams {
@@ -135,6 +136,53 @@ __device__ __forceinline__ void lanes_dependency_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Cluster helpers (CTA pairs share the activation staging).
+__device__ __forceinline__ uint32_t lanes_cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address of the same location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t lanes_mapa(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Every thread of the cluster arrives once (split barrier: arrive, later wait).
+__device__ __forceinline__ void lanes_cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void lanes_cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores into a peer CTA's shared memory that complete on its mbarrier's
+// transaction count (addresses from lanes_mapa).
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, uint32_t a, uint32_t b, uint32_t rbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 ::"r"(raddr), "r"(a), "r"(b), "r"(rbar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t rbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+                 ::"r"(raddr), "f"(v), "r"(rbar) : "memory");
+}
+
 __device__ __forceinline__ void lanes_error()
 {
     atomicOr(&g_lanes_error, 32u);
@@ -176,33 +224,33 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Reduce-scatter of U values per lane (U = 8 or 16) over the 32 lanes of a
-// warp: afterwards lane l holds the reduction of unit unit_of(l) over all 32
-// lanes (U = 16: unit (l >> 1) & 15, held by lanes 2u and 2u + 1; U = 8: unit
-// (l >> 2) & 7, held by lanes 4u .. 4u + 3).  A fixed order of operations, so
-// the result is the same whatever the units hold.
+// Reduce-scatter of U values per lane (U = 4, 8 or 16) over the 32 lanes of
+// a warp: afterwards lane l holds the reduction of unit (l / (32/U)) over all
+// 32 lanes, as do the other 32/U - 1 lanes of its run (unit u's run starts at
+// lane 32u/U).  A fixed order of operations, so the result is the same
+// whatever the units hold.
 template <int U>
 __device__ __forceinline__ int rs_unit(int lane)
 {
-    return U == 16 ? (lane >> 1) & 15 : (lane >> 2) & 7;
+    return lane / (32 / U);
 }
 
 template <int U>
 __device__ __forceinline__ int rs_owner(int u)
 {
-    return U == 16 ? 2 * u : 4 * u;
+    return u * (32 / U);
 }
 
 template <int U, class T, class Op>
 __device__ __forceinline__ T reduce_scatter(const T (&v)[U], int lane, Op op)
 {
-    static_assert(U == 8 || U == 16, "units per warp");
+    static_assert(U == 4 || U == 8 || U == 16, "units per warp");
     T a[U];
 #pragma unroll
     for (int i = 0; i < U; ++i) a[i] = v[i];
     int n = U;
 #pragma unroll
-    for (int off = 16; off >= (U == 16 ? 2 : 4); off >>= 1) {
+    for (int off = 16; off >= 32 / U; off >>= 1) {
         n >>= 1;
         const bool up = (lane & off) != 0;
 #pragma unroll
@@ -214,7 +262,7 @@ __device__ __forceinline__ T reduce_scatter(const T (&v)[U], int lane, Op op)
         }
     }
 #pragma unroll
-    for (int off = (U == 16 ? 1 : 2); off >= 1; off >>= 1) a[0] = op(a[0], __shfl_xor_sync(0xffffffffu, a[0], off));
+    for (int off = 16 / U; off >= 1; off >>= 1) a[0] = op(a[0], __shfl_xor_sync(0xffffffffu, a[0], off));
     return a[0];
 }
 
@@ -267,9 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     uint64_t *sfull = empty + kMaxStages;  // the helper wrote a ring entry's scale scratch
     uint64_t *pbar = sfull + kMaxStages;   // the consumer warps wrote a ring entry's partials
     uint64_t *aload = pbar + kMaxStages;   // the consumer warps' activation loads returned
-    int *s_seq = reinterpret_cast<int *>(aload + 1);  // stage a ring entry holds
+    uint64_t *peerb = aload + 1;           // the partner CTA's half of the staging landed
+    int *s_seq = reinterpret_cast<int *>(peerb + 1);  // stage a ring entry holds
     float *s_inv = reinterpret_cast<float *>(smem + p.off_misc);        // [4] inverse RMS per lane
-    float *s_sq = s_inv + 4;                                            // [8 warps][4] square sums
+    float *s_sq = s_inv + 4;                                            // [warps][4] square sums
+    float *s_sqp = s_sq + 4 * kConsumerWarps;                           // [4] the partner's half sums
     unsigned char *s_act = smem + p.off_act;
     const float4 *s_fx = reinterpret_cast<const float4 *>(smem + p.off_fx);  // [KB][4] {f1, f2, X, 0}
 
@@ -282,9 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int u1 = (int)((long long)p.n_units * (blockIdx.x + 1) / gridDim.x);
     const int col_begin = u0 * p.unit;
     const int col_end = min(u1 * p.unit, p.N);
-    if (col_begin >= col_end) return;  // uniform for the CTA, before any barrier
-    const int ncols = col_end - col_begin;
+    // a CTA without columns still stages its half of the activations for
+    // its partner (and then runs no stage)
+    const int ncols = col_end > col_begin ? col_end - col_begin : 0;
     const int n_stages = (ncols + TCOLS - 1) / TCOLS;
+    // CTA pairs: this CTA stages k-blocks [kb_lo, kb_hi), its partner the rest
+    const uint32_t crank = lanes_cluster_rank();
+    const uint32_t peer = crank ^ 1u;
+    const int kb_half = p.KB / 2;
+    const int kb_lo = crank ? kb_half : 0;
+    const int kb_hi = crank ? p.KB : kb_half;
+    const int kb_peer = crank ? kb_half : p.KB - kb_half;  // blocks the partner stages
 
     // =====================================================================
     // Producer warp.
@@ -299,9 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 s_seq[s] = -1;
             }
             mbar_init(aload, kConsumerWarps);
+            mbar_init(peerb, 1);  // completed by the partner's stores and one local expect
             mbar_fence_init();
         }
         __syncwarp();
+        lanes_cluster_arrive();  // after the initialisation: the partner may now use peerb
         lanes_bar_arrive(4, kBar2Threads);  // the consumers' first mbarrier use (aload)
         lanes_bar_arrive(2, kBar2Threads);  // the consumers' barrier after their prologue
         lanes_bar_arrive(3, 64);            // the helper's
@@ -377,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     (void)mbar_wait(&full[i % p.S], (i / p.S) & 1);
             }
         }
+        __syncwarp();
+        lanes_cluster_wait();
         return;
     }
 
@@ -392,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // stage i - S has read the buffer.
     // =====================================================================
     if (warp == kHelperWarp) {
+        lanes_cluster_arrive();
         lanes_bar(3, 64);  // the producer has initialised the mbarriers
         const int g = lane >> 2, t = lane & 3;
         const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
@@ -495,6 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             step(i, s0, z0, s1, z1);
             if (i + 1 < n_stages + p.S) step(i + 1, s1, z1, s0, z0);
         }
+        __syncwarp();
+        lanes_cluster_wait();
         return;
     }
 
@@ -517,13 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // sum l 2^-24, sum x}.
     // =====================================================================
     const int ctid = threadIdx.x;
+    lanes_cluster_arrive();
     lanes_dependency_wait();
     float sq[NP];
 #pragma unroll
     for (int m = 0; m < NP; ++m) sq[m] = 0.0f;
     const bool cta0 = blockIdx.x == 0;
+    const bool cl0 = blockIdx.x < 2;  // the first CTA pair writes residual_out (each its half)
     constexpr bool TWO = PRO != kProNone;  // A_b (norm) or the gate vector
-    constexpr int U = 4 * NP;
+    constexpr int U = kPrologueBlocks * NP;
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const int par = lane & 1;  // codes 0-3 (0) or 4-7 (1) of word lane >> 1
     const int wsl = lane >> 1;
@@ -532,13 +599,24 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // every consumer thread passes named barrier 4 once, before any mbarrier
     // use: the producer arrives there after initialising the mbarriers
     lanes_bar(4, kBar2Threads);
-    bool arrived = 4 * warp >= p.KB;  // a warp without k-blocks signals at once
+    // the partner's mbarriers are initialised once every thread of the pair
+    // has arrived; its staging area, block factors and peerb, seen from here
+    lanes_cluster_wait();
+    const uint32_t act_r = lanes_mapa(smem_addr(s_act), peer);
+    const uint32_t fx_r = lanes_mapa(smem_addr(smem + p.off_fx), peer);
+    const uint32_t sqp_r = lanes_mapa(smem_addr(s_sqp), peer);
+    const uint32_t peerb_r = lanes_mapa(smem_addr(peerb), peer);
+    if (ctid == 0)  // the bytes the partner stores here: pieces, block factors, norm half sums
+        mbar_arrive_expect_tx(peerb, (uint32_t)kb_peer * (uint32_t)NP * (2u * 32u * 8u + 16u) +
+                                         (NORM ? 4u * (uint32_t)NP : 0u));
+    bool pfail = false;
+    bool arrived = kb_lo + kPrologueBlocks * warp >= kb_hi;  // a warp without k-blocks signals at once
     if (arrived && lane == 0) mbar_arrive(aload);
-    for (int kb0 = 4 * warp; kb0 < p.KB; kb0 += 4 * kConsumerWarps) {
-        float4 va[U], vb[U], vg[4];
+    for (int kb0 = kb_lo + kPrologueBlocks * warp; kb0 < kb_hi; kb0 += kPrologueBlocks * kConsumerWarps) {
+        float4 va[U], vb[U], vg[kPrologueBlocks];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool okb = kb0 + i < p.KB;
+        for (int i = 0; i < kPrologueBlocks; ++i) {
+            const bool okb = kb0 + i < kb_hi;
             const size_t k0 = (size_t)(kb0 + i) * kBlock + 4 * lane;
 #pragma unroll
             for (int m = 0; m < NP; ++m) {
@@ -560,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             if constexpr (NORM) {
                 const float4 a = vb[u];
                 v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
-                if (cta0 && kb0 + i < p.KB && m < p.M && p.residual_out)
+                if (cl0 && kb0 + i < kb_hi && m < p.M && p.residual_out)
                     *reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + (size_t)(kb0 + i) * kBlock +
                                                 4 * lane) = v;
                 float s2 = v.x * v.x;
@@ -618,20 +696,25 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             // even lane: (code 0, code 4), (code 1, code 5); odd: (2, 6), (3, 7)
             const uint32_t ha = par ? hrcv : hown, hb = par ? hown : hrcv;
             const uint32_t la = par ? lrcv : lown, lb = par ? lown : lrcv;
-            if (kb0 + i < p.KB) {
-                unsigned char *d = s_act + (size_t)(kb0 + i) * 4 * (2 * NP) * 64 + (size_t)(2 * m) * 64 + act_lane;
-                *reinterpret_cast<uint2 *>(d) = make_uint2(__byte_perm(ha, hb, 0x5410), __byte_perm(ha, hb, 0x7632));
-                *reinterpret_cast<uint2 *>(d + 64) =
-                    make_uint2(__byte_perm(la, lb, 0x5410), __byte_perm(la, lb, 0x7632));
+            if (kb0 + i < kb_hi) {
+                const uint32_t o = (uint32_t)(kb0 + i) * 4u * (2 * NP) * 64u + (uint32_t)(2 * m) * 64u + act_lane;
+                const uint32_t h0 = __byte_perm(ha, hb, 0x5410), h1 = __byte_perm(ha, hb, 0x7632);
+                const uint32_t l0 = __byte_perm(la, lb, 0x5410), l1 = __byte_perm(la, lb, 0x7632);
+                *reinterpret_cast<uint2 *>(s_act + o) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(s_act + o + 64) = make_uint2(l0, l1);
+                st_async_v2(act_r + o, h0, h1, peerb_r);  // and the partner's copy
+                st_async_v2(act_r + o + 64, l0, l1, peerb_r);
             }
         }
         const int shown = reduce_scatter<U>(shv, lane, OpAdd());
         const int slown = reduce_scatter<U>(slv, lane, OpAdd());
         const int uo = rs_unit<U>(lane);
-        if (lane == rs_owner<U>(uo) && kb0 + uo / NP < p.KB) {
+        if (lane == rs_owner<U>(uo) && kb0 + uo / NP < kb_hi) {
             const float e24 = 5.9604644775390625e-8f;  // 2^-24
-            *reinterpret_cast<float4 *>(smem + p.off_fx + ((size_t)(kb0 + uo / NP) * 4 + uo % NP) * 16) =
-                make_float4(fown, (float)shown * e24, (float)slown * e24, sown);
+            const uint32_t o = ((uint32_t)(kb0 + uo / NP) * 4u + (uint32_t)(uo % NP)) * 16u;
+            const float4 v = make_float4(fown, (float)shown * e24, (float)slown * e24, sown);
+            *reinterpret_cast<float4 *>(smem + p.off_fx + o) = v;
+            st_async_v4(fx_r + o, v, peerb_r);
         }
     }
     if constexpr (NORM) {
@@ -643,11 +726,21 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             if (lane == 0) s_sq[warp * 4 + m] = sq[m];
         }
         lanes_bar(1, kCT);
-        if (ctid < NP) {
-            float sum = 0.0f;
-            for (int w = 0; w < kConsumerWarps; ++w) sum += s_sq[w * 4 + ctid];
-            s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
-        }
+    }
+    float own = 0.0f;  // this CTA's half of a lane's square sum (threads ctid < NP)
+    if (NORM && ctid < NP) {
+        for (int w = 0; w < kConsumerWarps; ++w) own += s_sq[w * 4 + ctid];
+        st_async_f32(sqp_r + 4u * (uint32_t)ctid, own, peerb_r);
+    }
+    // the partner's half of the staging (and of the square sums) has landed
+    if (!mbar_wait(peerb, 0)) {
+        lanes_error();
+        pfail = true;
+    }
+    if (NORM && ctid < NP) {
+        // both CTAs add the halves in the same order (rank 0's first)
+        const float sum = crank ? s_sqp[ctid] + own : own + s_sqp[ctid];
+        s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
     }
     lanes_bar(2, kBar2Threads);  // activations staged; the producer has initialised the mbarriers
 
@@ -655,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // Consumer warps: stages.
     // =====================================================================
     // `failed` stays uniform across each warp: the MMAs need every lane
-    bool failed = false;
+    bool failed = __any_sync(0xffffffffu, pfail);
     const int g = lane >> 2, t = lane & 3;
     // this warp's K slice: blocks [bw0, bw1)
     const int bw0 = (int)((long long)p.KB * warp / kConsumerWarps);
@@ -805,18 +898,30 @@ cudaError_t launch_lanes_variant(const LanesParams &prm, size_t smem, cudaStream
         if (dev >= 0 && dev < kMaxDevices) smem_ready[dev].store(1, std::memory_order_release);
     }
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    int grid = sms;
-    if (grid > prm.n_units) grid = prm.n_units;
+    // CTA pairs (clusters of 2) share the activation staging: as many pairs
+    // as are resident, no more than the columns need (a CTA may get none)
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3((unsigned)grid);
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
+    int pairs = sms / 2;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) == cudaSuccess && resident > 0 && resident < pairs)
+        pairs = resident;
+    const int need = (prm.n_units + 1) / 2;
+    if (pairs > need) pairs = need;
+    if (pairs < 1) pairs = 1;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
@@ -864,7 +969,7 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     const uint32_t act_bytes = (uint32_t)prm.KB * 4u * (uint32_t)(2 * NP) * 64u;
     const uint32_t fx_bytes = (uint32_t)prm.KB * 4u * 16u;
     const uint32_t misc_bytes = 256u;
-    const uint32_t bar_bytes = (4 * kMaxStages + 1) * 8u + kMaxStages * 4u;
+    const uint32_t bar_bytes = (4 * kMaxStages + 2) * 8u + kMaxStages * 4u;
     // per ring entry: the codes, the scale scratch [G][16 rows] {s, z}
     // and the consumer warps' partial sums
     const uint32_t scr_per_stage = (uint32_t)prm.G * 16u * 8u;
