@@ -332,7 +332,7 @@ def lane_path(M):
         return "one-lane streaming kernel, CUDA cores", "M1"
     if M <= 4:
         return ("2-4-lane kernel: exact fp16 products on the warp-level MMA (the 11008-long down "
-                "projection on the multi-lane fp32 kernel)"), f"M{M}"
+                "projection with K split over a 4-CTA cluster)"), f"M{M}"
     if M < 16:
         return "multi-lane fp32 kernel, CUDA cores", f"M{M}"
     return "tensor-core kernel (tcgen05, bf16 operands, f32 accumulate)", f"M{M}"

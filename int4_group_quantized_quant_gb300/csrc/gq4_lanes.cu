@@ -61,6 +61,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 
 #include "gq4_device.cuh"
 #include "gq4_host.h"
@@ -86,6 +87,9 @@ constexpr int kBlock = 128;  // codes per activation block (one scale exponent, 
 constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
 constexpr int kMaxWarpBlocks = 3;   // 128-code blocks per consumer warp (K <= 4608)
 constexpr int kPrologueBlocks = 2;  // k-blocks per warp per prologue pass
+constexpr int kMaxSplit = 4;        // K chunks per cluster when K is split
+constexpr int kCombine = 4;         // stages of partial sums in flight to a cluster's rank 0
+constexpr int kSplitWarpBlocks = 2; // preferred blocks per consumer warp when K is split
 constexpr uint32_t kSmemLimit = 226u * 1024u;  // of the 227 KB a block may opt in to
 
 struct LanesParams {
@@ -96,12 +100,12 @@ struct LanesParams {
     int bpg;         // blocks per scale group (gs / 128, a power of two)
     int bpg_shift;   // log2(bpg)
     int S;           // ring depth
+    int ks;          // K chunks per cluster (1: CTA pairs share the staging of all of K)
+    int Gs;          // scale groups per ring entry's scratch (G, or the largest chunk's)
     int unit;        // column granularity of the balanced split
     int n_units;
-    uint32_t col_bytes;    // bytes of one column's codes (K / 2)
     uint32_t stage_bytes;
-    uint32_t off_reg1;     // second region of a stage (64 mod 128)
-    uint32_t off_act, off_fx, off_part, off_scr, off_misc, off_bar;
+    uint32_t off_act, off_fx, off_part, off_scr, off_misc, off_cmb, off_bar;
     const float *A;
     const float *A_b;
     const float *W_norm;
@@ -181,6 +185,12 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t r
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
                  ::"r"(raddr), "f"(v), "r"(rbar) : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster (address from lanes_mapa).
+__device__ __forceinline__ void lanes_remote_arrive(uint32_t rbar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
 __device__ __forceinline__ void lanes_error()
@@ -305,8 +315,12 @@ __device__ __forceinline__ uint32_t piece_pair(int a, int b)
     return h2_bits(__floats2half2_rn((float)a, (float)b * 0.0625f));
 }
 
+template <int V>
+using IntC = std::integral_constant<int, V>;
+
 // NP: lanes per MMA (2 or 4; the N columns are {hi, lo} of each lane).
-template <int NMAT, int PRO, int EPI, int NP>
+// SPLIT: K split over the cluster (p.ks > 1), else CTA pairs.
+template <int NMAT, int PRO, int EPI, int NP, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_constant__ LanesParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -316,10 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     uint64_t *pbar = sfull + kMaxStages;   // the consumer warps wrote a ring entry's partials
     uint64_t *aload = pbar + kMaxStages;   // the consumer warps' activation loads returned
     uint64_t *peerb = aload + 1;           // the partner CTA's half of the staging landed
-    int *s_seq = reinterpret_cast<int *>(peerb + 1);  // stage a ring entry holds
+    uint64_t *cfull = peerb + 1;           // [kCombine] split K: the other ranks' partials landed
+    uint64_t *cfree = cfull + kCombine;    // [kCombine] split K: rank 0 has read a combine entry
+    int *s_seq = reinterpret_cast<int *>(cfree + kCombine);  // stage a ring entry holds
     float *s_inv = reinterpret_cast<float *>(smem + p.off_misc);        // [4] inverse RMS per lane
     float *s_sq = s_inv + 4;                                            // [warps][4] square sums
-    float *s_sqp = s_sq + 4 * kConsumerWarps;                           // [4] the partner's half sums
+    // [kMaxSplit - 1][4] the other CTAs' square sums (pairs: the partner's half in [0])
+    float *s_sqp = s_sq + 4 * kConsumerWarps;
     unsigned char *s_act = smem + p.off_act;
     const float4 *s_fx = reinterpret_cast<const float4 *>(smem + p.off_fx);  // [KB][4] {f1, f2, X, 0}
 
@@ -328,21 +345,36 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int u0 = (int)((long long)p.n_units * blockIdx.x / gridDim.x);
-    const int u1 = (int)((long long)p.n_units * (blockIdx.x + 1) / gridDim.x);
+    // Two cluster forms.  CTA pairs (ks = 1): each CTA owns its columns and
+    // stages half of K's activations for both.  Split K (ks > 1): the ks CTAs
+    // of a cluster own the same columns, each a chunk of whole scale groups
+    // of K, and rank 0 adds the others' partial sums in rank order.
+    constexpr bool split = SPLIT;
+    const uint32_t crank = lanes_cluster_rank();
+    const int owner = split ? (int)blockIdx.x / p.ks : (int)blockIdx.x;
+    const int n_owners = split ? (int)gridDim.x / p.ks : (int)gridDim.x;
+    const int u0 = (int)((long long)p.n_units * owner / n_owners);
+    const int u1 = (int)((long long)p.n_units * (owner + 1) / n_owners);
     const int col_begin = u0 * p.unit;
     const int col_end = min(u1 * p.unit, p.N);
     // a CTA without columns still stages its half of the activations for
     // its partner (and then runs no stage)
     const int ncols = col_end > col_begin ? col_end - col_begin : 0;
     const int n_stages = (ncols + TCOLS - 1) / TCOLS;
-    // CTA pairs: this CTA stages k-blocks [kb_lo, kb_hi), its partner the rest
-    const uint32_t crank = lanes_cluster_rank();
+    // this CTA's groups [g_lo, g_lo + GL) and blocks [kbc0, kbc0 + KBL) of K
+    const int g_lo = split ? (int)((long long)p.G * crank / p.ks) : 0;
+    const int GL = split ? (int)((long long)p.G * (crank + 1) / p.ks) - g_lo : p.G;
+    const int kbc0 = g_lo * p.bpg;
+    const int KBL = GL * p.bpg;
+    const uint32_t cb = (uint32_t)KBL * 64u;  // a column's codes in a stage (bytes)
+    const uint32_t off_reg1 = 8u * cb + 64u;  // second region of a stage (64 mod 128)
+    // the blocks [kb_lo, kb_hi) of the chunk this CTA stages (pairs: its half,
+    // the partner the rest)
     const uint32_t peer = crank ^ 1u;
-    const int kb_half = p.KB / 2;
-    const int kb_lo = crank ? kb_half : 0;
-    const int kb_hi = crank ? p.KB : kb_half;
-    const int kb_peer = crank ? kb_half : p.KB - kb_half;  // blocks the partner stages
+    const int kb_half = KBL / 2;
+    const int kb_lo = split ? 0 : (crank ? kb_half : 0);
+    const int kb_hi = split ? KBL : (crank ? KBL : kb_half);
+    const int kb_peer = split ? 0 : (crank ? kb_half : KBL - kb_half);  // blocks the partner stages
 
     // =====================================================================
     // Producer warp.
@@ -358,10 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             }
             mbar_init(aload, kConsumerWarps);
             mbar_init(peerb, 1);  // completed by the partner's stores and one local expect
+            for (int s = 0; s < kCombine; ++s) {
+                mbar_init(&cfull[s], 1);  // rank 0's expect plus the other ranks' stores
+                mbar_init(&cfree[s], 1);  // rank 0's remote arrive
+            }
             mbar_fence_init();
         }
         __syncwarp();
-        lanes_cluster_arrive();  // after the initialisation: the partner may now use peerb
+        lanes_cluster_arrive();  // after the initialisation: the cluster may now use peerb, cfull, cfree
         lanes_bar_arrive(4, kBar2Threads);  // the consumers' first mbarrier use (aload)
         lanes_bar_arrive(2, kBar2Threads);  // the consumers' barrier after their prologue
         lanes_bar_arrive(3, 64);            // the helper's
@@ -406,27 +442,41 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 stage_regions(i, rc, rn);
                 unsigned char *dst = smem + (size_t)slot * p.stage_bytes;
                 s_seq[slot] = i;  // published by the release of the arrive below
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)(rn[0] + rn[1]) * p.col_bytes);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)(rn[0] + rn[1]) * cb);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (rn[r] == 0) continue;
                     const int m = NMAT == 2 ? r : 0;
-                    bulk_g2s(dst + (r ? p.off_reg1 : 0u), p.Bq[m] + (size_t)rc[r] * (p.KW / 4),
-                             (uint32_t)rn[r] * p.col_bytes, &full[slot]);
+                    const uint4 *src = p.Bq[m] + (size_t)rc[r] * (p.KW / 4);
+                    if (!split) {
+                        // whole columns: one run
+                        bulk_g2s(dst + (r ? off_reg1 : 0u), src, (uint32_t)rn[r] * cb, &full[slot]);
+                    } else {
+                        // the chunk of each column (16-byte aligned: 64 bytes a block)
+                        for (int q = 0; q < rn[r]; ++q)
+                            bulk_g2s(dst + (r ? off_reg1 : 0u) + (uint32_t)q * cb,
+                                     src + (size_t)q * (p.KW / 4) + (size_t)kbc0 * 4, cb, &full[slot]);
+                    }
                 }
                 issued = i + 1;
                 if (i >= 2) {
                     for (; pf < n_stages && pf <= i + kPrefetchAhead; ++pf) {
                         int pc[2], pn[2];
                         stage_regions(pf, pc, pn);
-                        if constexpr (NMAT == 2) {
+                        if (split) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const int m = NMAT == 2 ? r : 0;
+                                for (int q = 0; q < pn[r]; ++q)
+                                    prefetch_l2(p.Bq[m] + (size_t)(pc[r] + q) * (p.KW / 4) + (size_t)kbc0 * 4, cb);
+                            }
+                        } else if constexpr (NMAT == 2) {
 #pragma unroll
                             for (int r = 0; r < 2; ++r)
-                                prefetch_l2(p.Bq[r] + (size_t)pc[r] * (p.KW / 4), (uint32_t)pn[r] * p.col_bytes);
+                                prefetch_l2(p.Bq[r] + (size_t)pc[r] * (p.KW / 4), (uint32_t)pn[r] * cb);
                         } else {
                             // the two regions are one contiguous run of columns
-                            prefetch_l2(p.Bq[0] + (size_t)pc[0] * (p.KW / 4),
-                                        (uint32_t)(pn[0] + pn[1]) * p.col_bytes);
+                            prefetch_l2(p.Bq[0] + (size_t)pc[0] * (p.KW / 4), (uint32_t)(pn[0] + pn[1]) * cb);
                         }
                     }
                 }
@@ -460,11 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
         const bool lane_ok = t < p.M;
         const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [S][warps][32]
+        // split K: rank 0's [kCombine][kMaxSplit - 1][32] partial sums of the other ranks
+        const float2 *cmb = reinterpret_cast<const float2 *>(smem + p.off_cmb);
+        const uint32_t cmb_r0 = split ? lanes_mapa(smem_addr(smem + p.off_cmb), 0u) : 0u;
+        const uint32_t cfull_r0 = split ? lanes_mapa(smem_addr(cfull), 0u) : 0u;
         bool hfail = false;
-        // the scale and zero of stage i's 16 MMA rows, lane = group (G <= 32)
+        // the scale and zero of stage i's 16 MMA rows, lane = group of this
+        // CTA's chunk (at most 32 groups)
         auto load_scales = [&](int i, float (&sv)[16], float (&zv)[16]) {
             const int lc0 = i * TCOLS;
-            const bool ok = lane < p.G;
+            const bool ok = lane < GL;
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 int m, lc;
@@ -476,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     lc = lc0 + 8 * (r & 1) + (r >> 1);
                 }
                 lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
-                const size_t si = (size_t)(col_begin + lc) * p.G + lane;
+                const size_t si = (size_t)(col_begin + lc) * p.G + g_lo + lane;
                 sv[r] = ok ? __ldg(p.scales[m] + si) : 0.0f;
                 zv[r] = ok ? __ldg(p.zeros[m] + si) : 0.0f;
             }
@@ -494,6 +549,36 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 const float2 v = part[((size_t)slot * kConsumerWarps + w) * 32 + lane];
                 a0 += v.x;
                 a8 += v.y;
+            }
+            if (split) {
+                // the chunks' sums meet in rank 0, added in rank order
+                const int cs = j % kCombine;
+                const uint32_t cpar = (uint32_t)(j / kCombine) & 1u;
+                if (crank != 0) {
+                    // rank 0 has read entry cs's stage j - kCombine
+                    if (j >= kCombine && !hfail &&
+                        !__all_sync(0xffffffffu, mbar_wait(&cfree[cs], cpar ^ 1u))) {
+                        lanes_error();
+                        hfail = true;
+                    }
+                    if (hfail) a0 = a8 = __int_as_float(0x7fffffff);
+                    const uint32_t o = (uint32_t)((cs * (kMaxSplit - 1) + (int)crank - 1) * 32 + lane) * 8u;
+                    st_async_v2(cmb_r0 + o, __float_as_uint(a0), __float_as_uint(a8), cfull_r0 + 8u * (uint32_t)cs);
+                    return;  // the outputs are rank 0's
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&cfull[cs], (uint32_t)(p.ks - 1) * 32u * 8u);
+                if (!hfail && !__all_sync(0xffffffffu, mbar_wait(&cfull[cs], cpar))) {
+                    lanes_error();
+                    hfail = true;
+                }
+                for (int r = 1; r < p.ks; ++r) {
+                    const float2 v = cmb[(cs * (kMaxSplit - 1) + r - 1) * 32 + lane];
+                    a0 += v.x;
+                    a8 += v.y;
+                }
+                __syncwarp();
+                // entry cs is free again on every rank
+                if (lane > 0 && lane < p.ks) lanes_remote_arrive(lanes_mapa(smem_addr(&cfree[cs]), (uint32_t)lane));
             }
             if constexpr (NORM) {
                 const float inv = s_inv[t];
@@ -543,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             if (i >= p.S) reduce_stage(i - p.S);
             if (i < n_stages) {
                 const int slot = i % p.S;
-                float2 *scr = reinterpret_cast<float2 *>(smem + p.off_scr) + (size_t)slot * p.G * 16;
-                if (lane < p.G) {
+                float2 *scr = reinterpret_cast<float2 *>(smem + p.off_scr) + (size_t)slot * p.Gs * 16;
+                if (lane < GL) {
 #pragma unroll
                     for (int r = 0; r < 16; ++r) scr[lane * 16 + r] = make_float2(sv[r], zv[r]);
                 }
@@ -557,6 +642,15 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         for (int i = 0; i < n_stages + p.S; i += 2) {
             step(i, s0, z0, s1, z1);
             if (i + 1 < n_stages + p.S) step(i + 1, s1, z1, s0, z0);
+        }
+        if (split && crank != 0 && !hfail) {
+            // rank 0's last remote arrives have landed here before this CTA exits
+            for (int j = max(0, n_stages - kCombine); j < n_stages; ++j) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&cfree[j % kCombine], (uint32_t)(j / kCombine) & 1u))) {
+                    lanes_error();
+                    break;
+                }
+            }
         }
         __syncwarp();
         lanes_cluster_wait();
@@ -588,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
 #pragma unroll
     for (int m = 0; m < NP; ++m) sq[m] = 0.0f;
     const bool cta0 = blockIdx.x == 0;
-    const bool cl0 = blockIdx.x < 2;  // the first CTA pair writes residual_out (each its half)
+    // the first cluster writes residual_out (each CTA the blocks it stages)
+    const bool cl0 = (int)blockIdx.x < (split ? p.ks : 2);
     constexpr bool TWO = PRO != kProNone;  // A_b (norm) or the gate vector
     constexpr int U = kPrologueBlocks * NP;
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -599,16 +694,23 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // every consumer thread passes named barrier 4 once, before any mbarrier
     // use: the producer arrives there after initialising the mbarriers
     lanes_bar(4, kBar2Threads);
-    // the partner's mbarriers are initialised once every thread of the pair
-    // has arrived; its staging area, block factors and peerb, seen from here
+    // the cluster's mbarriers are initialised once every thread of it has
+    // arrived; the partner's staging area, block factors and peerb (split K:
+    // rank 0's square sums and peerb), seen from here
     lanes_cluster_wait();
-    const uint32_t act_r = lanes_mapa(smem_addr(s_act), peer);
-    const uint32_t fx_r = lanes_mapa(smem_addr(smem + p.off_fx), peer);
-    const uint32_t sqp_r = lanes_mapa(smem_addr(s_sqp), peer);
-    const uint32_t peerb_r = lanes_mapa(smem_addr(peerb), peer);
-    if (ctid == 0)  // the bytes the partner stores here: pieces, block factors, norm half sums
-        mbar_arrive_expect_tx(peerb, (uint32_t)kb_peer * (uint32_t)NP * (2u * 32u * 8u + 16u) +
-                                         (NORM ? 4u * (uint32_t)NP : 0u));
+    const uint32_t target = split ? 0u : peer;  // a rank of this cluster
+    const uint32_t act_r = lanes_mapa(smem_addr(s_act), target);  // (pairs only)
+    const uint32_t fx_r = lanes_mapa(smem_addr(smem + p.off_fx), target);
+    const uint32_t sqp_r = lanes_mapa(smem_addr(s_sqp), target);
+    const uint32_t peerb_r = lanes_mapa(smem_addr(peerb), target);
+    if (ctid == 0) {
+        // the bytes stored here by the cluster: pairs, the partner's pieces,
+        // block factors and norm half sums; split K, the other ranks' square
+        // sums in rank 0
+        const uint32_t norm_bytes = NORM ? 4u * (uint32_t)NP : 0u;
+        mbar_arrive_expect_tx(peerb, split ? (crank == 0 ? (uint32_t)(p.ks - 1) * norm_bytes : 0u)
+                                           : (uint32_t)kb_peer * (uint32_t)NP * (2u * 32u * 8u + 16u) + norm_bytes);
+    }
     bool pfail = false;
     bool arrived = kb_lo + kPrologueBlocks * warp >= kb_hi;  // a warp without k-blocks signals at once
     if (arrived && lane == 0) mbar_arrive(aload);
@@ -617,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < kPrologueBlocks; ++i) {
             const bool okb = kb0 + i < kb_hi;
-            const size_t k0 = (size_t)(kb0 + i) * kBlock + 4 * lane;
+            const size_t k0 = (size_t)(kbc0 + kb0 + i) * kBlock + 4 * lane;
 #pragma unroll
             for (int m = 0; m < NP; ++m) {
                 const bool on = okb && m < p.M;
@@ -639,8 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 const float4 a = vb[u];
                 v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
                 if (cl0 && kb0 + i < kb_hi && m < p.M && p.residual_out)
-                    *reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K + (size_t)(kb0 + i) * kBlock +
-                                                4 * lane) = v;
+                    *reinterpret_cast<float4 *>(p.residual_out + (size_t)m * p.K +
+                                                (size_t)(kbc0 + kb0 + i) * kBlock + 4 * lane) = v;
                 float s2 = v.x * v.x;
                 s2 = fmaf(v.y, v.y, s2); s2 = fmaf(v.z, v.z, s2); s2 = fmaf(v.w, v.w, s2);
                 sq[m] += s2;
@@ -702,8 +804,10 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 const uint32_t l0 = __byte_perm(la, lb, 0x5410), l1 = __byte_perm(la, lb, 0x7632);
                 *reinterpret_cast<uint2 *>(s_act + o) = make_uint2(h0, h1);
                 *reinterpret_cast<uint2 *>(s_act + o + 64) = make_uint2(l0, l1);
-                st_async_v2(act_r + o, h0, h1, peerb_r);  // and the partner's copy
-                st_async_v2(act_r + o + 64, l0, l1, peerb_r);
+                if (!split) {  // and the partner's copy
+                    st_async_v2(act_r + o, h0, h1, peerb_r);
+                    st_async_v2(act_r + o + 64, l0, l1, peerb_r);
+                }
             }
         }
         const int shown = reduce_scatter<U>(shv, lane, OpAdd());
@@ -714,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             const uint32_t o = ((uint32_t)(kb0 + uo / NP) * 4u + (uint32_t)(uo % NP)) * 16u;
             const float4 v = make_float4(fown, (float)shown * e24, (float)slown * e24, sown);
             *reinterpret_cast<float4 *>(smem + p.off_fx + o) = v;
-            st_async_v4(fx_r + o, v, peerb_r);
+            if (!split) st_async_v4(fx_r + o, v, peerb_r);
         }
     }
     if constexpr (NORM) {
@@ -727,10 +831,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         }
         lanes_bar(1, kCT);
     }
-    float own = 0.0f;  // this CTA's half of a lane's square sum (threads ctid < NP)
+    float own = 0.0f;  // this CTA's part of a lane's square sum (threads ctid < NP)
     if (NORM && ctid < NP) {
         for (int w = 0; w < kConsumerWarps; ++w) own += s_sq[w * 4 + ctid];
-        st_async_f32(sqp_r + 4u * (uint32_t)ctid, own, peerb_r);
+        // pairs: to the partner; split K: ranks 1.. to rank 0
+        if (!split || crank != 0)
+            st_async_f32(sqp_r + 4u * (uint32_t)((split ? (int)crank - 1 : 0) * 4 + ctid), own, peerb_r);
     }
     // the partner's half of the staging (and of the square sums) has landed
     if (!mbar_wait(peerb, 0)) {
@@ -738,9 +844,16 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         pfail = true;
     }
     if (NORM && ctid < NP) {
-        // both CTAs add the halves in the same order (rank 0's first)
-        const float sum = crank ? s_sqp[ctid] + own : own + s_sqp[ctid];
-        s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
+        if (!split) {
+            // both CTAs add the halves in the same order (rank 0's first)
+            const float sum = crank ? s_sqp[ctid] + own : own + s_sqp[ctid];
+            s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
+        } else if (crank == 0) {
+            // the chunks in rank order (only rank 0 applies the norm)
+            float sum = own;
+            for (int r = 1; r < p.ks; ++r) sum += s_sqp[(r - 1) * 4 + ctid];
+            s_inv[ctid] = 1.0f / sqrtf(sum / (float)p.K + p.eps);
+        }
     }
     lanes_bar(2, kBar2Threads);  // activations staged; the producer has initialised the mbarriers
 
@@ -751,12 +864,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     bool failed = __any_sync(0xffffffffu, pfail);
     const int g = lane >> 2, t = lane & 3;
     // this warp's K slice: blocks [bw0, bw1)
-    const int bw0 = (int)((long long)p.KB * warp / kConsumerWarps);
-    const int bw1 = (int)((long long)p.KB * (warp + 1) / kConsumerWarps);
+    const int bw0 = (int)((long long)KBL * warp / kConsumerWarps);
+    const int bw1 = (int)((long long)KBL * (warp + 1) / kConsumerWarps);
     float2 *part = reinterpret_cast<float2 *>(smem + p.off_part);  // [S][warps][32]
     // MMA rows g and g + 8: region g & 1, columns (g >> 1) and (g >> 1) + 4 of it
-    const uint32_t row_off = ((g & 1) ? p.off_reg1 : 0u) + (uint32_t)(g >> 1) * p.col_bytes;
-    const uint32_t row8_delta = 4u * p.col_bytes;
+    const uint32_t row_off = ((g & 1) ? off_reg1 : 0u) + (uint32_t)(g >> 1) * cb;
+    const uint32_t row8_delta = 4u * cb;
     const uint32_t b_lane_off = (uint32_t)(g * 4 + t) * 16u;
     const bool b_active = g < 2 * NP;
     // The warp's K slice is the same in every stage: its B fragments and
@@ -787,38 +900,36 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         }
         const unsigned char *st = smem + (size_t)ring * p.stage_bytes;
         // {s, z} per [group][MMA row] of this stage
-        const float2 *scr = reinterpret_cast<const float2 *>(smem + p.off_scr) + (size_t)ring * p.G * 16;
+        const float2 *scr = reinterpret_cast<const float2 *>(smem + p.off_scr) + (size_t)ring * p.Gs * 16;
 
         float y0 = 0.0f, y8 = 0.0f;
         if (!failed) {
             const unsigned char *ra = st + row_off;
-            // two blocks at a time: their codes and scales first, then four
-            // independent MMA chains (a repeated last block is discarded)
+            // NBL (1 or 2) blocks from the warp's block U0 on: their codes
+            // and scales first, then 2 NBL independent MMA chains
+            auto run_blocks = [&](auto u0c, auto nbc) {
+                constexpr int U0 = decltype(u0c)::value, NBL = decltype(nbc)::value;
+                uint4 wa[NBL], wb[NBL];
+                float2 sz0[NBL], sz8[NBL];
 #pragma unroll
-            for (int u0 = 0; u0 < kMaxWarpBlocks; u0 += 2) {
-                if (u0 >= nb) break;
-                const bool two = u0 + 1 < nb;
-                const int bb[2] = {bw0 + u0, bw0 + (two ? u0 + 1 : u0)};
-                uint4 wa[2], wb[2];
-                float2 sz0[2], sz8[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    wa[u] = *reinterpret_cast<const uint4 *>(ra + bb[u] * 64 + t * 16);
-                    wb[u] = *reinterpret_cast<const uint4 *>(ra + row8_delta + bb[u] * 64 + t * 16);
-                    const int j = bb[u] >> p.bpg_shift;
+                for (int u = 0; u < NBL; ++u) {
+                    const int b = bw0 + U0 + u;
+                    wa[u] = *reinterpret_cast<const uint4 *>(ra + b * 64 + t * 16);
+                    wb[u] = *reinterpret_cast<const uint4 *>(ra + row8_delta + b * 64 + t * 16);
+                    const int j = b >> p.bpg_shift;
                     sz0[u] = scr[j * 16 + g];  // {s, z} of row g
                     sz8[u] = scr[j * 16 + g + 8];
                 }
-                float d1[2][4], d2[2][4];
+                float d1[NBL][4], d2[NBL][4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
+                for (int u = 0; u < NBL; ++u)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) d1[u][k] = d2[u][k] = 0.0f;
 #pragma unroll
                 for (int pr = 0; pr < 4; ++pr) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint4 bq = bqc[u0 + u][pr];
+                    for (int u = 0; u < NBL; ++u) {
+                        const uint4 bq = bqc[U0 + u][pr];
                         const uint32_t w0 = pr == 0 ? wa[u].x : pr == 1 ? wa[u].y : pr == 2 ? wa[u].z : wa[u].w;
                         const uint32_t w8 = pr == 0 ? wb[u].x : pr == 1 ? wb[u].y : pr == 2 ? wb[u].z : wb[u].w;
                         mma_f16(d1[u], w0 & 0x000F000Fu, w8 & 0x000F000Fu, w0 & 0x00F000F0u, w8 & 0x00F000F0u,
@@ -829,9 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (u == 1 && !two) break;
-                    const float4 fx = fxc[u0 + u];
+                for (int u = 0; u < NBL; ++u) {
+                    const float4 fx = fxc[U0 + u];
                     // zi: the zero's integer part (clamped to the code range)
                     const float zi0 = rintf(fminf(fmaxf(sz0[u].y, 0.0f), 15.0f));
                     const float zi8 = rintf(fminf(fmaxf(sz8[u].y, 0.0f), 15.0f));
@@ -844,7 +954,13 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     y0 = fmaf(sz0[u].x, fmaf(zi0 - sz0[u].y, fx.w, fmaf(h0, 2048.0f, l0) * fx.x), y0);
                     y8 = fmaf(sz8[u].x, fmaf(zi8 - sz8[u].y, fx.w, fmaf(h8, 2048.0f, l8) * fx.x), y8);
                 }
-            }
+            };
+            // the warp's blocks two at a time, an odd last one alone (nb is
+            // uniform across the warp)
+            static_assert(kMaxWarpBlocks <= 3, "blocks per warp");
+            if (nb >= 2) run_blocks(IntC<0>{}, IntC<2>{});
+            else if (nb == 1) run_blocks(IntC<0>{}, IntC<1>{});
+            if (nb == 3) run_blocks(IntC<2>{}, IntC<1>{});
         }
 
         // this warp is done with the stage's codes and scratch
@@ -880,10 +996,10 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     }
 }
 
-template <int NMAT, int PRO, int EPI, int NP>
+template <int NMAT, int PRO, int EPI, int NP, bool SPLIT>
 cudaError_t launch_lanes_variant(const LanesParams &prm, size_t smem, cudaStream_t stream)
 {
-    auto kern = lanes_matvec_kernel<NMAT, PRO, EPI, NP>;
+    auto kern = lanes_matvec_kernel<NMAT, PRO, EPI, NP, SPLIT>;
     int dev = 0, sms = 0;
     cudaError_t err;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -898,38 +1014,44 @@ cudaError_t launch_lanes_variant(const LanesParams &prm, size_t smem, cudaStream
         if (dev >= 0 && dev < kMaxDevices) smem_ready[dev].store(1, std::memory_order_release);
     }
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    // CTA pairs (clusters of 2) share the activation staging: as many pairs
-    // as are resident, no more than the columns need (a CTA may get none)
+    // Clusters of 2 (pairs sharing the activation staging) or of ks (split
+    // K): as many as are resident, no more than the columns need (a CTA may
+    // get none)
+    const int cd = prm.ks > 1 ? prm.ks : 2;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)cd;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    int pairs = sms / 2;
-    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    int clusters = sms / cd;
+    cfg.gridDim = dim3((unsigned)(cd * clusters));
     int resident = 0;
-    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) == cudaSuccess && resident > 0 && resident < pairs)
-        pairs = resident;
-    const int need = (prm.n_units + 1) / 2;
-    if (pairs > need) pairs = need;
-    if (pairs < 1) pairs = 1;
-    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) == cudaSuccess && resident > 0 &&
+        resident < clusters)
+        clusters = resident;
+    const int need = prm.ks > 1 ? prm.n_units : (prm.n_units + 1) / 2;
+    if (clusters > need) clusters = need;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3((unsigned)(cd * clusters));
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 template <int NMAT, int PRO, int EPI>
 cudaError_t launch_lanes_np(const LanesParams &prm, size_t smem, cudaStream_t stream)
 {
-    return prm.M <= 2 ? launch_lanes_variant<NMAT, PRO, EPI, 2>(prm, smem, stream)
-                      : launch_lanes_variant<NMAT, PRO, EPI, 4>(prm, smem, stream);
+    if (prm.ks > 1)
+        return prm.M <= 2 ? launch_lanes_variant<NMAT, PRO, EPI, 2, true>(prm, smem, stream)
+                          : launch_lanes_variant<NMAT, PRO, EPI, 4, true>(prm, smem, stream);
+    return prm.M <= 2 ? launch_lanes_variant<NMAT, PRO, EPI, 2, false>(prm, smem, stream)
+                      : launch_lanes_variant<NMAT, PRO, EPI, 4, false>(prm, smem, stream);
 }
 
 int lanes_sm_count()
@@ -956,26 +1078,44 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     if ((prm.bpg & (prm.bpg - 1)) != 0) return false;  // group of a block by a shift
     prm.bpg_shift = 0;
     while ((1 << prm.bpg_shift) < prm.bpg) ++prm.bpg_shift;
-    if (prm.G > 32) return false;  // the helper holds a stage's scales as one group per lane
-    // each consumer warp keeps its slice's activations in registers
-    if ((prm.KB + kConsumerWarps - 1) / kConsumerWarps > kMaxWarpBlocks) return false;
+    // A CTA's chunk of K: at most 32 scale groups (the helper holds a
+    // stage's scales as one group per lane) and at most kMaxWarpBlocks blocks
+    // per consumer warp (its activations stay in registers).  All of K in
+    // one CTA (pairs) where it fits; else the fewest chunks per cluster that
+    // give each warp at most kSplitWarpBlocks blocks (at most kMaxWarpBlocks).
+    auto chunk_fits = [&](int ks, int warp_blocks) {
+        const int gmax = (prm.G + ks - 1) / ks;  // the largest chunk's groups
+        return gmax <= 32 && (gmax * prm.bpg + kConsumerWarps - 1) / kConsumerWarps <= warp_blocks;
+    };
+    int ks = 0;
+    if (chunk_fits(1, kMaxWarpBlocks)) {
+        ks = 1;
+    } else {
+        for (int k = 2; k <= kMaxSplit && ks == 0; ++k)
+            if (chunk_fits(k, kSplitWarpBlocks)) ks = k;
+        for (int k = 2; k <= kMaxSplit && ks == 0; ++k)
+            if (chunk_fits(k, kMaxWarpBlocks)) ks = k;
+        if (ks == 0) return false;
+    }
+    prm.ks = ks;
+    prm.Gs = (prm.G + ks - 1) / ks;
+    const int KBC = prm.Gs * prm.bpg;  // the largest chunk's blocks
     prm.unit = 1;
     prm.n_units = call.N;
     const int NP = call.M <= 2 ? 2 : 4;
-    prm.col_bytes = (uint32_t)call.K / 2u;
-    const uint32_t reg_bytes = 8u * prm.col_bytes;  // a multiple of 512
-    prm.off_reg1 = reg_bytes + 64u;
-    const uint32_t stage = round_up(prm.off_reg1 + reg_bytes, 128u);
-    const uint32_t act_bytes = (uint32_t)prm.KB * 4u * (uint32_t)(2 * NP) * 64u;
-    const uint32_t fx_bytes = (uint32_t)prm.KB * 4u * 16u;
+    const uint32_t reg_bytes = 8u * (uint32_t)KBC * 64u;  // a multiple of 512
+    const uint32_t stage = round_up(reg_bytes + 64u + reg_bytes, 128u);
+    const uint32_t act_bytes = (uint32_t)KBC * 4u * (uint32_t)(2 * NP) * 64u;
+    const uint32_t fx_bytes = (uint32_t)KBC * 4u * 16u;
     const uint32_t misc_bytes = 256u;
-    const uint32_t bar_bytes = (4 * kMaxStages + 2) * 8u + kMaxStages * 4u;
-    // per ring entry: the codes, the scale scratch [G][16 rows] {s, z}
+    const uint32_t cmb_bytes = ks > 1 ? (uint32_t)kCombine * (kMaxSplit - 1) * 32u * 8u : 0u;
+    const uint32_t bar_bytes = (4 * kMaxStages + 2 + 2 * kCombine) * 8u + kMaxStages * 4u;
+    // per ring entry: the codes, the scale scratch [Gs][16 rows] {s, z}
     // and the consumer warps' partial sums
-    const uint32_t scr_per_stage = (uint32_t)prm.G * 16u * 8u;
+    const uint32_t scr_per_stage = (uint32_t)prm.Gs * 16u * 8u;
     const uint32_t part_per_stage = (uint32_t)kConsumerWarps * 32u * 8u;
     const uint32_t per_stage = stage + scr_per_stage + part_per_stage;
-    const uint32_t fixed = act_bytes + fx_bytes + misc_bytes + bar_bytes + 3u * 128u;
+    const uint32_t fixed = act_bytes + fx_bytes + misc_bytes + cmb_bytes + bar_bytes + 4u * 128u;
     if (fixed + 2u * per_stage > kSmemLimit) return false;
     int S = (int)((kSmemLimit - fixed) / per_stage);
     if (S > kMaxStages) S = kMaxStages;
@@ -992,6 +1132,8 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     off += round_up((uint32_t)S * scr_per_stage, 128u);
     prm.off_misc = off;
     off += misc_bytes;
+    prm.off_cmb = off;
+    off += round_up(cmb_bytes, 128u);
     prm.off_bar = off;
     off += bar_bytes;
     smem = off;

@@ -9,6 +9,9 @@ inside one group), M = 3 (a zero lane in the MMA), the stack's QKV, O and
 gate/up calls at M = 4 at full size; lane permutation, repeat calls and
 quad == plain bit for bit; a non-finite activation in one lane (that lane's
 outputs NaN, the others unchanged); activations over a wide dynamic range.
+K split over a cluster (the stack's down projection at M = 4, 2 to 4 chunks of
+unequal sizes, groups of 1 to 4 blocks, fewer columns than clusters) with the
+plain, RMSNorm, quad, gated, dual and gated-input forms.
 """
 
 import numpy as np
@@ -154,6 +157,93 @@ def test_lanes_dual(gq4, M, K, N, gs):
         # each output equals the plain call on its matrix bit for bit
         solo = host(gq4.matvec(dev(A), *wdev(w), gs))
         assert np.array_equal(host(C).view(np.uint32), solo.view(np.uint32)), name
+
+
+# K split over a cluster: each CTA a chunk of whole groups, rank 0 adds the
+# chunks' sums (K past 36 blocks, or more than 32 groups per column)
+SPLIT_CASES = [
+    # M, K, N, gs
+    (4, 11008, 4096, 128),   # the stack's down projection at M = 4 (4 chunks)
+    (2, 4736, 37, 128),      # 37 groups: 2 chunks of 18 and 19, ragged tiles
+    (3, 8192, 300, 256),     # 3 chunks of 10, 11 and 11 groups of two blocks
+    (4, 16384, 64, 512),     # 4 chunks of 8 groups of four blocks (3 blocks per warp)
+    (2, 5120, 5, 128),       # fewer columns than clusters
+]
+
+
+@pytest.mark.parametrize("M,K,N,gs", SPLIT_CASES)
+def test_lanes_split_matvec(gq4, M, K, N, gs):
+    w = I.quant_weights(K, N, gs, 1711, M, K, N)
+    A = I.activations(M, K, 1711, M, K, N)
+    ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+    out = Guarded((M, N))
+    gq4.matvec(dev(A), *wdev(w), gs, C=out.t)
+    out.check()
+    check_close(f"lanes split matvec M{M} K{K} N{N} gs{gs}", host(out.t), ref, tol_fp32(S))
+    # repeatable to the bit, and lane m equals a two-lane call on row m
+    again = host(gq4.matvec(dev(A), *wdev(w), gs))
+    assert np.array_equal(again.view(np.uint32), host(out.t).view(np.uint32))
+    pair = host(gq4.matvec(dev(np.ascontiguousarray(A[[M - 1, 0]])), *wdev(w), gs))
+    assert np.array_equal(pair[0].view(np.uint32), host(out.t)[M - 1].view(np.uint32))
+
+
+def test_lanes_split_norm_quad(gq4):
+    """RMSNorm prologue (square sums over the chunks) with quad routing, K = 5120 (40 groups)."""
+    M, K, N, gs = 4, 5120, 400, 128
+    w = I.quant_weights(K, N, gs, 1712, M, K, N)
+    A = I.activations(M, K, 1712, M, K, N)
+    A_b = I.activations(M, K, 1713, M, K, N)
+    W = I.norm_gain(K, 1712, M, K)
+    C_ref, S, res_ref, nout_ref = oracle.norm_matvec(A, A_b, W, 1e-6, w.Bq, w.scales, w.zeros, K, N, gs)
+    C, res, nout = Guarded((M, N)), Guarded((M, K)), Guarded((M, K))
+    gq4.norm_matvec(dev(A), *wdev(w), gs, dev(W), 1e-6, A_b=dev(A_b), residual_out=res.t,
+                    norm_out=nout.t, C=C.t)
+    for g in (C, res, nout):
+        g.check()
+    check_close("lanes split norm C", host(C.t), C_ref, tol_fp32(S))
+    assert np.array_equal(host(res.t).view(np.uint32), res_ref.view(np.uint32)), "residual_out"
+    check_close("lanes split norm_out", host(nout.t), nout_ref, 1e-5 * np.abs(nout_ref) + 1e-7)
+    n0, n1, n2 = 100, 250, 333
+    outs_ref, sabs = oracle.quad_matvec(A, w.Bq, w.scales, w.zeros, K, N, gs, n0, n1, n2)
+    lens = [n0, n1 - n0, n2 - n1, N - n2]
+    outs = [Guarded((M, n)) for n in lens]
+    gq4.quad_matvec(dev(A), *wdev(w), gs, n0, n1, n2, outs=[o.t for o in outs])
+    for i, o in enumerate(outs):
+        o.check()
+        check_close(f"lanes split quad out{i}", host(o.t), outs_ref[i], tol_fp32(sabs[i]))
+
+
+@pytest.mark.parametrize("use_norm", [True, False])
+def test_lanes_split_gated(gq4, use_norm):
+    M, K, N, gs = 3, 5120, 70, 128
+    wg = I.quant_weights(K, N, gs, 1714, M, K, N, scale_range=I.SCALE_RANGE_GATED)
+    wu = I.quant_weights(K, N, gs, 1715, M, K, N, scale_range=I.SCALE_RANGE_GATED)
+    A = I.activations(M, K, 1714, M, K, N)
+    kw, dkw = {}, {}
+    if use_norm:
+        kw = dict(A_b=I.activations(M, K, 1715, M, K, N), W_norm=I.norm_gain(K, 1714, M, K), eps=1e-6)
+        dkw = dict(A_b=dev(kw["A_b"]), W_norm=dev(kw["W_norm"]), eps=1e-6)
+    ref = oracle.gated_matvec(A, wg.Bq, wg.scales, wg.zeros, wu.Bq, wu.scales, wu.zeros, K, N, gs, **kw)
+    out = Guarded((M, N))
+    gq4.gated_matvec(dev(A), *wdev(wg), *wdev(wu), gs, out=out.t, **dkw)
+    out.check()
+    tol = tol_gated(ref["g"], ref["u"], ref["Sg"], ref["Su"], ref["out"])
+    check_close(f"lanes split gated norm={use_norm}", host(out.t), ref["out"], tol)
+
+
+def test_lanes_split_dual_and_gated_input(gq4):
+    M, K, N, gs = 4, 6144, 90, 128
+    w0 = I.quant_weights(K, N, gs, 1716, M, K, N, 0)
+    w1 = I.quant_weights(K, N, gs, 1716, M, K, N, 1)
+    A = I.activations(M, K, 1716, M, K, N)
+    C0, C1 = gq4.dual_matvec(dev(A), *wdev(w0), *wdev(w1), gs)
+    for name, C, w in (("C0", C0, w0), ("C1", C1, w1)):
+        ref, S = oracle.matvec(A, w.Bq, w.scales, w.zeros, K, N, gs)
+        check_close(f"lanes split dual {name}", host(C), ref, tol_fp32(S))
+    G = I.activations(M, K, 1717, M, K, N)
+    C = host(gq4.swiglu_gated_matvec(dev(A), dev(G), *wdev(w0), gs))
+    ref, S, _ = oracle.gated_input_matvec("swiglu", A, G, w0.Bq, w0.scales, w0.zeros, K, N, gs)
+    check_close("lanes split gated input", C, ref, tol_fp32(S))
 
 
 @pytest.mark.parametrize("kind", ["sigmoid", "swiglu"])
