@@ -32,23 +32,34 @@
 //     comes off through S).
 //
 // Decomposition:
-//   * Persistent grid, one CTA per SM, a contiguous range of whole columns per
-//     CTA; 8 consumer warps, a producer warp and a helper warp.
+//   * Persistent grid of thread-block clusters, one CTA per SM; 12 consumer
+//     warps, a producer warp and a helper warp per CTA.  Two cluster forms:
+//     - CTA pairs (K up to 36 blocks, at most 32 groups): each CTA owns a
+//       contiguous range of whole columns and stages half of K's activations,
+//       storing them into its own and its partner's shared memory;
+//     - split K (longer K): the 2-4 CTAs of a cluster own the same columns,
+//       each a chunk of whole scale groups of K, and rank 0 adds the others'
+//       per-stage partial sums (sent through distributed shared memory) in
+//       rank order before the epilogue.
 //   * The producer streams the codes through a ring of S stages.  A stage is
 //     one MMA tile: 16 columns (8 gate and 8 up columns for gate/up, 8 and 8
-//     of the two matrices for dual), fetched as two bulk copies of 8 whole
-//     columns into two regions whose bases differ by 64 bytes mod 128, so
-//     that MMA rows g and g + 1 (lanes 4g.. and 4g+4..) read disjoint bank
-//     halves.  Stages beyond the ring are prefetched into L2.
-//   * The helper warp writes each stage's scale scratch ({s, z} per
-//     group and MMA row, read from global memory, laid out for conflict-free
-//     reads) and adds each stage's 8 partial sums in warp order, applies the
-//     norm's inverse RMS and the epilogue, and writes the outputs.
-//   * The consumer warps split each stage's K into 8 slices of whole 128-code
-//     blocks; per stage a warp waits for the codes and the scratch, runs its
-//     blocks, releases the ring entry and posts its partials to the ring
-//     entry's buffer.  A ring entry's scratch and partial buffer are rewritten
-//     for stage i only after the helper has summed stage i - S.
+//     of the two matrices for dual), fetched as bulk copies (two runs of 8
+//     whole columns, or one copy per column chunk when K is split) into two
+//     regions whose bases differ by 64 bytes mod 128, so that MMA rows g and
+//     g + 1 (lanes 4g.. and 4g+4..) read disjoint bank halves.  Stages beyond
+//     the ring are prefetched into L2.
+//   * The helper warp fills each stage's scale scratch ({s, z} per group and
+//     MMA row, laid out for conflict-free reads) by 4-byte cp.async straight
+//     from global memory, completing on the stage's mbarrier, so that the
+//     scales' round trip under the weight stream never paces the loop; and
+//     adds each stage's 12 partial sums in warp order, applies the norm's
+//     inverse RMS and the epilogue, and writes the outputs.
+//   * The consumer warps split each stage's K into 12 slices of whole 128-code
+//     blocks (at most 3 per warp, held in registers as MMA B fragments); per
+//     stage a warp waits for the codes and the scratch, runs its blocks,
+//     releases the ring entry and posts its partials to the ring entry's
+//     buffer.  A ring entry's scratch and partial buffer are rewritten for
+//     stage i only after the helper has summed stage i - S.
 //   * Programmatic dependent launch as in the one-lane kernel: the producer
 //     and the helper read weights before the dependency wait, the consumers
 //     wait before reading activations; a kernel signals its dependents at its
@@ -185,6 +196,19 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t r
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
                  ::"r"(raddr), "f"(v), "r"(rbar) : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned).
+__device__ __forceinline__ void lanes_cp_async_4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void lanes_cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Arrive on an mbarrier of a CTA of the cluster (address from lanes_mapa).
@@ -384,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             for (int s = 0; s < p.S; ++s) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
-                mbar_init(&sfull[s], 1);
+                mbar_init(&sfull[s], 32);  // the helper lanes' cp.async arrivals
                 mbar_init(&pbar[s], kConsumerWarps);
                 s_seq[s] = -1;
             }
@@ -494,14 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
 
     // =====================================================================
     // Helper warp.  Per stage i, after the sum of stage i - S (whose scratch
-    // and partial buffer share ring entry i mod S): the scale scratch of stage
-    // i, {s, z} per [group][MMA row], read from global memory
+    // and partial buffer share ring entry i mod S): the copies of stage i's
+    // scale scratch, {s, z} per [group][MMA row], from global memory
     // (the scales are weights: no dependency wait).  The sum of a stage adds
-    // the 8 consumer warps' partials in warp order, applies the norm's
-    // inverse RMS and writes the outputs (its lane l mirrors consumer lane l:
-    // MMA rows g and g + 8, decode lane t).  The consumers of stage i wait for
-    // its scratch, so they write stage i's partials only after the sum of
-    // stage i - S has read the buffer.
+    // the 12 consumer warps' partials in warp order (split K: then the other
+    // ranks' sums in rank order, in rank 0), applies the norm's inverse RMS
+    // and writes the outputs (its lane l mirrors consumer lane l: MMA rows g
+    // and g + 8, decode lane t).  The consumers of stage i wait for its
+    // scratch, so they write stage i's partials only after the sum of stage
+    // i - S has read the buffer.
     // =====================================================================
     if (warp == kHelperWarp) {
         lanes_cluster_arrive();
@@ -515,26 +540,33 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         const uint32_t cmb_r0 = split ? lanes_mapa(smem_addr(smem + p.off_cmb), 0u) : 0u;
         const uint32_t cfull_r0 = split ? lanes_mapa(smem_addr(cfull), 0u) : 0u;
         bool hfail = false;
-        // the scale and zero of stage i's 16 MMA rows, lane = group of this
-        // CTA's chunk (at most 32 groups)
-        auto load_scales = [&](int i, float (&sv)[16], float (&zv)[16]) {
+        // Stage i's scale scratch, {s, z} per [group = lane][MMA row] of this
+        // CTA's chunk (at most 32 groups), copied straight from global memory
+        // by 4-byte cp.async; each lane's copies arrive on sfull when they
+        // land (32 arrivals), so the helper never waits for the scales.
+        auto copy_scales = [&](int i) {
+            const int slot = i % p.S;
+            float *scr = reinterpret_cast<float *>(smem + p.off_scr) + (size_t)slot * p.Gs * 32;
             const int lc0 = i * TCOLS;
-            const bool ok = lane < GL;
+            if (lane < GL) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                int m, lc;
-                if constexpr (NMAT == 2) {
-                    m = r & 1;
-                    lc = lc0 + (r >> 1);
-                } else {
-                    m = 0;
-                    lc = lc0 + 8 * (r & 1) + (r >> 1);
+                for (int r = 0; r < 16; ++r) {
+                    int m, lc;
+                    if constexpr (NMAT == 2) {
+                        m = r & 1;
+                        lc = lc0 + (r >> 1);
+                    } else {
+                        m = 0;
+                        lc = lc0 + 8 * (r & 1) + (r >> 1);
+                    }
+                    lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
+                    const size_t si = (size_t)(col_begin + lc) * p.G + g_lo + lane;
+                    float *d = scr + (lane * 16 + r) * 2;
+                    lanes_cp_async_4(d, p.scales[m] + si);
+                    lanes_cp_async_4(d + 1, p.zeros[m] + si);
                 }
-                lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
-                const size_t si = (size_t)(col_begin + lc) * p.G + g_lo + lane;
-                sv[r] = ok ? __ldg(p.scales[m] + si) : 0.0f;
-                zv[r] = ok ? __ldg(p.zeros[m] + si) : 0.0f;
             }
+            lanes_cp_async_arrive(&sfull[slot]);
         };
         // the sum of stage j's partials and its outputs
         auto reduce_stage = [&](int j) {
@@ -621,28 +653,13 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 }
             }
         };
-        // one step: the loads of stage i + 1 go out first, then the sum of
-        // stage i - S (freeing ring entry i mod S), then stage i's scratch
-        auto step = [&](int i, float (&sv)[16], float (&zv)[16], float (&sn)[16], float (&zn)[16]) {
-            if (i + 1 < n_stages) load_scales(i + 1, sn, zn);
+        // per step: the sum of stage i - S (freeing ring entry i mod S), then
+        // the copies of stage i's scratch into that entry
+        for (int i = 0; i < n_stages + p.S; ++i) {
             if (i >= p.S) reduce_stage(i - p.S);
-            if (i < n_stages) {
-                const int slot = i % p.S;
-                float2 *scr = reinterpret_cast<float2 *>(smem + p.off_scr) + (size_t)slot * p.Gs * 16;
-                if (lane < GL) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) scr[lane * 16 + r] = make_float2(sv[r], zv[r]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sfull[slot]);
-            }
-        };
-        float s0[16], z0[16], s1[16], z1[16];
-        if (n_stages > 0) load_scales(0, s0, z0);
-        for (int i = 0; i < n_stages + p.S; i += 2) {
-            step(i, s0, z0, s1, z1);
-            if (i + 1 < n_stages + p.S) step(i + 1, s1, z1, s0, z0);
+            if (i < n_stages) copy_scales(i);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no copy of this warp in flight at exit
         if (split && crank != 0 && !hfail) {
             // rank 0's last remote arrives have landed here before this CTA exits
             for (int j = max(0, n_stages - kCombine); j < n_stages; ++j) {
@@ -660,8 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // =====================================================================
     // Consumer warps: prologue.  One warp load instruction reads one 128-
     // activation block of one lane (lane l: activations 4l .. 4l + 3), so the
-    // loads are fully coalesced.  A warp takes 4 k-blocks of every lane per
-    // pass (U = 4 NP units), all its loads issued before any is used (one
+    // loads are fully coalesced.  A warp takes 2 k-blocks of every lane per
+    // pass (U = 2 NP units), all its loads issued before any is used (one
     // round trip under the weight stream); the loop bounds are uniform per
     // warp.  Per unit: the block's largest magnitude and sums are reduce-
     // scattered over the warp, the scales gathered back from the unit's owner
