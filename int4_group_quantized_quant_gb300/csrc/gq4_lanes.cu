@@ -33,7 +33,8 @@
 //
 // Decomposition:
 //   * Persistent grid of thread-block clusters, one CTA per SM; 12 consumer
-//     warps, a producer warp and a helper warp per CTA.  Two cluster forms:
+//     warps, a producer warp, a helper warp and a scale warp per CTA.  Two
+//     cluster forms:
 //     - CTA pairs (K up to 36 blocks, at most 32 groups): each CTA owns a
 //       contiguous range of whole columns and stages half of K's activations,
 //       storing them into its own and its partner's shared memory;
@@ -48,20 +49,21 @@
 //     regions whose bases differ by 64 bytes mod 128, so that MMA rows g and
 //     g + 1 (lanes 4g.. and 4g+4..) read disjoint bank halves.  Stages beyond
 //     the ring are prefetched into L2.
-//   * The helper warp fills each stage's scale scratch ({s, z} per group and
-//     MMA row, laid out for conflict-free reads) by 4-byte cp.async straight
-//     from global memory, completing on the stage's mbarrier, so that the
-//     scales' round trip under the weight stream never paces the loop; and
-//     adds each stage's 12 partial sums in warp order, applies the norm's
-//     inverse RMS and the epilogue, and writes the outputs.
+//   * A scale warp fills each stage's scale scratch ({s, z} per MMA row and
+//     group, laid out for conflict-free reads) by 16-, 8- or 4-byte cp.async
+//     straight from global memory as soon as the ring entry is free,
+//     completing on the stage's mbarrier, so that no warp waits for the
+//     scales' round trip under the weight stream.
+//   * The helper warp adds each stage's 12 partial sums in warp order,
+//     applies the norm's inverse RMS and the epilogue, and writes the
+//     outputs.
 //   * The consumer warps split each stage's K into 12 slices of whole 128-code
 //     blocks (at most 3 per warp, held in registers as MMA B fragments); per
 //     stage a warp waits for the codes and the scratch, runs its blocks,
 //     releases the ring entry and posts its partials to the ring entry's
-//     buffer.  A ring entry's scratch and partial buffer are rewritten for
-//     stage i only after the helper has summed stage i - S.
+//     buffer (once the helper has read stage i - S's from it).
 //   * Programmatic dependent launch as in the one-lane kernel: the producer
-//     and the helper read weights before the dependency wait, the consumers
+//     reads weights (codes, scales) before the dependency wait, the consumers
 //     wait before reading activations; a kernel signals its dependents at its
 //     last stage.
 //   * Every mbarrier wait is bounded in time; on expiry the kernel records an
@@ -89,8 +91,9 @@ namespace {
 
 constexpr int kConsumerWarps = 12;
 constexpr int kProducerWarp = kConsumerWarps;      // bulk copies of the codes
-constexpr int kHelperWarp = kConsumerWarps + 1;    // scale scratch, cross-warp sums, outputs
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kHelperWarp = kConsumerWarps + 1;    // cross-warp sums, outputs
+constexpr int kScaleWarp = kConsumerWarps + 2;     // scale scratch copies
+constexpr int kThreads = (kConsumerWarps + 3) * 32;
 constexpr int kBar2Threads = (kConsumerWarps + 1) * 32;  // consumers + producer
 constexpr int kCT = kConsumerWarps * 32;
 constexpr int kMaxStages = 16;
@@ -102,6 +105,16 @@ constexpr int kMaxSplit = 4;        // K chunks per cluster when K is split
 constexpr int kCombine = 4;         // stages of partial sums in flight to a cluster's rank 0
 constexpr int kSplitWarpBlocks = 2; // preferred blocks per consumer warp when K is split
 constexpr uint32_t kSmemLimit = 226u * 1024u;  // of the 227 KB a block may opt in to
+
+// First scale group of K chunk r of ks (r = ks: G).  Inner bounds fall on
+// multiples of 4 groups when G is, else of 2 when G is even, so that the
+// chunk's scale rows start 16- (8-) byte aligned for the scale copies.
+__host__ __device__ __forceinline__ int chunk_group(int G, int ks, int r)
+{
+    if (r >= ks) return G;
+    const int a = (G & 3) == 0 ? 4 : (G & 1) == 0 ? 2 : 1;
+    return (int)((long long)G * r / ks) / a * a;
+}
 
 struct LanesParams {
     int M, K, N, gs;
@@ -202,6 +215,23 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t r
 __device__ __forceinline__ void lanes_cp_async_4(void *dst, const void *src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// 8-byte asynchronous copy global -> shared (both 8-byte aligned) of the
+// first `bytes` (4 or 8) of the source; a short copy zero-fills the rest.
+__device__ __forceinline__ void lanes_cp_async_8(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned) of the
+// first `bytes` (4..16) of the source; the rest of the 16 destination bytes
+// are zero-filled.
+__device__ __forceinline__ void lanes_cp_async_16(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(bytes)
+                 : "memory");
 }
 
 // Arrive on `bar` once every cp.async this thread issued so far has landed
@@ -350,9 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // codes of a stage landed
     uint64_t *empty = full + kMaxStages;   // the consumer warps are done with a ring entry
-    uint64_t *sfull = empty + kMaxStages;  // the helper wrote a ring entry's scale scratch
+    uint64_t *sfull = empty + kMaxStages;  // a ring entry's scale scratch landed
     uint64_t *pbar = sfull + kMaxStages;   // the consumer warps wrote a ring entry's partials
-    uint64_t *aload = pbar + kMaxStages;   // the consumer warps' activation loads returned
+    uint64_t *pfree = pbar + kMaxStages;   // the helper has read a ring entry's partials
+    uint64_t *aload = pfree + kMaxStages;  // the consumer warps' activation loads returned
     uint64_t *peerb = aload + 1;           // the partner CTA's half of the staging landed
     uint64_t *cfull = peerb + 1;           // [kCombine] split K: the other ranks' partials landed
     uint64_t *cfree = cfull + kCombine;    // [kCombine] split K: rank 0 has read a combine entry
@@ -386,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int ncols = col_end > col_begin ? col_end - col_begin : 0;
     const int n_stages = (ncols + TCOLS - 1) / TCOLS;
     // this CTA's groups [g_lo, g_lo + GL) and blocks [kbc0, kbc0 + KBL) of K
-    const int g_lo = split ? (int)((long long)p.G * crank / p.ks) : 0;
-    const int GL = split ? (int)((long long)p.G * (crank + 1) / p.ks) - g_lo : p.G;
+    const int g_lo = split ? chunk_group(p.G, p.ks, (int)crank) : 0;
+    const int GL = split ? chunk_group(p.G, p.ks, (int)crank + 1) - g_lo : p.G;
     const int kbc0 = g_lo * p.bpg;
     const int KBL = GL * p.bpg;
     const uint32_t cb = (uint32_t)KBL * 64u;  // a column's codes in a stage (bytes)
@@ -401,15 +432,17 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     const int kb_peer = split ? 0 : (crank ? kb_half : KBL - kb_half);  // blocks the partner stages
 
     // =====================================================================
-    // Producer warp.
+    // Producer warp: lane 0 the bulk copies of the codes and the L2
+    // prefetches.
     // =====================================================================
     if (warp == kProducerWarp) {
         if (lane == 0) {
             for (int s = 0; s < p.S; ++s) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
-                mbar_init(&sfull[s], 32);  // the helper lanes' cp.async arrivals
+                mbar_init(&sfull[s], 32);  // the producer lanes' cp.async arrivals
                 mbar_init(&pbar[s], kConsumerWarps);
+                mbar_init(&pfree[s], 1);
                 s_seq[s] = -1;
             }
             mbar_init(aload, kConsumerWarps);
@@ -424,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         lanes_cluster_arrive();  // after the initialisation: the cluster may now use peerb, cfull, cfree
         lanes_bar_arrive(4, kBar2Threads);  // the consumers' first mbarrier use (aload)
         lanes_bar_arrive(2, kBar2Threads);  // the consumers' barrier after their prologue
-        lanes_bar_arrive(3, 64);            // the helper's
-        if (lane == 0) {
+        lanes_bar_arrive(3, 96);            // the helper's and the scale warp's
+        {
             int issued = 0;
             bool ok = true;
             // the codes of stage i as (first column, count) per region
@@ -452,38 +485,39 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             int pf = 3;  // next stage to prefetch
             for (int i = 0; ok && i < n_stages; ++i) {
                 const int slot = i % p.S;
-                if (i == 2 && !mbar_wait(aload, 0)) {
-                    lanes_error();
+                // a ring entry (codes and scale scratch) is refilled once
+                // every consumer warp is done with it
+                bool w = i != 2 || mbar_wait(aload, 0);
+                w = w && (i < p.S || mbar_wait(&empty[slot], ((i / p.S) - 1) & 1));
+                if (!__all_sync(0xffffffffu, w)) {
+                    if (lane == 0) lanes_error();
                     ok = false;
                     break;
                 }
-                if (i >= p.S && !mbar_wait(&empty[slot], ((i / p.S) - 1) & 1)) {
-                    lanes_error();
-                    ok = false;
-                    break;
-                }
-                int rc[2], rn[2];  // first column and count of each region
-                stage_regions(i, rc, rn);
-                unsigned char *dst = smem + (size_t)slot * p.stage_bytes;
-                s_seq[slot] = i;  // published by the release of the arrive below
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)(rn[0] + rn[1]) * cb);
+                if (lane == 0) {
+                    int rc[2], rn[2];  // first column and count of each region
+                    stage_regions(i, rc, rn);
+                    unsigned char *dst = smem + (size_t)slot * p.stage_bytes;
+                    s_seq[slot] = i;  // published by the release of the arrive below
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(rn[0] + rn[1]) * cb);
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (rn[r] == 0) continue;
-                    const int m = NMAT == 2 ? r : 0;
-                    const uint4 *src = p.Bq[m] + (size_t)rc[r] * (p.KW / 4);
-                    if (!split) {
-                        // whole columns: one run
-                        bulk_g2s(dst + (r ? off_reg1 : 0u), src, (uint32_t)rn[r] * cb, &full[slot]);
-                    } else {
-                        // the chunk of each column (16-byte aligned: 64 bytes a block)
-                        for (int q = 0; q < rn[r]; ++q)
-                            bulk_g2s(dst + (r ? off_reg1 : 0u) + (uint32_t)q * cb,
-                                     src + (size_t)q * (p.KW / 4) + (size_t)kbc0 * 4, cb, &full[slot]);
+                    for (int r = 0; r < 2; ++r) {
+                        if (rn[r] == 0) continue;
+                        const int m = NMAT == 2 ? r : 0;
+                        const uint4 *src = p.Bq[m] + (size_t)rc[r] * (p.KW / 4);
+                        if (!split) {
+                            // whole columns: one run
+                            bulk_g2s(dst + (r ? off_reg1 : 0u), src, (uint32_t)rn[r] * cb, &full[slot]);
+                        } else {
+                            // the chunk of each column (16-byte aligned: 64 bytes a block)
+                            for (int q = 0; q < rn[r]; ++q)
+                                bulk_g2s(dst + (r ? off_reg1 : 0u) + (uint32_t)q * cb,
+                                         src + (size_t)q * (p.KW / 4) + (size_t)kbc0 * 4, cb, &full[slot]);
+                        }
                     }
                 }
                 issued = i + 1;
-                if (i >= 2) {
+                if (lane == 0 && i >= 2) {
                     for (; pf < n_stages && pf <= i + kPrefetchAhead; ++pf) {
                         int pc[2], pn[2];
                         stage_regions(pf, pc, pn);
@@ -505,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 // leave no copy in flight into this CTA's shared memory
                 for (int i = (issued > p.S ? issued - p.S : 0); i < issued; ++i)
                     (void)mbar_wait(&full[i % p.S], (i / p.S) & 1);
@@ -517,40 +551,40 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     }
 
     // =====================================================================
-    // Helper warp.  Per stage i, after the sum of stage i - S (whose scratch
-    // and partial buffer share ring entry i mod S): the copies of stage i's
-    // scale scratch, {s, z} per [group][MMA row], from global memory
-    // (the scales are weights: no dependency wait).  The sum of a stage adds
-    // the 12 consumer warps' partials in warp order (split K: then the other
-    // ranks' sums in rank order, in rank 0), applies the norm's inverse RMS
-    // and writes the outputs (its lane l mirrors consumer lane l: MMA rows g
-    // and g + 8, decode lane t).  The consumers of stage i wait for its
-    // scratch, so they write stage i's partials only after the sum of stage
-    // i - S has read the buffer.
+    // Scale warp: each stage's scale scratch, as soon as its ring entry is
+    // free (the consumer warps are done with stage i - S).
     // =====================================================================
-    if (warp == kHelperWarp) {
+    if (warp == kScaleWarp) {
         lanes_cluster_arrive();
-        lanes_bar(3, 64);  // the producer has initialised the mbarriers
-        const int g = lane >> 2, t = lane & 3;
-        const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
-        const bool lane_ok = t < p.M;
-        const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [S][warps][32]
-        // split K: rank 0's [kCombine][kMaxSplit - 1][32] partial sums of the other ranks
-        const float2 *cmb = reinterpret_cast<const float2 *>(smem + p.off_cmb);
-        const uint32_t cmb_r0 = split ? lanes_mapa(smem_addr(smem + p.off_cmb), 0u) : 0u;
-        const uint32_t cfull_r0 = split ? lanes_mapa(smem_addr(cfull), 0u) : 0u;
-        bool hfail = false;
-        // Stage i's scale scratch, {s, z} per [group = lane][MMA row] of this
-        // CTA's chunk (at most 32 groups), copied straight from global memory
-        // by 4-byte cp.async; each lane's copies arrive on sfull when they
-        // land (32 arrivals), so the helper never waits for the scales.
+        lanes_bar(3, 96);  // the producer has initialised the mbarriers
+        // Stage i's scale scratch: the scales, then the zeros, of this CTA's
+        // groups (at most 32) for each of the 16 MMA rows, 32 floats a row;
+        // the 4-group piece c of row r sits at piece c ^ (r & 7), so the 8
+        // rows a load instruction reads fall in distinct banks.  Copied
+        // straight from global memory by cp.async, 16 bytes (4 groups) at a
+        // time where the rows allow it; each lane's copies arrive on sfull
+        // when they land (32 arrivals), so no warp waits for the scales'
+        // round trip under the weight stream.
+        const int nch = (GL + 3) >> 2;  // 4-group pieces per row (at most 8)
+        // floats per copy: 4 where every row's piece starts 16-byte aligned,
+        // 2 where 8-byte, else 1
+        uintptr_t align = 0;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+            align |= reinterpret_cast<uintptr_t>(p.scales[m]) | reinterpret_cast<uintptr_t>(p.zeros[m]);
+        const int vec = ((p.G | g_lo) & 3) == 0 && (align & 15u) == 0 ? 4
+                        : ((p.G | g_lo) & 1) == 0 && (align & 7u) == 0 ? 2 : 1;
         auto copy_scales = [&](int i) {
             const int slot = i % p.S;
-            float *scr = reinterpret_cast<float *>(smem + p.off_scr) + (size_t)slot * p.Gs * 32;
+            float *scr = reinterpret_cast<float *>(smem + p.off_scr) + (size_t)slot * 32 * 32;
             const int lc0 = i * TCOLS;
-            if (lane < GL) {
+            // lane: piece c = lane & 7 of MMA rows (lane >> 3) + 4 k, k = 0..3
+            const int c = lane & 7;
+            if (c < nch) {
+                const int n = min(4, GL - 4 * c);
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
+                for (int k = 0; k < 4; ++k) {
+                    const int r = (lane >> 3) + 4 * k;  // MMA row
                     int m, lc;
                     if constexpr (NMAT == 2) {
                         m = r & 1;
@@ -560,14 +594,60 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                         lc = lc0 + 8 * (r & 1) + (r >> 1);
                     }
                     lc = lc < ncols ? lc : 0;  // past the range: any valid row (discarded)
-                    const size_t si = (size_t)(col_begin + lc) * p.G + g_lo + lane;
-                    float *d = scr + (lane * 16 + r) * 2;
-                    lanes_cp_async_4(d, p.scales[m] + si);
-                    lanes_cp_async_4(d + 1, p.zeros[m] + si);
+                    const size_t off = (size_t)(col_begin + lc) * p.G + g_lo + 4 * c;
+                    float *d = scr + r * 32 + 4 * (c ^ (r & 7));
+#pragma unroll
+                    for (int arr = 0; arr < 2; ++arr) {  // scales, zeros
+                        const float *src = (arr ? p.zeros[m] : p.scales[m]) + off;
+                        float *da = d + arr * 16 * 32;
+                        if (vec == 4) {
+                            lanes_cp_async_16(da, src, 4u * (uint32_t)n);
+                        } else if (vec == 2) {
+                            lanes_cp_async_8(da, src, n >= 2 ? 8u : 4u);
+                            if (n > 2) lanes_cp_async_8(da + 2, src + 2, n >= 4 ? 8u : 4u);
+                        } else {
+                            for (int e = 0; e < n; ++e) lanes_cp_async_4(da + e, src + e);
+                        }
+                    }
                 }
             }
             lanes_cp_async_arrive(&sfull[slot]);
         };
+
+        for (int i = 0; i < n_stages; ++i) {
+            if (i >= p.S &&
+                !__all_sync(0xffffffffu, mbar_wait(&empty[i % p.S], ((i / p.S) - 1) & 1))) {
+                lanes_error();  // the consumers' scratch waits then expire as well
+                break;
+            }
+            copy_scales(i);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no copy of this warp in flight at exit
+        __syncwarp();
+        lanes_cluster_wait();
+        return;
+    }
+
+    // =====================================================================
+    // Helper warp: per stage, in order, the sum of the 12 consumer warps'
+    // partials in warp order (split K: then the other ranks' sums in rank
+    // order, in rank 0), the norm's inverse RMS and the outputs (its lane l
+    // mirrors consumer lane l: MMA rows g and g + 8, decode lane t).  Once it
+    // has read a ring entry's partials it releases the buffer (pfree) for the
+    // consumers' partials of stage i + S.
+    // =====================================================================
+    if (warp == kHelperWarp) {
+        lanes_cluster_arrive();
+        lanes_bar(3, 96);  // the producer has initialised the mbarriers
+        const int g = lane >> 2, t = lane & 3;
+        const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
+        const bool lane_ok = t < p.M;
+        const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [S][warps][32]
+        // split K: rank 0's [kCombine][kMaxSplit - 1][32] partial sums of the other ranks
+        const float2 *cmb = reinterpret_cast<const float2 *>(smem + p.off_cmb);
+        const uint32_t cmb_r0 = split ? lanes_mapa(smem_addr(smem + p.off_cmb), 0u) : 0u;
+        const uint32_t cfull_r0 = split ? lanes_mapa(smem_addr(cfull), 0u) : 0u;
+        bool hfail = false;
         // the sum of stage j's partials and its outputs
         auto reduce_stage = [&](int j) {
             const int slot = j % p.S;
@@ -582,6 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 a0 += v.x;
                 a8 += v.y;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfree[slot]);  // the consumers may rewrite the buffer
             if (split) {
                 // the chunks' sums meet in rank 0, added in rank order
                 const int cs = j % kCombine;
@@ -653,13 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                 }
             }
         };
-        // per step: the sum of stage i - S (freeing ring entry i mod S), then
-        // the copies of stage i's scratch into that entry
-        for (int i = 0; i < n_stages + p.S; ++i) {
-            if (i >= p.S) reduce_stage(i - p.S);
-            if (i < n_stages) copy_scales(i);
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");  // no copy of this warp in flight at exit
+        for (int j = 0; j < n_stages; ++j) reduce_stage(j);
         if (split && crank != 0 && !hfail) {
             // rank 0's last remote arrives have landed here before this CTA exits
             for (int j = max(0, n_stages - kCombine); j < n_stages; ++j) {
@@ -917,7 +993,11 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         }
         const unsigned char *st = smem + (size_t)ring * p.stage_bytes;
         // {s, z} per [group][MMA row] of this stage
-        const float2 *scr = reinterpret_cast<const float2 *>(smem + p.off_scr) + (size_t)ring * p.Gs * 16;
+        // the scales and zeros of MMA rows g and g + 8 in this stage's scratch
+        // (group j at (((j >> 2) ^ g) << 2) | (j & 3) of either row)
+        const float *scr = reinterpret_cast<const float *>(smem + p.off_scr) + (size_t)ring * 32 * 32;
+        const float *sg0 = scr + g * 32, *sg8 = scr + (g + 8) * 32;
+        const float *zg0 = scr + (16 + g) * 32, *zg8 = scr + (24 + g) * 32;
 
         float y0 = 0.0f, y8 = 0.0f;
         if (!failed) {
@@ -934,8 +1014,9 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                     wa[u] = *reinterpret_cast<const uint4 *>(ra + b * 64 + t * 16);
                     wb[u] = *reinterpret_cast<const uint4 *>(ra + row8_delta + b * 64 + t * 16);
                     const int j = b >> p.bpg_shift;
-                    sz0[u] = scr[j * 16 + g];  // {s, z} of row g
-                    sz8[u] = scr[j * 16 + g + 8];
+                    const int js = (((j >> 2) ^ g) << 2) | (j & 3);
+                    sz0[u] = make_float2(sg0[js], zg0[js]);  // {s, z} of row g
+                    sz8[u] = make_float2(sg8[js], zg8[js]);
                 }
                 float d1[NBL][4], d2[NBL][4];
 #pragma unroll
@@ -983,7 +1064,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         // this warp is done with the stage's codes and scratch
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[ring]);
-        // its partial sums go to the helper warp (buffer of this ring entry)
+        // its partial sums go to the helper warp (buffer of this ring entry,
+        // once the helper has read stage i - S's)
+        if (i >= p.S && !failed && !__all_sync(0xffffffffu, mbar_wait(&pfree[ring], ph ^ 1u))) {
+            lanes_error();
+            failed = true;
+        }
         if (failed) y0 = y8 = __int_as_float(0x7fffffff);
         part[((size_t)ring * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
         __syncwarp();
@@ -1100,8 +1186,14 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     // per consumer warp (its activations stay in registers).  All of K in
     // one CTA (pairs) where it fits; else the fewest chunks per cluster that
     // give each warp at most kSplitWarpBlocks blocks (at most kMaxWarpBlocks).
+    auto largest_chunk = [&](int ks) {  // groups
+        int most = 0;
+        for (int r = 0; r < ks; ++r)
+            most = max(most, chunk_group(prm.G, ks, r + 1) - chunk_group(prm.G, ks, r));
+        return most;
+    };
     auto chunk_fits = [&](int ks, int warp_blocks) {
-        const int gmax = (prm.G + ks - 1) / ks;  // the largest chunk's groups
+        const int gmax = largest_chunk(ks);
         return gmax <= 32 && (gmax * prm.bpg + kConsumerWarps - 1) / kConsumerWarps <= warp_blocks;
     };
     int ks = 0;
@@ -1115,7 +1207,7 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
         if (ks == 0) return false;
     }
     prm.ks = ks;
-    prm.Gs = (prm.G + ks - 1) / ks;
+    prm.Gs = largest_chunk(ks);
     const int KBC = prm.Gs * prm.bpg;  // the largest chunk's blocks
     prm.unit = 1;
     prm.n_units = call.N;
@@ -1126,10 +1218,10 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     const uint32_t fx_bytes = (uint32_t)KBC * 4u * 16u;
     const uint32_t misc_bytes = 256u;
     const uint32_t cmb_bytes = ks > 1 ? (uint32_t)kCombine * (kMaxSplit - 1) * 32u * 8u : 0u;
-    const uint32_t bar_bytes = (4 * kMaxStages + 2 + 2 * kCombine) * 8u + kMaxStages * 4u;
+    const uint32_t bar_bytes = (5 * kMaxStages + 2 + 2 * kCombine) * 8u + kMaxStages * 4u;
     // per ring entry: the codes, the scale scratch [Gs][16 rows] {s, z}
     // and the consumer warps' partial sums
-    const uint32_t scr_per_stage = (uint32_t)prm.Gs * 16u * 8u;
+    const uint32_t scr_per_stage = 32u * 32u * 4u;  // 16 rows of scales, 16 of zeros, 32 groups each
     const uint32_t part_per_stage = (uint32_t)kConsumerWarps * 32u * 8u;
     const uint32_t per_stage = stage + scr_per_stage + part_per_stage;
     const uint32_t fixed = act_bytes + fx_bytes + misc_bytes + cmb_bytes + bar_bytes + 4u * 128u;

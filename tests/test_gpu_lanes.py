@@ -165,7 +165,7 @@ SPLIT_CASES = [
     # M, K, N, gs
     (4, 11008, 4096, 128),   # the stack's down projection at M = 4 (4 chunks)
     (2, 4736, 37, 128),      # 37 groups: 2 chunks of 18 and 19, ragged tiles
-    (3, 8192, 300, 256),     # 3 chunks of 10, 11 and 11 groups of two blocks
+    (3, 8192, 300, 256),     # 3 chunks of 8, 12 and 12 groups of two blocks
     (4, 16384, 64, 512),     # 4 chunks of 8 groups of four blocks (3 blocks per warp)
     (2, 5120, 5, 128),       # fewer columns than clusters
 ]
