@@ -778,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // the first cluster writes residual_out (each CTA the blocks it stages)
     const bool cl0 = (int)blockIdx.x < (split ? p.ks : 2);
     constexpr bool TWO = PRO != kProNone;  // A_b (norm) or the gate vector
-    constexpr int U = kPrologueBlocks * NP;
+    constexpr int PB = kPrologueBlocks;  // k-blocks per warp per pass
+    constexpr int U = PB * NP;
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const int par = lane & 1;  // codes 0-3 (0) or 4-7 (1) of word lane >> 1
     const int wsl = lane >> 1;
@@ -805,12 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
                                            : (uint32_t)kb_peer * (uint32_t)NP * (2u * 32u * 8u + 16u) + norm_bytes);
     }
     bool pfail = false;
-    bool arrived = kb_lo + kPrologueBlocks * warp >= kb_hi;  // a warp without k-blocks signals at once
+    bool arrived = kb_lo + PB * warp >= kb_hi;  // a warp without k-blocks signals at once
     if (arrived && lane == 0) mbar_arrive(aload);
-    for (int kb0 = kb_lo + kPrologueBlocks * warp; kb0 < kb_hi; kb0 += kPrologueBlocks * kConsumerWarps) {
-        float4 va[U], vb[U], vg[kPrologueBlocks];
+    for (int kb0 = kb_lo + PB * warp; kb0 < kb_hi; kb0 += PB * kConsumerWarps) {
+        float4 va[U], vb[U], vg[PB];
 #pragma unroll
-        for (int i = 0; i < kPrologueBlocks; ++i) {
+        for (int i = 0; i < PB; ++i) {
             const bool okb = kb0 + i < kb_hi;
             const size_t k0 = (size_t)(kbc0 + kb0 + i) * kBlock + 4 * lane;
 #pragma unroll
