@@ -85,8 +85,8 @@
  *     it non-finite (NaN at M = 1 and on the 2..4-lane kernel below).
  *   - Arithmetic: with 2 <= M <= 4 lanes, a group size that is a power-of-
  *     two multiple of 128 and K a multiple of 128 that splits into at most
- *     four chunks of whole groups, each at most 32 groups and 36 blocks of
- *     128 codes (one chunk up to K = 4608; e.g. K = 11008 at group 128 in
+ *     four chunks of whole groups, each at most 32 groups and 32 blocks of
+ *     128 codes (one chunk up to K = 4096; e.g. K = 11008 at group 128 in
  *     four; the chunks' f32 sums are added in chunk order), each 128-code
  *     block of a lane's activations is held
  *     as 22-bit fixed point with a power-of-two scale (each value within

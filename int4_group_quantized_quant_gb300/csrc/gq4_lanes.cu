@@ -32,10 +32,10 @@
 //     comes off through S).
 //
 // Decomposition:
-//   * Persistent grid of thread-block clusters, one CTA per SM; 12 consumer
+//   * Persistent grid of thread-block clusters, one CTA per SM; 16 consumer
 //     warps, a producer warp, a helper warp and a scale warp per CTA.  Two
 //     cluster forms:
-//     - CTA pairs (K up to 36 blocks, at most 32 groups): each CTA owns a
+//     - CTA pairs (K up to 32 blocks, at most 32 groups): each CTA owns a
 //       contiguous range of whole columns and stages half of K's activations,
 //       storing them into its own and its partner's shared memory;
 //     - split K (longer K): the 2-4 CTAs of a cluster own the same columns,
@@ -54,14 +54,15 @@
 //     straight from global memory as soon as the ring entry is free,
 //     completing on the stage's mbarrier, so that no warp waits for the
 //     scales' round trip under the weight stream.
-//   * The helper warp adds each stage's 12 partial sums in warp order,
+//   * The helper warp adds each stage's 16 partial sums in warp order,
 //     applies the norm's inverse RMS and the epilogue, and writes the
 //     outputs.
-//   * The consumer warps split each stage's K into 12 slices of whole 128-code
-//     blocks (at most 3 per warp, held in registers as MMA B fragments); per
+//   * The consumer warps split each stage's K into 16 slices of whole 128-code
+//     blocks (at most 2 per warp, held in registers as MMA B fragments); per
 //     stage a warp waits for the codes and the scratch, runs its blocks,
-//     releases the ring entry and posts its partials to the ring entry's
-//     buffer (once the helper has read stage i - S's from it).
+//     releases the ring entry and posts its partials to a 2-deep partial
+//     ring (once the helper has read stage i - 2's from it).  96 registers a
+//     thread: 19 warps put 5 on a scheduler.
 //   * Programmatic dependent launch as in the one-lane kernel: the producer
 //     reads weights (codes, scales) before the dependency wait, the consumers
 //     wait before reading activations; a kernel signals its dependents at its
@@ -89,20 +90,23 @@ __device__ unsigned int g_lanes_error = 0;
 
 namespace {
 
-constexpr int kConsumerWarps = 12;
+constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = kConsumerWarps;      // bulk copies of the codes
 constexpr int kHelperWarp = kConsumerWarps + 1;    // cross-warp sums, outputs
 constexpr int kScaleWarp = kConsumerWarps + 2;     // scale scratch copies
 constexpr int kThreads = (kConsumerWarps + 3) * 32;
 constexpr int kBar2Threads = (kConsumerWarps + 1) * 32;  // consumers + producer
 constexpr int kCT = kConsumerWarps * 32;
+// registers per thread: 19 warps put 5 on a scheduler, 5 * 32 * 96 <= 16384
+constexpr int kMaxRegs = 96;
 constexpr int kMaxStages = 16;
 constexpr int kBlock = 128;  // codes per activation block (one scale exponent, one MMA run)
 constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
-constexpr int kMaxWarpBlocks = 3;   // 128-code blocks per consumer warp (K <= 4608)
+constexpr int kMaxWarpBlocks = 2;   // 128-code blocks per consumer warp (K <= 4096 in one CTA)
 constexpr int kPrologueBlocks = 2;  // k-blocks per warp per prologue pass
 constexpr int kMaxSplit = 4;        // K chunks per cluster when K is split
 constexpr int kCombine = 4;         // stages of partial sums in flight to a cluster's rank 0
+constexpr int kPartRing = 2;        // stages of consumer partial sums awaiting the helper
 constexpr int kSplitWarpBlocks = 2; // preferred blocks per consumer warp when K is split
 constexpr uint32_t kSmemLimit = 226u * 1024u;  // of the 227 KB a block may opt in to
 
@@ -375,7 +379,7 @@ using IntC = std::integral_constant<int, V>;
 // NP: lanes per MMA (2 or 4; the N columns are {hi, lo} of each lane).
 // SPLIT: K split over the cluster (p.ks > 1), else CTA pairs.
 template <int NMAT, int PRO, int EPI, int NP, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_constant__ LanesParams p)
+__global__ void __maxnreg__(kMaxRegs) lanes_matvec_kernel(const __grid_constant__ LanesParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bar);  // codes of a stage landed
@@ -440,10 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
             for (int s = 0; s < p.S; ++s) {
                 mbar_init(&full[s], 1);
                 mbar_init(&empty[s], kConsumerWarps);
-                mbar_init(&sfull[s], 32);  // the producer lanes' cp.async arrivals
+                mbar_init(&sfull[s], 32);  // the scale warp lanes' cp.async arrivals
+                s_seq[s] = -1;
+            }
+            for (int s = 0; s < kPartRing; ++s) {
                 mbar_init(&pbar[s], kConsumerWarps);
                 mbar_init(&pfree[s], 1);
-                s_seq[s] = -1;
             }
             mbar_init(aload, kConsumerWarps);
             mbar_init(peerb, 1);  // completed by the partner's stores and one local expect
@@ -629,12 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     }
 
     // =====================================================================
-    // Helper warp: per stage, in order, the sum of the 12 consumer warps'
+    // Helper warp: per stage, in order, the sum of the 16 consumer warps'
     // partials in warp order (split K: then the other ranks' sums in rank
     // order, in rank 0), the norm's inverse RMS and the outputs (its lane l
     // mirrors consumer lane l: MMA rows g and g + 8, decode lane t).  Once it
-    // has read a ring entry's partials it releases the buffer (pfree) for the
-    // consumers' partials of stage i + S.
+    // has read a stage's partials it releases their buffer (pfree) for the
+    // consumers' partials of stage i + kPartRing.
     // =====================================================================
     if (warp == kHelperWarp) {
         lanes_cluster_arrive();
@@ -642,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         const int g = lane >> 2, t = lane & 3;
         const int ci = g >> 1;  // column of row g within its region (row g + 8: ci + 4)
         const bool lane_ok = t < p.M;
-        const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [S][warps][32]
+        const float2 *part = reinterpret_cast<const float2 *>(smem + p.off_part);  // [kPartRing][warps][32]
         // split K: rank 0's [kCombine][kMaxSplit - 1][32] partial sums of the other ranks
         const float2 *cmb = reinterpret_cast<const float2 *>(smem + p.off_cmb);
         const uint32_t cmb_r0 = split ? lanes_mapa(smem_addr(smem + p.off_cmb), 0u) : 0u;
@@ -650,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         bool hfail = false;
         // the sum of stage j's partials and its outputs
         auto reduce_stage = [&](int j) {
-            const int slot = j % p.S;
-            if (!hfail && !__all_sync(0xffffffffu, mbar_wait(&pbar[slot], (j / p.S) & 1))) {
+            const int slot = j % kPartRing;
+            if (!hfail && !__all_sync(0xffffffffu, mbar_wait(&pbar[slot], (j / kPartRing) & 1))) {
                 lanes_error();
                 hfail = true;
             }
@@ -778,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // the first cluster writes residual_out (each CTA the blocks it stages)
     const bool cl0 = (int)blockIdx.x < (split ? p.ks : 2);
     constexpr bool TWO = PRO != kProNone;  // A_b (norm) or the gate vector
-    constexpr int PB = kPrologueBlocks;  // k-blocks per warp per pass
+    constexpr int PB = 4 / NP;  // k-blocks per warp per pass (4 block-lane units)
     constexpr int U = PB * NP;
     const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const int par = lane & 1;  // codes 0-3 (0) or 4-7 (1) of word lane >> 1
@@ -960,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
     // this warp's K slice: blocks [bw0, bw1)
     const int bw0 = (int)((long long)KBL * warp / kConsumerWarps);
     const int bw1 = (int)((long long)KBL * (warp + 1) / kConsumerWarps);
-    float2 *part = reinterpret_cast<float2 *>(smem + p.off_part);  // [S][warps][32]
+    float2 *part = reinterpret_cast<float2 *>(smem + p.off_part);  // [kPartRing][warps][32]
     // MMA rows g and g + 8: region g & 1, columns (g >> 1) and (g >> 1) + 4 of it
     const uint32_t row_off = ((g & 1) ? off_reg1 : 0u) + (uint32_t)(g >> 1) * cb;
     const uint32_t row8_delta = 4u * cb;
@@ -1065,16 +1071,18 @@ __global__ void __launch_bounds__(kThreads, 1) lanes_matvec_kernel(const __grid_
         // this warp is done with the stage's codes and scratch
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[ring]);
-        // its partial sums go to the helper warp (buffer of this ring entry,
-        // once the helper has read stage i - S's)
-        if (i >= p.S && !failed && !__all_sync(0xffffffffu, mbar_wait(&pfree[ring], ph ^ 1u))) {
+        // its partial sums go to the helper warp (partial buffer i mod
+        // kPartRing, once the helper has read stage i - kPartRing's)
+        const int pr_slot = i % kPartRing;
+        if (i >= kPartRing && !failed &&
+            !__all_sync(0xffffffffu, mbar_wait(&pfree[pr_slot], (uint32_t)((i / kPartRing) - 1) & 1u))) {
             lanes_error();
             failed = true;
         }
         if (failed) y0 = y8 = __int_as_float(0x7fffffff);
-        part[((size_t)ring * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
+        part[((size_t)pr_slot * kConsumerWarps + warp) * 32 + lane] = make_float2(y0, y8);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pbar[ring]);
+        if (lane == 0) mbar_arrive(&pbar[pr_slot]);
     }
 
     if constexpr (NORM) {
@@ -1197,14 +1205,17 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
         const int gmax = largest_chunk(ks);
         return gmax <= 32 && (gmax * prm.bpg + kConsumerWarps - 1) / kConsumerWarps <= warp_blocks;
     };
+    // clusters of 2 or 4 before 3 (3-CTA clusters measured slower: they pack
+    // fewer SMs per GPC)
+    constexpr int kSplitOrder[3] = {2, 4, 3};
     int ks = 0;
     if (chunk_fits(1, kMaxWarpBlocks)) {
         ks = 1;
     } else {
-        for (int k = 2; k <= kMaxSplit && ks == 0; ++k)
-            if (chunk_fits(k, kSplitWarpBlocks)) ks = k;
-        for (int k = 2; k <= kMaxSplit && ks == 0; ++k)
-            if (chunk_fits(k, kMaxWarpBlocks)) ks = k;
+        for (int o = 0; o < 3 && ks == 0; ++o)
+            if (kSplitOrder[o] <= kMaxSplit && chunk_fits(kSplitOrder[o], kSplitWarpBlocks)) ks = kSplitOrder[o];
+        for (int o = 0; o < 3 && ks == 0; ++o)
+            if (kSplitOrder[o] <= kMaxSplit && chunk_fits(kSplitOrder[o], kMaxWarpBlocks)) ks = kSplitOrder[o];
         if (ks == 0) return false;
     }
     prm.ks = ks;
@@ -1217,15 +1228,14 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     const uint32_t stage = round_up(reg_bytes + 64u + reg_bytes, 128u);
     const uint32_t act_bytes = (uint32_t)KBC * 4u * (uint32_t)(2 * NP) * 64u;
     const uint32_t fx_bytes = (uint32_t)KBC * 4u * 16u;
-    const uint32_t misc_bytes = 256u;
+    const uint32_t misc_bytes = 384u;  // inverse RMS [4], square sums [warps][4], the others' [3][4]
     const uint32_t cmb_bytes = ks > 1 ? (uint32_t)kCombine * (kMaxSplit - 1) * 32u * 8u : 0u;
     const uint32_t bar_bytes = (5 * kMaxStages + 2 + 2 * kCombine) * 8u + kMaxStages * 4u;
-    // per ring entry: the codes, the scale scratch [Gs][16 rows] {s, z}
-    // and the consumer warps' partial sums
+    // per ring entry: the codes and the scale scratch
     const uint32_t scr_per_stage = 32u * 32u * 4u;  // 16 rows of scales, 16 of zeros, 32 groups each
-    const uint32_t part_per_stage = (uint32_t)kConsumerWarps * 32u * 8u;
-    const uint32_t per_stage = stage + scr_per_stage + part_per_stage;
-    const uint32_t fixed = act_bytes + fx_bytes + misc_bytes + cmb_bytes + bar_bytes + 4u * 128u;
+    const uint32_t part_bytes = (uint32_t)kPartRing * kConsumerWarps * 32u * 8u;  // the partial ring
+    const uint32_t per_stage = stage + scr_per_stage;
+    const uint32_t fixed = act_bytes + fx_bytes + part_bytes + misc_bytes + cmb_bytes + bar_bytes + 4u * 128u;
     if (fixed + 2u * per_stage > kSmemLimit) return false;
     int S = (int)((kSmemLimit - fixed) / per_stage);
     if (S > kMaxStages) S = kMaxStages;
@@ -1237,7 +1247,7 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
     prm.off_fx = off;
     off += round_up(fx_bytes, 128u);
     prm.off_part = off;
-    off += round_up((uint32_t)S * part_per_stage, 128u);
+    off += round_up(part_bytes, 128u);
     prm.off_scr = off;
     off += round_up((uint32_t)S * scr_per_stage, 128u);
     prm.off_misc = off;

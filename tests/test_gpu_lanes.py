@@ -9,8 +9,8 @@ inside one group), M = 3 (a zero lane in the MMA), the stack's QKV, O and
 gate/up calls at M = 4 at full size; lane permutation, repeat calls and
 quad == plain bit for bit; a non-finite activation in one lane (that lane's
 outputs NaN, the others unchanged); activations over a wide dynamic range.
-K split over a cluster (the stack's down projection at M = 4, 2 to 4 chunks of
-unequal sizes, groups of 1 to 4 blocks, fewer columns than clusters) with the
+K split over a cluster (the stack's down projection at M = 4, 2 and 4 chunks,
+of unequal sizes, groups of 1 to 4 blocks, fewer columns than clusters) with the
 plain, RMSNorm, quad, gated, dual and gated-input forms.
 """
 
@@ -165,8 +165,8 @@ SPLIT_CASES = [
     # M, K, N, gs
     (4, 11008, 4096, 128),   # the stack's down projection at M = 4 (4 chunks)
     (2, 4736, 37, 128),      # 37 groups: 2 chunks of 18 and 19, ragged tiles
-    (3, 8192, 300, 256),     # 3 chunks of 8, 12 and 12 groups of two blocks
-    (4, 16384, 64, 512),     # 4 chunks of 8 groups of four blocks (3 blocks per warp)
+    (3, 8192, 300, 256),     # 2 chunks of 16 groups of two blocks
+    (4, 16384, 64, 512),     # 4 chunks of 8 groups of four blocks
     (2, 5120, 5, 128),       # fewer columns than clusters
 ]
 
