@@ -102,6 +102,7 @@ constexpr int kMaxRegs = 96;
 constexpr int kMaxStages = 16;
 constexpr int kBlock = 128;  // codes per activation block (one scale exponent, one MMA run)
 constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
+constexpr int kPreStages = 3;       // stages issued before the consumers' activation loads return
 constexpr int kMaxWarpBlocks = 2;   // 128-code blocks per consumer warp (K <= 4096 in one CTA)
 constexpr int kPrologueBlocks = 2;  // k-blocks per warp per prologue pass
 constexpr int kMaxSplit = 4;        // K chunks per cluster when K is split
@@ -481,19 +482,19 @@ __global__ void __maxnreg__(kMaxRegs) lanes_matvec_kernel(const __grid_constant_
                     rn[1] = nc - rn[0];
                 }
             };
-            // Two stages go out at once; the rest once the consumers'
+            // kPreStages stages go out at once; the rest once the consumers'
             // activation loads have returned (they are not queued behind the
             // weight stream), while the consumers still stage activations.
             // From then on stages up to kPrefetchAhead ahead are prefetched
             // into L2, so a ring entry's refill reads L2 and the weight
             // stream runs through the prologue: more bytes in flight than
             // the ring holds.
-            int pf = 3;  // next stage to prefetch
+            int pf = kPreStages + 1;  // next stage to prefetch
             for (int i = 0; ok && i < n_stages; ++i) {
                 const int slot = i % p.S;
                 // a ring entry (codes and scale scratch) is refilled once
                 // every consumer warp is done with it
-                bool w = i != 2 || mbar_wait(aload, 0);
+                bool w = i != kPreStages || mbar_wait(aload, 0);
                 w = w && (i < p.S || mbar_wait(&empty[slot], ((i / p.S) - 1) & 1));
                 if (!__all_sync(0xffffffffu, w)) {
                     if (lane == 0) lanes_error();
@@ -523,7 +524,7 @@ __global__ void __maxnreg__(kMaxRegs) lanes_matvec_kernel(const __grid_constant_
                     }
                 }
                 issued = i + 1;
-                if (lane == 0 && i >= 2) {
+                if (lane == 0 && i >= kPreStages) {
                     for (; pf < n_stages && pf <= i + kPrefetchAhead; ++pf) {
                         int pc[2], pn[2];
                         stage_regions(pf, pc, pn);
