@@ -104,7 +104,6 @@ constexpr int kBlock = 128;  // codes per activation block (one scale exponent, 
 constexpr int kPrefetchAhead = 16;  // stages prefetched into L2 ahead of the ring copies
 constexpr int kPreStages = 3;       // stages issued before the consumers' activation loads return
 constexpr int kMaxWarpBlocks = 2;   // 128-code blocks per consumer warp (K <= 4096 in one CTA)
-constexpr int kPrologueBlocks = 2;  // k-blocks per warp per prologue pass
 constexpr int kMaxSplit = 4;        // K chunks per cluster when K is split
 constexpr int kCombine = 4;         // stages of partial sums in flight to a cluster's rank 0
 constexpr int kPartRing = 2;        // stages of consumer partial sums awaiting the helper
@@ -760,8 +759,8 @@ __global__ void __maxnreg__(kMaxRegs) lanes_matvec_kernel(const __grid_constant_
     // =====================================================================
     // Consumer warps: prologue.  One warp load instruction reads one 128-
     // activation block of one lane (lane l: activations 4l .. 4l + 3), so the
-    // loads are fully coalesced.  A warp takes 2 k-blocks of every lane per
-    // pass (U = 2 NP units), all its loads issued before any is used (one
+    // loads are fully coalesced.  A warp takes 4 / NP k-blocks of every lane
+    // per pass (U = 4 units), all its loads issued before any is used (one
     // round trip under the weight stream); the loop bounds are uniform per
     // warp.  Per unit: the block's largest magnitude and sums are reduce-
     // scattered over the warp, the scales gathered back from the unit's owner
