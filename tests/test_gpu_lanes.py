@@ -187,9 +187,10 @@ def test_lanes_split_matvec(gq4, M, K, N, gs):
     assert np.array_equal(pair[0].view(np.uint32), host(out.t)[M - 1].view(np.uint32))
 
 
-def test_lanes_split_norm_quad(gq4):
+@pytest.mark.parametrize("M", [2, 4])
+def test_lanes_split_norm_quad(gq4, M):
     """RMSNorm prologue (square sums over the chunks) with quad routing, K = 5120 (40 groups)."""
-    M, K, N, gs = 4, 5120, 400, 128
+    K, N, gs = 5120, 400, 128
     w = I.quant_weights(K, N, gs, 1712, M, K, N)
     A = I.activations(M, K, 1712, M, K, N)
     A_b = I.activations(M, K, 1713, M, K, N)
@@ -213,9 +214,9 @@ def test_lanes_split_norm_quad(gq4):
         check_close(f"lanes split quad out{i}", host(o.t), outs_ref[i], tol_fp32(sabs[i]))
 
 
-@pytest.mark.parametrize("use_norm", [True, False])
-def test_lanes_split_gated(gq4, use_norm):
-    M, K, N, gs = 3, 5120, 70, 128
+@pytest.mark.parametrize("M,use_norm", [(3, True), (3, False), (2, True)])
+def test_lanes_split_gated(gq4, M, use_norm):
+    K, N, gs = 5120, 70, 128
     wg = I.quant_weights(K, N, gs, 1714, M, K, N, scale_range=I.SCALE_RANGE_GATED)
     wu = I.quant_weights(K, N, gs, 1715, M, K, N, scale_range=I.SCALE_RANGE_GATED)
     A = I.activations(M, K, 1714, M, K, N)
@@ -228,7 +229,7 @@ def test_lanes_split_gated(gq4, use_norm):
     gq4.gated_matvec(dev(A), *wdev(wg), *wdev(wu), gs, out=out.t, **dkw)
     out.check()
     tol = tol_gated(ref["g"], ref["u"], ref["Sg"], ref["Su"], ref["out"])
-    check_close(f"lanes split gated norm={use_norm}", host(out.t), ref["out"], tol)
+    check_close(f"lanes split gated M{M} norm={use_norm}", host(out.t), ref["out"], tol)
 
 
 def test_lanes_split_dual_and_gated_input(gq4):
