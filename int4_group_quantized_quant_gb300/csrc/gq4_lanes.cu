@@ -1202,6 +1202,10 @@ bool plan_lanes(const Call &call, LanesParams &prm, size_t &smem, int grid)
         return most;
     };
     auto chunk_fits = [&](int ks, int warp_blocks) {
+        // every chunk holds at least one group (aligned bounds can merge
+        // neighbours when G is small): no empty copies, no idle rank
+        for (int r = 0; r < ks; ++r)
+            if (chunk_group(prm.G, ks, r + 1) <= chunk_group(prm.G, ks, r)) return false;
         const int gmax = largest_chunk(ks);
         return gmax <= 32 && (gmax * prm.bpg + kConsumerWarps - 1) / kConsumerWarps <= warp_blocks;
     };

@@ -168,6 +168,7 @@ SPLIT_CASES = [
     (3, 8192, 300, 256),     # 2 chunks of 16 groups of two blocks
     (4, 16384, 64, 512),     # 4 chunks of 8 groups of four blocks
     (2, 5120, 5, 128),       # fewer columns than clusters
+    (3, 12288, 40, 2048),    # 6 groups of 16 blocks: 3 chunks (4 would leave one empty)
 ]
 
 
